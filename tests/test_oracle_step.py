@@ -1,0 +1,214 @@
+"""Whole-step pins for the CPU oracle at tiny dimensions.
+
+The oracle's decode step is compared with an independent float64 restatement
+written here with torch library routines (F.rms_norm, matmul,
+scaled_dot_product_attention, F.silu, torch's own bf16/e4m3 casts).  The two
+share no code; a mis-wired residual, a norm gain on the wrong vector, a
+transposed head or a wrong KV write position fails these tests.  No GPU."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+
+TINY = synth.Dims(n_layers=2, hidden=64, n_q=4, n_kv=2, head_dim=16, inter=96, n_cb=8,
+                  cb_vocab=1026)
+MAXPOS = 32
+
+
+def dec_bf16(bits):
+    t = torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64)
+
+
+def to_bf16_f64(x: torch.Tensor) -> torch.Tensor:
+    return x.to(torch.bfloat16).to(torch.float64)
+
+
+def fp8_quant(x64: torch.Tensor):
+    x32 = x64.to(torch.float32)
+    s = torch.clamp(x32.abs().amax(), min=1e-12) / 448.0
+    q = (x32 / s).to(torch.float8_e4m3fn)
+    return q.to(torch.float64), s
+
+
+def fp8_weight(W64: torch.Tensor):
+    W32 = W64.to(torch.float32)
+    amax = W32.abs().amax(dim=1)
+    s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (W32 / s[:, None]).to(torch.float8_e4m3fn)
+    return q.to(torch.float64), s
+
+
+class TorchRestatement:
+    """The decode step as written from the model description, in torch float64."""
+
+    def __init__(self, w: synth.Weights, max_pos: int, fp8: bool = False):
+        self.d = w.dims
+        self.fp8 = fp8
+        d = self.d
+        self.E = dec_bf16(w.embed)
+        self.head = dec_bf16(w.head)
+        self.fn = dec_bf16(w.final_norm)
+        self.L = []
+        for l in range(d.n_layers):
+            layer = dict(qkv=dec_bf16(w.wqkv[l]), o=dec_bf16(w.wo[l]), gu=dec_bf16(w.wgu[l]),
+                         d=dec_bf16(w.wd[l]), ln_in=dec_bf16(w.ln_in[l]), ln_post=dec_bf16(w.ln_post[l]),
+                         qn=dec_bf16(w.q_norm[l]), kn=dec_bf16(w.k_norm[l]))
+            if fp8:
+                for key in ("qkv", "o", "gu", "d"):
+                    layer[key + "_q"] = fp8_weight(layer[key])
+            self.L.append(layer)
+        self.K = torch.zeros(d.n_layers, d.n_kv, max_pos, d.head_dim, dtype=torch.float64)
+        self.V = torch.zeros_like(self.K)
+        self.pos, self.t, self.eoc = 0, 0, -1
+
+    def rope(self, x, pos):
+        D = x.shape[-1]
+        i = torch.arange(D // 2, dtype=torch.float64)
+        ang = pos * self.d.rope_theta ** (-2.0 * i / D)
+        c, s = torch.cos(ang), torch.sin(ang)
+        x1, x2 = x[..., : D // 2], x[..., D // 2:]
+        return torch.cat([x1 * c - x2 * s, x2 * c + x1 * s], dim=-1)
+
+    def proj(self, layer, key, a):
+        if not self.fp8:
+            return layer[key] @ a
+        qa, sa = fp8_quant(a)
+        qw, sw = layer[key + "_q"]
+        acc = (qw @ qa).to(torch.float32)
+        return to_bf16_f64(acc * (sa * sw))
+
+    def step(self, codes):
+        d = self.d
+        D, NQ, NKV, I = d.head_dim, d.n_q, d.n_kv, d.inter
+        eps = d.rms_eps
+        h = sum(self.E[k, int(codes[k])] for k in range(d.n_cb))
+        for l, P in enumerate(self.L):
+            a = F.rms_norm(h, (d.hidden,), P["ln_in"], eps)
+            qkv = self.proj(P, "qkv", a)
+            q = qkv[: NQ * D].view(NQ, D)
+            k = qkv[NQ * D:(NQ + NKV) * D].view(NKV, D)
+            v = qkv[(NQ + NKV) * D:].view(NKV, D)
+            q = self.rope(F.rms_norm(q, (D,), P["qn"], eps), self.pos)
+            k = self.rope(F.rms_norm(k, (D,), P["kn"], eps), self.pos)
+            self.K[l, :, self.pos] = to_bf16_f64(k)
+            self.V[l, :, self.pos] = to_bf16_f64(v)
+            Kc = self.K[l, :, : self.pos + 1].repeat_interleave(NQ // NKV, 0)
+            Vc = self.V[l, :, : self.pos + 1].repeat_interleave(NQ // NKV, 0)
+            attn = F.scaled_dot_product_attention(q[:, None, :], Kc, Vc)[:, 0, :].reshape(-1)
+            h = h + self.proj(P, "o", attn)
+            a2 = F.rms_norm(h, (d.hidden,), P["ln_post"], eps)
+            gu = self.proj(P, "gu", a2)
+            m = F.silu(gu[:I]) * gu[I:]
+            if self.fp8:
+                m = to_bf16_f64(m)
+            h = h + self.proj(P, "d", m)
+        f = F.rms_norm(h, (d.hidden,), self.fn, eps)
+        logits = (self.head @ f).view(d.n_cb, d.cb_vocab)
+        out = []
+        for k in range(d.n_cb):
+            am = int(torch.argmax(logits[k]))
+            if self.t < k:
+                c = 1024
+            elif self.eoc >= 0 and self.t >= self.eoc + k:
+                c = 1025
+            else:
+                c = am
+            out.append(c)
+        if self.eoc < 0 and out[0] == 1025:
+            self.eoc = self.t
+        self.pos += 1
+        self.t += 1
+        return np.array(out, np.int32), logits.numpy()
+
+
+def _weights(gamma_variant=True):
+    return synth.make_weights(TINY, std=0.1, gamma_variant=gamma_variant)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_tiny_step_matches_torch_restatement(fp8):
+    w = _weights()
+    orc = oracle.Oracle(w, MAXPOS, precision=1 if fp8 else 0)
+    ref = TorchRestatement(w, MAXPOS, fp8=fp8)
+    codes = synth.random_codes(12, seed=2)
+    orc.set_frame(5)
+    ref.t = 5
+    cin = codes[0]
+    for f in range(12):
+        out, logits, gaps = orc.decode_step(cin)
+        rout, rlogits = ref.step(cin)
+        tol = 1e-9 if not fp8 else 1e-6
+        assert np.allclose(logits, rlogits, rtol=tol, atol=tol), f
+        live = gaps > 1e-6
+        assert np.array_equal(out[live], rout[live]), f
+        cin = out
+    assert orc.pos == 12
+
+
+def test_tiny_step_with_kv_prefix_and_kv_contents():
+    w = _weights(gamma_variant=False)
+    orc = oracle.Oracle(w, MAXPOS)
+    ref = TorchRestatement(w, MAXPOS)
+    k, v = synth.make_kv_prefix(TINY, 9, MAXPOS)
+    orc.set_kv(k, v, 9)
+    ref.K[:, :, :9] = dec_bf16(k[:, :, :9])
+    ref.V[:, :, :9] = dec_bf16(v[:, :, :9])
+    ref.pos = 9
+    cin = synth.random_codes(1, seed=2)[0]
+    out, logits, _ = orc.decode_step(cin)
+    rout, rlogits = ref.step(cin)
+    assert np.allclose(logits, rlogits, rtol=1e-9, atol=1e-9)
+    # the new K/V row went to position 9 in bf16
+    assert np.allclose(dec_bf16(orc.k[:, :, 9]).numpy(), ref.K[:, :, 9].numpy(), rtol=2 ** -7, atol=1e-12)
+    assert np.allclose(dec_bf16(orc.v[:, :, 9]).numpy(), ref.V[:, :, 9].numpy(), rtol=2 ** -7, atol=1e-12)
+    assert not np.array_equal(orc.k[:, :, 9], np.zeros_like(orc.k[:, :, 9]))
+    assert np.array_equal(orc.k[:, :, 10:], np.zeros_like(orc.k[:, :, 10:]))
+
+
+def test_prefill_equals_repeated_steps():
+    w = _weights()
+    codes = synth.delayed_prompt_codes(7)
+    a = oracle.Oracle(w, MAXPOS)
+    a.prefill(codes)
+    b = oracle.Oracle(w, MAXPOS)
+    for p in range(7):
+        b.decode_step(codes[p])
+    b.set_frame(0)
+    assert a.pos == b.pos == 7
+    assert np.array_equal(a.k, b.k) and np.array_equal(a.v, b.v)
+    k_after_prefill, v_after_prefill = a.k.copy(), a.v.copy()
+    nxt = synth.random_codes(1, seed=2, stream=3)[0]
+    oa, la, _ = a.decode_step(nxt)
+    ob, lb, _ = b.decode_step(nxt)
+    assert np.array_equal(la, lb) and np.array_equal(oa, ob)
+    # prefill split in two calls equals one call
+    c = oracle.Oracle(w, MAXPOS)
+    c.prefill(codes[:3])
+    c.prefill(codes[3:])
+    assert np.array_equal(c.k, k_after_prefill) and np.array_equal(c.v, v_after_prefill)
+
+
+def test_prefill_a16_rounds_projection_inputs():
+    """a16 changes the result by bf16-rounding-sized amounts only."""
+    w = _weights()
+    codes = synth.delayed_prompt_codes(5)
+    a = oracle.Oracle(w, MAXPOS)
+    a.prefill(codes, a16=True)
+    b = oracle.Oracle(w, MAXPOS)
+    b.prefill(codes, a16=False)
+    ka, kb = dec_bf16(a.k[:, :, :5]).numpy(), dec_bf16(b.k[:, :, :5]).numpy()
+    assert not np.array_equal(ka, kb)
+    assert np.abs(ka - kb).max() < 0.1
+
+
+def test_oracle_rejects_bad_input():
+    w = _weights()
+    orc = oracle.Oracle(w, MAXPOS)
+    with pytest.raises(ValueError):
+        orc.decode_step(np.array([0, 0, 0, 1026, 0, 0, 0, 0], np.int32))
+    with pytest.raises(ValueError):
+        orc.prefill(np.zeros((MAXPOS + 1, 8), np.int32))
