@@ -1,0 +1,290 @@
+"""Python binding of the GB300 batch-1 TTS decode-step library (libtts_decode.so).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels behind the C ABI declared in ``include/tts_decode.h``.  PyTorch is used
+for device memory and streams.  There is no fallback: importing this package
+raises if the CUDA library has not been built, and every call raises
+``TtsError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtts_decode.so")
+
+TTS_BF16 = 0
+TTS_FP8 = 1
+
+_STATUS = {0: "ok", -1: "bad argument", -2: "code out of range", -3: "context full",
+           -4: "CUDA error", -5: "device error flag set", -6: "not initialised", -7: "unsupported"}
+
+
+class TtsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} -> {status} ({_STATUS.get(status, 'unknown')})")
+        self.status = status
+
+
+class tts_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "inter",
+                 "n_codebooks", "cb_vocab", "max_pos")] + \
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("precision", ctypes.c_int), ("stream", ctypes.c_void_p)]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class tts_weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("head", ctypes.c_void_p), ("final_norm", ctypes.c_void_p)] + \
+               [(n, _PP) for n in ("wqkv", "wo", "wgu", "wd", "sqkv", "so", "sgu", "sd",
+                                   "ln_in", "ln_post", "q_norm", "k_norm")]
+
+
+# Every symbol include/tts_decode.h declares, with its ctypes signature.
+_I, _VP, _F = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+SIGNATURES = {
+    "tts_init": (_I, [ctypes.POINTER(tts_config), ctypes.POINTER(tts_weights), ctypes.POINTER(_VP)]),
+    "tts_shutdown": (_I, [_VP]),
+    "tts_reset": (_I, [_VP]),
+    "tts_prefill": (_I, [_VP, _VP, _I]),
+    "tts_decode_step": (_I, [_VP, _VP, _VP]),
+    "tts_decode_steps": (_I, [_VP, _I, _VP]),
+    "tts_rewind": (_I, [_VP, _I, _I]),
+    "tts_set_kv": (_I, [_VP, _VP, _VP, _I, _I]),
+    "tts_get_kv": (_I, [_VP, _VP, _VP, _I, _I]),
+    "tts_get_logits": (_I, [_VP, _VP]),
+    "tts_get_hidden": (_I, [_VP, _VP]),
+    "tts_set_frame": (_I, [_VP, _I, _I]),
+    "tts_get_state": (_I, [_VP, _VP, _VP, _VP]),
+    "tts_last_steps_ms": (_I, [_VP, _VP]),
+    "tts_time_gemv": (_I, [_VP, _I, _I, _VP]),
+    "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
+    "tts_status_str": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtts_decode.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with "
+                              "`python -m ar_decode_step_gb300.build` (nvcc, sm_103a)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _call(name: str, *args) -> None:
+    rc = getattr(load(), name)(*args)
+    if rc != 0:
+        raise TtsError(name, rc)
+
+
+def status_str(code: int) -> str:
+    return load().tts_status_str(code).decode()
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ----------------------------------------------------------------------------
+# Device weights (torch is only the allocator here)
+# ----------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _to_dev_u16(a: np.ndarray, device):
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device, non_blocking=False)
+
+
+def quantize_fp8_weight(w_dev, stream=None):
+    """Per-row E4M3 quantisation on the GPU; w_dev: int16 (bf16 bits) [N][K].
+    Returns (uint8 [N][K], float32 [N]) device tensors."""
+    torch = _torch()
+    N, K = w_dev.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w_dev.device)
+    s = torch.empty((N,), dtype=torch.float32, device=w_dev.device)
+    _call("tts_quantize_fp8_weight", w_dev.data_ptr(), N, K, q.data_ptr(), s.data_ptr(),
+          stream if stream is not None else None)
+    return q, s
+
+
+@dataclass
+class Dims:
+    n_layers: int = 36
+    hidden: int = 2560
+    n_q: int = 32
+    n_kv: int = 8
+    head_dim: int = 128
+    inter: int = 9728
+    n_cb: int = 8
+    cb_vocab: int = 1026
+    rms_eps: float = 1e-6
+    rope_theta: float = 1e6
+
+
+class DeviceWeights:
+    """Device copies of a weight set.  ``host`` is any object with the
+    attributes embed, head, final_norm and per-layer lists wqkv, wo, wgu, wd,
+    ln_in, ln_post, q_norm, k_norm holding bf16 bit images (uint16 numpy).
+    For FP8 the four projection matrices of each layer are quantised on the
+    GPU by tts_quantize_fp8_weight and only the E4M3 copies are kept."""
+
+    def __init__(self, host, precision: int = TTS_BF16, device="cuda"):
+        torch = _torch()
+        self.precision = precision
+        d = lambda a: _to_dev_u16(a, device)
+        self.embed, self.head, self.final_norm = d(host.embed), d(host.head), d(host.final_norm)
+        self.mats = {n: [] for n in ("wqkv", "wo", "wgu", "wd")}
+        self.scales = {n: [] for n in ("wqkv", "wo", "wgu", "wd")}
+        for name in ("wqkv", "wo", "wgu", "wd"):
+            for m in getattr(host, name):
+                t = d(m)
+                if precision == TTS_FP8:
+                    q, s = quantize_fp8_weight(t)
+                    del t
+                    self.mats[name].append(q)
+                    self.scales[name].append(s)
+                else:
+                    self.mats[name].append(t)
+        self.norms = {n: [d(x) for x in getattr(host, n)] for n in ("ln_in", "ln_post", "q_norm", "k_norm")}
+        torch.cuda.synchronize()
+        self.n_layers = len(self.mats["wqkv"])
+
+    def struct(self) -> tts_weights:
+        L = self.n_layers
+        keep = []
+
+        def arr(ts):
+            a = (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+            keep.append(a)
+            return ctypes.cast(a, _PP)
+
+        w = tts_weights()
+        w.embed, w.head, w.final_norm = self.embed.data_ptr(), self.head.data_ptr(), self.final_norm.data_ptr()
+        w.wqkv, w.wo, w.wgu, w.wd = (arr(self.mats[n]) for n in ("wqkv", "wo", "wgu", "wd"))
+        if self.precision == TTS_FP8:
+            w.sqkv, w.so, w.sgu, w.sd = (arr(self.scales[n]) for n in ("wqkv", "wo", "wgu", "wd"))
+        w.ln_in, w.ln_post, w.q_norm, w.k_norm = (arr(self.norms[n]) for n in ("ln_in", "ln_post", "q_norm", "k_norm"))
+        self._keep = keep
+        return w
+
+
+# ----------------------------------------------------------------------------
+# The decoder context
+# ----------------------------------------------------------------------------
+
+class Decoder:
+    """One tts_ctx: KV cache, scratch and the captured decode-step graph."""
+
+    def __init__(self, dims, weights: DeviceWeights, max_pos: int, stream=None):
+        self.dims = dims
+        self.weights = weights
+        cfg = tts_config(dims.n_layers, dims.hidden, dims.n_q, dims.n_kv, dims.head_dim, dims.inter,
+                         dims.n_cb, dims.cb_vocab, max_pos, dims.rms_eps, dims.rope_theta,
+                         weights.precision, stream)
+        self._cfg = cfg
+        self._w = weights.struct()
+        self._ctx = ctypes.c_void_p()
+        _call("tts_init", ctypes.byref(cfg), ctypes.byref(self._w), ctypes.byref(self._ctx))
+        self.max_pos = max_pos
+
+    @property
+    def handle(self):
+        return self._ctx
+
+    def close(self):
+        if self._ctx:
+            _call("tts_shutdown", self._ctx)
+            self._ctx = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        _call("tts_reset", self._ctx)
+
+    def prefill(self, codes: np.ndarray):
+        c = np.ascontiguousarray(codes, np.int32)
+        _call("tts_prefill", self._ctx, _ptr(c), c.shape[0])
+
+    def decode_step(self, codes_in=None) -> np.ndarray:
+        out = np.empty(self.dims.n_cb, np.int32)
+        if codes_in is None:
+            _call("tts_decode_step", self._ctx, None, _ptr(out))
+        else:
+            c = np.ascontiguousarray(codes_in, np.int32)
+            _call("tts_decode_step", self._ctx, _ptr(c), _ptr(out))
+        return out
+
+    def decode_steps(self, n: int) -> np.ndarray:
+        out = np.empty((n, self.dims.n_cb), np.int32)
+        _call("tts_decode_steps", self._ctx, n, _ptr(out))
+        return out
+
+    def rewind(self, pos: int, t: int = 0):
+        _call("tts_rewind", self._ctx, pos, t)
+
+    def set_kv(self, k_dev, v_dev, length: int, len_stride: int | None = None):
+        _call("tts_set_kv", self._ctx, k_dev.data_ptr(), v_dev.data_ptr(), length,
+              length if len_stride is None else len_stride)
+
+    def get_kv(self, p0: int, p1: int):
+        d = self.dims
+        shape = (d.n_layers, d.n_kv, p1 - p0, d.head_dim)
+        k = np.empty(shape, np.uint16)
+        v = np.empty(shape, np.uint16)
+        _call("tts_get_kv", self._ctx, _ptr(k), _ptr(v), p0, p1)
+        return k, v
+
+    def get_logits(self) -> np.ndarray:
+        out = np.empty((self.dims.n_cb, self.dims.cb_vocab), np.float32)
+        _call("tts_get_logits", self._ctx, _ptr(out))
+        return out
+
+    def get_hidden(self) -> np.ndarray:
+        out = np.empty(self.dims.hidden, np.float32)
+        _call("tts_get_hidden", self._ctx, _ptr(out))
+        return out
+
+    def set_frame(self, t: int, eoc: int = -1):
+        _call("tts_set_frame", self._ctx, t, eoc)
+
+    def state(self):
+        p, t, e = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _call("tts_get_state", self._ctx, ctypes.byref(p), ctypes.byref(t), ctypes.byref(e))
+        return p.value, t.value, e.value
+
+    def time_gemv(self, kind: int, reps: int = 1) -> float:
+        """Mean device ms of one launch of projection `kind` (0 QKV, 1 O, 2 gate/up, 3 down, 4 head)."""
+        ms = ctypes.c_float()
+        _call("tts_time_gemv", self._ctx, kind, reps, ctypes.byref(ms))
+        return ms.value
+
+    def last_steps_ms(self) -> float:
+        ms = ctypes.c_float()
+        _call("tts_last_steps_ms", self._ctx, ctypes.byref(ms))
+        return ms.value

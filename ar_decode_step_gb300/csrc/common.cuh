@@ -1,0 +1,120 @@
+// Device-side helpers shared by the decode-step kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace tts {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxCodebooks = 8;
+
+// Error bits recorded by kernels in DevState::err (never a trap).
+enum : int {
+    kErrPos = 1,        // position outside [0, max_pos)
+    kErrCode = 2,       // input code outside [0, cb_vocab)
+    kErrShape = 4,      // launch geometry does not match the data
+};
+
+// Device-resident decode state.  The graph reads and advances it, so one
+// captured graph serves every position.
+struct alignas(64) DevState {
+    int pos;          // next KV position to write
+    int t;            // frame index (delay pattern)
+    int eoc;          // frame at which codebook 0 emitted EOC, -1 = none
+    int err;          // error bits
+    int hist_idx;     // next slot of the code history ring
+    int prefill_row;  // next prompt row the prefill embeds
+    int pad[2];
+    int codes[kMaxCodebooks];  // codes produced by the last step = next input
+};
+
+// ---- programmatic dependent launch ------------------------------------
+// wait: block until the preceding grid in the stream has completed and its
+// memory is visible.  trigger: let the next grid start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- loads ----------------------------------------------------------------
+// 16-byte streaming load of read-only data that is used once (weights): no L1
+// allocation.  Not volatile, so the compiler may schedule it freely; it must
+// only be used on memory no kernel in flight writes.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Asynchronous bulk prefetch of [p, p+bytes) into L2 (bytes multiple of 16,
+// p 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ---- number formats --------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Round an fp32 value to bf16 (nearest even) and return it widened again.
+__device__ __forceinline__ float round_bf16(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Four E4M3 bytes (little-endian in w) to four floats (exact).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
+    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&lo));
+    float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&hi));
+    a = f0.x; b = f0.y; c = f1.x; d = f1.y;
+}
+
+// fp32 -> E4M3 (round to nearest even, saturating to +-448) -> fp32.
+__device__ __forceinline__ float quant_e4m3(float x) {
+    __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+    __half_raw h = __nv_cvt_fp8_to_halfraw(q, __NV_E4M3);
+    return __half2float(*reinterpret_cast<__half*>(&h));
+}
+
+// ---- reductions -------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Block-wide sum / max; `red` is shared scratch of >= 32 floats.  All threads
+// get the result.  Contains __syncthreads().
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    for (int i = 0; i < nw; ++i) s += red[i];  // fixed order: deterministic
+    return s;
+}
+__device__ __forceinline__ float block_max(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = red[0];
+    for (int i = 1; i < nw; ++i) s = fmaxf(s, red[i]);
+    return s;
+}
+
+}  // namespace tts

@@ -1,0 +1,548 @@
+// C ABI of the decode-step library: context lifetime, the position-agnostic
+// CUDA graph of one decode step, prefill, and state/test accessors.
+//
+// The whole step (embedding, 36 x [QKV GEMV, fused q/k-norm+RoPE+KV-write
+// attention, O-proj+residual, gate/up+SwiGLU, down+residual], head + argmax +
+// delay mask) is captured once into a CUDA graph whose kernels read the
+// position from device memory ("Higgs Audio v3 TTS-4B on FlashRT",
+// Performance: "position-agnostic CUDA graph"; section 7: replayed at any
+// position).  Kernels after the first are linked by programmatic dependent
+// launch edges so each can start streaming its weights before its producer
+// ends.  The graph is destroyed before any buffer it references is freed (the
+// TTS-Audio-Suite report's CUDA-graph teardown hazard).
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "kernels.h"
+#include "tts_decode.h"
+
+using namespace tts;
+
+namespace {
+
+struct LayerW {
+    const void *wqkv, *wo, *wgu, *wd;
+    const float *sqkv, *so, *sgu, *sd;
+    const __nv_bfloat16 *ln_in, *ln_post, *qn, *kn;
+};
+
+}  // namespace
+
+struct tts_ctx {
+    tts_config cfg{};
+    cudaStream_t stream = nullptr;  // caller's stream (may be the legacy default)
+    cudaStream_t cap = nullptr;     // private stream used for graph capture
+    int device = 0, num_sms = 0;
+    int qkv_rows = 0, attn_dim = 0, G = 1, S = 1;
+    bool pdl = true;
+
+    const __nv_bfloat16 *embed = nullptr, *head = nullptr, *final_norm = nullptr;
+    std::vector<LayerW> L;
+
+    std::vector<void*> allocs;
+    __nv_bfloat16 *kc = nullptr, *vc = nullptr;
+    float2* rope = nullptr;
+    float *h = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr, *logits = nullptr;
+    float *part_o = nullptr, *part_ml = nullptr;
+    unsigned* counters = nullptr;  // [n_kv] attention tickets, [n_kv] head ticket
+    DevState* st = nullptr;
+    int* hist = nullptr;
+    int* prompt = nullptr;
+
+    DevState* h_in = nullptr;   // pinned staging, host -> device
+    DevState* h_out = nullptr;  // pinned staging, device -> host
+
+    cudaGraphExec_t step_exec = nullptr;     // one decode step
+    cudaGraphExec_t prefill_exec = nullptr;  // one prefill position (no head)
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    float last_ms = 0.f;
+    int pos = 0;  // host shadow of st->pos
+};
+
+namespace {
+
+int report(cudaError_t e, const char* what) {
+    std::fprintf(stderr, "tts: %s failed: %s\n", what, cudaGetErrorString(e));
+    return TTS_ERR_CUDA;
+}
+
+#define TTS_CK(call)                                      \
+    do {                                                  \
+        cudaError_t e_ = (call);                          \
+        if (e_ != cudaSuccess) return report(e_, #call);  \
+    } while (0)
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+int validate(const tts_config* c, const tts_weights* w) {
+    if (!c || !w) return TTS_ERR_ARG;
+    if (c->n_layers < 1 || c->n_layers > 4096) return TTS_ERR_ARG;
+    if (c->head_dim != kHeadDim) return TTS_ERR_ARG;
+    if (c->n_kv_heads < 1 || c->n_q_heads < 1 || c->n_q_heads % c->n_kv_heads) return TTS_ERR_ARG;
+    const int G = c->n_q_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return TTS_ERR_ARG;
+    // GEMV inputs are staged in 48 KB of shared memory as fp32: K <= 12288
+    if (c->hidden < 256 || c->hidden % 256 || c->hidden > 12288) return TTS_ERR_ARG;
+    if (c->inter < 256 || c->inter % 256 || c->inter > 12288) return TTS_ERR_ARG;
+    if ((long long)c->n_q_heads * kHeadDim > 12288) return TTS_ERR_ARG;
+    if (c->n_codebooks < 1 || c->n_codebooks > kMaxCodebooks) return TTS_ERR_ARG;
+    if (c->cb_vocab < 2 || c->cb_vocab > (1 << 20)) return TTS_ERR_ARG;
+    if (c->max_pos < 1 || c->max_pos > 65536) return TTS_ERR_ARG;
+    if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return TTS_ERR_ARG;
+    if (c->precision != TTS_BF16 && c->precision != TTS_FP8) return TTS_ERR_ARG;
+    if (!aligned16(w->embed) || !aligned16(w->head) || !aligned16(w->final_norm)) return TTS_ERR_ARG;
+    if (!w->wqkv || !w->wo || !w->wgu || !w->wd || !w->ln_in || !w->ln_post || !w->q_norm || !w->k_norm)
+        return TTS_ERR_ARG;
+    const bool fp8 = c->precision == TTS_FP8;
+    if (fp8 && (!w->sqkv || !w->so || !w->sgu || !w->sd)) return TTS_ERR_ARG;
+    for (int l = 0; l < c->n_layers; ++l) {
+        if (!aligned16(w->wqkv[l]) || !aligned16(w->wo[l]) || !aligned16(w->wgu[l]) || !aligned16(w->wd[l]))
+            return TTS_ERR_ARG;
+        if (!aligned16(w->ln_in[l]) || !aligned16(w->ln_post[l]) || !aligned16(w->q_norm[l]) ||
+            !aligned16(w->k_norm[l]))
+            return TTS_ERR_ARG;
+        if (fp8 && (!w->sqkv[l] || !w->so[l] || !w->sgu[l] || !w->sd[l])) return TTS_ERR_ARG;
+    }
+    return TTS_OK;
+}
+
+template <typename T>
+int dalloc(tts_ctx* c, T** p, size_t count) {
+    void* q = nullptr;
+    TTS_CK(cudaMalloc(&q, count * sizeof(T) > 0 ? count * sizeof(T) : 16));
+    c->allocs.push_back(q);
+    *p = static_cast<T*>(q);
+    return TTS_OK;
+}
+
+#define TTS_TRY(expr)              \
+    do {                           \
+        int r_ = (expr);           \
+        if (r_ != TTS_OK) return r_; \
+    } while (0)
+
+LaunchCfg gemv_cfg(const tts_ctx* c, bool pdl) { return LaunchCfg{c->num_sms, 256, pdl}; }
+
+// Enqueue one position through the layer stack, then either the head (decode)
+// or the prefill advance.
+int record_step(tts_ctx* c, cudaStream_t s, bool decode) {
+    const tts_config& k = c->cfg;
+    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    EmbedParams ep{c->embed, c->st, decode ? nullptr : c->prompt, c->h, k.n_codebooks, k.cb_vocab, k.hidden};
+    TTS_CK(launch_embed(ep, LaunchCfg{0, 0, false}, s));
+    for (int l = 0; l < k.n_layers; ++l) {
+        const LayerW& w = c->L[l];
+        GemvParams g{};
+        g.eps = k.rms_eps;
+        // QKV: input RMSNorm (+ FP8 quant) fused in the prologue
+        g.W = w.wqkv; g.wscale = w.sqkv; g.x = c->h; g.gamma = w.ln_in; g.y = c->qkv;
+        g.N = c->qkv_rows; g.K = k.hidden;
+        TTS_CK(launch_gemv(prec, kProRms, kEpiStore, g, gemv_cfg(c, c->pdl), s));
+        // attention with q/k norm + RoPE + KV write
+        AttnParams a{};
+        a.qkv = c->qkv; a.q_norm = w.qn; a.k_norm = w.kn; a.rope = c->rope;
+        const size_t lay = (size_t)l * k.n_kv_heads * k.max_pos * kHeadDim;
+        a.kc = c->kc + lay; a.vc = c->vc + lay;
+        a.out = c->attn; a.part_o = c->part_o; a.part_ml = c->part_ml; a.counter = c->counters;
+        a.st = c->st; a.pos_override = -1;
+        a.n_q = k.n_q_heads; a.n_kv = k.n_kv_heads; a.max_pos = k.max_pos; a.S = c->S; a.eps = k.rms_eps;
+        TTS_CK(launch_attention(a, LaunchCfg{0, 0, c->pdl}, s));
+        // O-proj with residual add into h
+        g = GemvParams{};
+        g.W = w.wo; g.wscale = w.so; g.x = c->attn; g.y = c->h; g.N = k.hidden; g.K = c->attn_dim;
+        TTS_CK(launch_gemv(prec, kProPlain, kEpiResid, g, gemv_cfg(c, c->pdl), s));
+        // post-attention RMSNorm + gate/up + SwiGLU
+        g = GemvParams{};
+        g.eps = k.rms_eps;
+        g.W = w.wgu; g.wscale = w.sgu; g.x = c->h; g.gamma = w.ln_post; g.y = c->act; g.N = k.inter; g.K = k.hidden;
+        TTS_CK(launch_gemv(prec, kProRms, kEpiSwiglu, g, gemv_cfg(c, c->pdl), s));
+        // down-proj with residual add into h
+        g = GemvParams{};
+        g.W = w.wd; g.wscale = w.sd; g.x = c->act; g.y = c->h; g.N = k.hidden; g.K = k.inter;
+        TTS_CK(launch_gemv(prec, kProPlain, kEpiResid, g, gemv_cfg(c, c->pdl), s));
+    }
+    if (decode) {
+        GemvParams g{};
+        g.eps = k.rms_eps;
+        g.W = c->head; g.x = c->h; g.gamma = c->final_norm; g.y = c->logits;
+        g.N = k.n_codebooks * k.cb_vocab; g.K = k.hidden;
+        g.st = c->st; g.counter = c->counters + k.n_kv_heads; g.n_cb = k.n_codebooks; g.cb_vocab = k.cb_vocab;
+        g.hist = c->hist; g.hist_cap = k.max_pos;
+        TTS_CK(launch_gemv(kBF16, kProRms, kEpiLogits, g, gemv_cfg(c, c->pdl), s));
+    } else {
+        TTS_CK(launch_advance(c->st, LaunchCfg{0, 0, c->pdl}, s));
+    }
+    return TTS_OK;
+}
+
+int capture(tts_ctx* c, bool decode, cudaGraphExec_t* out) {
+    cudaGraph_t graph = nullptr;
+    TTS_CK(cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+    int rc = record_step(c, c->cap, decode);
+    cudaError_t e = cudaStreamEndCapture(c->cap, &graph);
+    if (rc != TTS_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    if (e != cudaSuccess) return report(e, "cudaStreamEndCapture");
+    e = cudaGraphInstantiate(out, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return report(e, "cudaGraphInstantiate");
+    TTS_CK(cudaGraphUpload(*out, c->stream));
+    return TTS_OK;
+}
+
+// Read the device state into h_out (synchronising) and check the error word.
+int pull_state(tts_ctx* c) {
+    TTS_CK(cudaMemcpyAsync(c->h_out, c->st, sizeof(DevState), cudaMemcpyDeviceToHost, c->stream));
+    TTS_CK(cudaStreamSynchronize(c->stream));
+    c->pos = c->h_out->pos;
+    if (c->h_out->err) {
+        const int zero = 0;
+        cudaMemcpy(&c->st->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        return TTS_ERR_DEVICE;
+    }
+    return TTS_OK;
+}
+
+int push_state(tts_ctx* c, const DevState& s) {
+    *c->h_in = s;
+    TTS_CK(cudaMemcpyAsync(c->st, c->h_in, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
+    TTS_CK(cudaStreamSynchronize(c->stream));
+    c->pos = s.pos;
+    return TTS_OK;
+}
+
+DevState bos_state(const tts_ctx* c, int pos, int t, int eoc) {
+    DevState s{};
+    s.pos = pos;
+    s.t = t;
+    s.eoc = eoc;
+    for (int k = 0; k < kMaxCodebooks; ++k) s.codes[k] = c->cfg.cb_vocab - 2;
+    return s;
+}
+
+int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
+    c->cfg = *cfg;
+    const tts_config& k = c->cfg;
+    c->stream = static_cast<cudaStream_t>(cfg->stream);
+    c->qkv_rows = (k.n_q_heads + 2 * k.n_kv_heads) * kHeadDim;
+    c->attn_dim = k.n_q_heads * kHeadDim;
+    c->G = k.n_q_heads / k.n_kv_heads;
+    c->S = attn_splits_for(k.max_pos);
+    const char* nopdl = std::getenv("TTS_NO_PDL");
+    c->pdl = !(nopdl && nopdl[0] == '1');
+
+    TTS_CK(cudaGetDevice(&c->device));
+    TTS_CK(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
+    TTS_CK(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking));
+    TTS_CK(cudaEventCreate(&c->ev0));
+    TTS_CK(cudaEventCreate(&c->ev1));
+
+    c->embed = static_cast<const __nv_bfloat16*>(w->embed);
+    c->head = static_cast<const __nv_bfloat16*>(w->head);
+    c->final_norm = static_cast<const __nv_bfloat16*>(w->final_norm);
+    const bool fp8 = k.precision == TTS_FP8;
+    c->L.resize(k.n_layers);
+    for (int l = 0; l < k.n_layers; ++l) {
+        LayerW& x = c->L[l];
+        x.wqkv = w->wqkv[l]; x.wo = w->wo[l]; x.wgu = w->wgu[l]; x.wd = w->wd[l];
+        x.sqkv = fp8 ? w->sqkv[l] : nullptr; x.so = fp8 ? w->so[l] : nullptr;
+        x.sgu = fp8 ? w->sgu[l] : nullptr; x.sd = fp8 ? w->sd[l] : nullptr;
+        x.ln_in = static_cast<const __nv_bfloat16*>(w->ln_in[l]);
+        x.ln_post = static_cast<const __nv_bfloat16*>(w->ln_post[l]);
+        x.qn = static_cast<const __nv_bfloat16*>(w->q_norm[l]);
+        x.kn = static_cast<const __nv_bfloat16*>(w->k_norm[l]);
+    }
+
+    const size_t kv = (size_t)k.n_layers * k.n_kv_heads * k.max_pos * kHeadDim;
+    TTS_TRY(dalloc(c, &c->kc, kv));
+    TTS_TRY(dalloc(c, &c->vc, kv));
+    TTS_TRY(dalloc(c, &c->rope, (size_t)k.max_pos * (kHeadDim / 2)));
+    TTS_TRY(dalloc(c, &c->h, k.hidden));
+    TTS_TRY(dalloc(c, &c->qkv, c->qkv_rows));
+    TTS_TRY(dalloc(c, &c->attn, c->attn_dim));
+    TTS_TRY(dalloc(c, &c->act, k.inter));
+    TTS_TRY(dalloc(c, &c->logits, (size_t)k.n_codebooks * k.cb_vocab));
+    TTS_TRY(dalloc(c, &c->part_o, (size_t)k.n_kv_heads * c->S * c->G * kHeadDim));
+    TTS_TRY(dalloc(c, &c->part_ml, (size_t)k.n_kv_heads * c->S * c->G * 2));
+    TTS_TRY(dalloc(c, &c->counters, (size_t)2 * k.n_kv_heads));
+    TTS_TRY(dalloc(c, &c->st, 1));
+    TTS_TRY(dalloc(c, &c->hist, (size_t)k.max_pos * k.n_codebooks));
+    TTS_TRY(dalloc(c, &c->prompt, (size_t)k.max_pos * k.n_codebooks));
+    TTS_CK(cudaMemsetAsync(c->kc, 0, kv * sizeof(__nv_bfloat16), c->stream));
+    TTS_CK(cudaMemsetAsync(c->vc, 0, kv * sizeof(__nv_bfloat16), c->stream));
+    TTS_CK(cudaMemsetAsync(c->counters, 0, 2 * k.n_kv_heads * sizeof(unsigned), c->stream));
+    TTS_CK(cudaMemsetAsync(c->h, 0, k.hidden * sizeof(float), c->stream));
+    TTS_CK(cudaMemsetAsync(c->logits, 0, (size_t)k.n_codebooks * k.cb_vocab * sizeof(float), c->stream));
+    TTS_CK(cudaHostAlloc((void**)&c->h_in, sizeof(DevState), cudaHostAllocDefault));
+    TTS_CK(cudaHostAlloc((void**)&c->h_out, sizeof(DevState), cudaHostAllocDefault));
+
+    // RoPE table: inverse frequencies theta^(-2i/D), angle pos * inv_f in fp64,
+    // cos/sin rounded to fp32.
+    {
+        std::vector<float2> tab((size_t)k.max_pos * (kHeadDim / 2));
+        for (int p = 0; p < k.max_pos; ++p)
+            for (int i = 0; i < kHeadDim / 2; ++i) {
+                const double inv_f = std::pow((double)k.rope_theta, -2.0 * i / (double)kHeadDim);
+                const double ang = (double)p * inv_f;
+                tab[(size_t)p * (kHeadDim / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+        TTS_CK(cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    }
+    TTS_TRY(push_state(c, bos_state(c, 0, 0, -1)));
+    TTS_TRY(capture(c, true, &c->step_exec));
+    TTS_TRY(capture(c, false, &c->prefill_exec));
+    TTS_CK(cudaStreamSynchronize(c->stream));
+    return TTS_OK;
+}
+
+void destroy(tts_ctx* c) {
+    if (!c) return;
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    else cudaDeviceSynchronize();
+    // graphs first: they reference the buffers below
+    if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
+    if (c->prefill_exec) cudaGraphExecDestroy(c->prefill_exec);
+    for (void* p : c->allocs) cudaFree(p);
+    if (c->h_in) cudaFreeHost(c->h_in);
+    if (c->h_out) cudaFreeHost(c->h_out);
+    if (c->ev0) cudaEventDestroy(c->ev0);
+    if (c->ev1) cudaEventDestroy(c->ev1);
+    if (c->cap) cudaStreamDestroy(c->cap);
+    delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tts_init(const tts_config* cfg, const tts_weights* w, tts_ctx** out) {
+    if (!out) return TTS_ERR_ARG;
+    *out = nullptr;
+    int rc = validate(cfg, w);
+    if (rc != TTS_OK) return rc;
+    tts_ctx* c = new tts_ctx();
+    rc = init_impl(c, cfg, w);
+    if (rc != TTS_OK) {
+        destroy(c);
+        return rc;
+    }
+    *out = c;
+    return TTS_OK;
+}
+
+int tts_shutdown(tts_ctx* ctx) {
+    destroy(ctx);
+    return TTS_OK;
+}
+
+int tts_reset(tts_ctx* ctx) {
+    if (!ctx) return TTS_ERR_STATE;
+    return push_state(ctx, bos_state(ctx, 0, 0, -1));
+}
+
+int tts_decode_step(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (ctx->pos >= k.max_pos) return TTS_ERR_FULL;
+    if (codes_in) {
+        for (int i = 0; i < k.n_codebooks; ++i)
+            if (codes_in[i] < 0 || codes_in[i] >= k.cb_vocab) return TTS_ERR_CODE;
+        std::memcpy(ctx->h_in->codes, codes_in, sizeof(int32_t) * k.n_codebooks);
+        TTS_CK(cudaMemcpyAsync(ctx->st->codes, ctx->h_in->codes, sizeof(int32_t) * k.n_codebooks,
+                               cudaMemcpyHostToDevice, ctx->stream));
+    }
+    TTS_CK(cudaGraphLaunch(ctx->step_exec, ctx->stream));
+    int rc = pull_state(ctx);
+    if (rc != TTS_OK) return rc;
+    if (codes_out) std::memcpy(codes_out, ctx->h_out->codes, sizeof(int32_t) * k.n_codebooks);
+    return TTS_OK;
+}
+
+int tts_decode_steps(tts_ctx* ctx, int n, int32_t* codes_out) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (n < 0) return TTS_ERR_ARG;
+    const tts_config& k = ctx->cfg;
+    if ((long long)ctx->pos + n > k.max_pos) return TTS_ERR_FULL;
+    if (n == 0) return TTS_OK;
+    const int zero = 0;
+    TTS_CK(cudaMemcpyAsync(&ctx->st->hist_idx, &zero, sizeof(int), cudaMemcpyHostToDevice, ctx->stream));
+    TTS_CK(cudaEventRecord(ctx->ev0, ctx->stream));
+    for (int i = 0; i < n; ++i) TTS_CK(cudaGraphLaunch(ctx->step_exec, ctx->stream));
+    TTS_CK(cudaEventRecord(ctx->ev1, ctx->stream));
+    if (codes_out)
+        TTS_CK(cudaMemcpyAsync(codes_out, ctx->hist, sizeof(int32_t) * (size_t)n * k.n_codebooks,
+                               cudaMemcpyDeviceToHost, ctx->stream));
+    int rc = pull_state(ctx);
+    TTS_CK(cudaEventElapsedTime(&ctx->last_ms, ctx->ev0, ctx->ev1));
+    return rc;
+}
+
+int tts_prefill(tts_ctx* ctx, const int32_t* codes, int P) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (P < 0 || (P > 0 && !codes)) return TTS_ERR_ARG;
+    if ((long long)ctx->pos + P > k.max_pos) return TTS_ERR_FULL;
+    for (long long i = 0; i < (long long)P * k.n_codebooks; ++i)
+        if (codes[i] < 0 || codes[i] >= k.cb_vocab) return TTS_ERR_CODE;
+    if (P == 0) return TTS_OK;
+    TTS_CK(cudaMemcpyAsync(ctx->prompt, codes, sizeof(int32_t) * (size_t)P * k.n_codebooks,
+                           cudaMemcpyHostToDevice, ctx->stream));
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    DevState s = *ctx->h_out;
+    s.prefill_row = 0;
+    TTS_TRY(push_state(ctx, s));
+    for (int p = 0; p < P; ++p) TTS_CK(cudaGraphLaunch(ctx->prefill_exec, ctx->stream));
+    int rc = pull_state(ctx);
+    if (rc != TTS_OK) return rc;
+    DevState after = *ctx->h_out;
+    for (int i = 0; i < kMaxCodebooks; ++i) after.codes[i] = k.cb_vocab - 2;  // next input: all-BOS frame
+    return push_state(ctx, after);
+}
+
+int tts_rewind(tts_ctx* ctx, int pos, int t) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (pos < 0 || pos > ctx->pos || t < 0) return TTS_ERR_ARG;
+    return push_state(ctx, bos_state(ctx, pos, t, -1));
+}
+
+int tts_set_kv(tts_ctx* ctx, const void* kd, const void* vd, int len, int len_stride) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (!kd || !vd || len < 0 || len > k.max_pos || len_stride < len) return TTS_ERR_ARG;
+    if (len > 0) {
+        const size_t row = (size_t)len * kHeadDim * sizeof(__nv_bfloat16);
+        const size_t spitch = (size_t)len_stride * kHeadDim * sizeof(__nv_bfloat16);
+        const size_t dpitch = (size_t)k.max_pos * kHeadDim * sizeof(__nv_bfloat16);
+        const size_t rows = (size_t)k.n_layers * k.n_kv_heads;
+        TTS_CK(cudaMemcpy2DAsync(ctx->kc, dpitch, kd, spitch, row, rows, cudaMemcpyDeviceToDevice, ctx->stream));
+        TTS_CK(cudaMemcpy2DAsync(ctx->vc, dpitch, vd, spitch, row, rows, cudaMemcpyDeviceToDevice, ctx->stream));
+    }
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    DevState s = *ctx->h_out;
+    s.pos = len;
+    return push_state(ctx, s);
+}
+
+int tts_get_kv(tts_ctx* ctx, void* k_host, void* v_host, int p0, int p1) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (p0 < 0 || p1 < p0 || p1 > k.max_pos) return TTS_ERR_ARG;
+    if (p1 == p0) return TTS_OK;
+    const size_t row = (size_t)(p1 - p0) * kHeadDim * sizeof(__nv_bfloat16);
+    const size_t spitch = (size_t)k.max_pos * kHeadDim * sizeof(__nv_bfloat16);
+    const size_t rows = (size_t)k.n_layers * k.n_kv_heads;
+    const size_t off = (size_t)p0 * kHeadDim;
+    if (k_host) TTS_CK(cudaMemcpy2DAsync(k_host, row, ctx->kc + off, spitch, row, rows, cudaMemcpyDeviceToHost, ctx->stream));
+    if (v_host) TTS_CK(cudaMemcpy2DAsync(v_host, row, ctx->vc + off, spitch, row, rows, cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    return TTS_OK;
+}
+
+int tts_get_logits(tts_ctx* ctx, float* out) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!out) return TTS_ERR_ARG;
+    const size_t n = (size_t)ctx->cfg.n_codebooks * ctx->cfg.cb_vocab;
+    TTS_CK(cudaMemcpyAsync(out, ctx->logits, n * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    return TTS_OK;
+}
+
+int tts_get_hidden(tts_ctx* ctx, float* out) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!out) return TTS_ERR_ARG;
+    TTS_CK(cudaMemcpyAsync(out, ctx->h, (size_t)ctx->cfg.hidden * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    return TTS_OK;
+}
+
+int tts_set_frame(tts_ctx* ctx, int t, int eoc_frame) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (t < 0 || eoc_frame < -1) return TTS_ERR_ARG;
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    DevState s = *ctx->h_out;
+    s.t = t;
+    s.eoc = eoc_frame;
+    return push_state(ctx, s);
+}
+
+int tts_get_state(tts_ctx* ctx, int* pos, int* t, int* eoc) {
+    if (!ctx) return TTS_ERR_STATE;
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    if (pos) *pos = ctx->h_out->pos;
+    if (t) *t = ctx->h_out->t;
+    if (eoc) *eoc = ctx->h_out->eoc;
+    return TTS_OK;
+}
+
+int tts_last_steps_ms(tts_ctx* ctx, float* ms) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!ms) return TTS_ERR_ARG;
+    *ms = ctx->last_ms;
+    return TTS_OK;
+}
+
+int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (kind < 0 || kind > 4 || reps < 1 || !ms_per_launch) return TTS_ERR_ARG;
+    const tts_config& k = ctx->cfg;
+    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    TTS_CK(cudaEventRecord(ctx->ev0, ctx->stream));
+    for (int r = 0; r < reps; ++r)
+        for (int l = 0; l < k.n_layers; ++l) {
+            const LayerW& w = ctx->L[l];
+            GemvParams g{};
+            g.eps = k.rms_eps;
+            int pro = kProRms, epi = kEpiStore, p = prec;
+            switch (kind) {
+                case 0: g.W = w.wqkv; g.wscale = w.sqkv; g.x = ctx->h; g.gamma = w.ln_in; g.y = ctx->qkv;
+                        g.N = ctx->qkv_rows; g.K = k.hidden; break;
+                case 1: g.W = w.wo; g.wscale = w.so; g.x = ctx->attn; g.y = ctx->h; g.N = k.hidden;
+                        g.K = ctx->attn_dim; pro = kProPlain; epi = kEpiResid; break;
+                case 2: g.W = w.wgu; g.wscale = w.sgu; g.x = ctx->h; g.gamma = w.ln_post; g.y = ctx->act;
+                        g.N = k.inter; g.K = k.hidden; epi = kEpiSwiglu; break;
+                case 3: g.W = w.wd; g.wscale = w.sd; g.x = ctx->act; g.y = ctx->h; g.N = k.hidden;
+                        g.K = k.inter; pro = kProPlain; epi = kEpiResid; break;
+                default: g.W = ctx->head; g.x = ctx->h; g.gamma = ctx->final_norm; g.y = ctx->logits;
+                         g.N = k.n_codebooks * k.cb_vocab; g.K = k.hidden; p = kBF16; break;
+            }
+            TTS_CK(launch_gemv(p, pro, epi, g, gemv_cfg(ctx, ctx->pdl && (r | l)), ctx->stream));
+        }
+    TTS_CK(cudaEventRecord(ctx->ev1, ctx->stream));
+    TTS_CK(cudaEventSynchronize(ctx->ev1));
+    float ms = 0.f;
+    TTS_CK(cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1));
+    *ms_per_launch = ms / (float)(reps * k.n_layers);
+    return TTS_OK;
+}
+
+int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream) {
+    if (!W || !W8 || !s || N <= 0 || K <= 0) return TTS_ERR_ARG;
+    TTS_CK(launch_quantize_weight(static_cast<const __nv_bfloat16*>(W), N, K, static_cast<uint8_t*>(W8), s,
+                                  static_cast<cudaStream_t>(stream)));
+    return TTS_OK;
+}
+
+const char* tts_status_str(int status) {
+    switch (status) {
+        case TTS_OK: return "ok";
+        case TTS_ERR_ARG: return "bad argument";
+        case TTS_ERR_CODE: return "code out of range";
+        case TTS_ERR_FULL: return "context full";
+        case TTS_ERR_CUDA: return "CUDA error";
+        case TTS_ERR_DEVICE: return "device error flag set";
+        case TTS_ERR_STATE: return "not initialised";
+        case TTS_ERR_UNSUPPORTED: return "unsupported";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

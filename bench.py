@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the batch-1 TTS decode step on one GB300 (or N replicas).
+
+Default workload: the full 36-layer BF16 backbone (hidden 2560, GQA 32q/8kv,
+head_dim 128, SwiGLU 9728, 8 x 1026 codebook head), seeded synthetic weights
+N(0, 0.02), a 13-position prompt under the delay pattern prefilled once, then
+greedy decode frames with device-side code feedback, context 13 -> 141 in
+segments of 128 frames (the cache is rewound to the prompt between segments).
+One bench step = one decode frame (every stage of the step: embedding, 36
+layers, head + argmax + delay mask).  Inputs (7.3 GB of weights per frame) are
+far larger than L2, so no flush is needed.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded per-step sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode ms/frame & frames/s at batch 1 (1 GB300); achieved HBM GB/s vs peak"
+
+WORKLOADS = {
+    # name: (n_layers, precision, prompt P, kv prefix, frames per segment)
+    "bf16-36L-prompt13-128frames": dict(n_layers=36, precision=0, prompt=13, kv=0, seg=128),
+    "fp8-36L-kv1024-256frames": dict(n_layers=36, precision=1, prompt=0, kv=1024, seg=256),
+    "bf16-36L-kv8192-64frames": dict(n_layers=36, precision=0, prompt=0, kv=8192, seg=64),
+}
+DEFAULT_WORKLOAD = "bf16-36L-prompt13-128frames"
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def step_bytes(d, precision: int, ctx_len: int) -> float:
+    """Algorithmic HBM bytes of one decode step at context length ctx_len (the
+    step attends ctx_len positions, the new one included): every weight and
+    FP8 scale once, the head, norm gains, 8 embedding rows, the KV read over
+    the context and the KV write of one position."""
+    H, I, D = d.hidden, d.inter, d.head_dim
+    qkv = (d.n_q + 2 * d.n_kv) * D
+    wb = 1 if precision == 1 else 2
+    per_layer = (qkv * H + H * d.n_q * D + 2 * I * H + H * I) * wb
+    if precision == 1:
+        per_layer += (qkv + H + 2 * I + H) * 4
+    per_layer += (2 * H + 2 * D) * 2                      # norm gains
+    kv_read = 2 * d.n_kv * D * 2 * (ctx_len - 1)          # cached rows
+    kv_write = 2 * d.n_kv * D * 2
+    head = d.n_cb * d.cb_vocab * H * 2 + H * 2
+    embed = d.n_cb * H * 2
+    return d.n_layers * (per_layer + kv_read + kv_write) + head + embed
+
+
+def gemv_bytes(d, precision: int, kind: int) -> float:
+    """Algorithmic bytes of one GEMV launch: weights (+ FP8 scales) plus the
+    input and output vectors."""
+    H, I, D = d.hidden, d.inter, d.head_dim
+    qkv = (d.n_q + 2 * d.n_kv) * D
+    wb = 1 if precision == 1 else 2
+    rows, K, nout = {0: (qkv, H, qkv), 1: (H, d.n_q * D, H), 2: (2 * I, H, I), 3: (H, I, H),
+                     4: (d.n_cb * d.cb_vocab, H, d.n_cb * d.cb_vocab)}[kind]
+    if kind == 4:
+        wb = 2
+    b = rows * K * wb + K * 4 + nout * 4
+    if precision == 1 and kind != 4:
+        b += rows * 4
+    return b
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+def dims_for(n_layers: int):
+    import synth
+    return synth.Dims(n_layers=n_layers)
+
+
+def make_host_weights(d):
+    import synth
+    return synth.make_weights(d)
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_frame_seconds(host_w, wl, frames: int, budget_s: float) -> tuple[float, int]:
+    """Time the oracle as it stands on whole frames of the workload's model
+    (KV prefix of the workload's starting context), up to `frames` frames or
+    `budget_s` seconds (at least one frame).  Returns (seconds/frame, frames)."""
+    import oracle
+    import synth
+    d = host_w.dims
+    ctx0 = wl["prompt"] or wl["kv"]
+    max_pos = ctx0 + frames + 1
+    orc = oracle.Oracle(host_w, max_pos, precision=wl["precision"])
+    k, v = synth.make_kv_prefix(d, ctx0, max_pos)
+    orc.set_kv(k, v, ctx0)
+    codes = np.full(d.n_cb, 1024, np.int32)
+    t0 = time.perf_counter()
+    n = 0
+    while n < frames:
+        codes, _, _ = orc.decode_step(codes)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return (time.perf_counter() - t0) / n, n
+
+
+def run_reference(args, wl_name, wl):
+    """The CPU oracle timed per bench step on a bounded sample: a 2-layer
+    prefix of the workload's model (full width, same context) plus the head,
+    scaled to the full depth by the ratio of algorithmic bytes."""
+    import synth
+    d_full = dims_for(wl["n_layers"])
+    nl_sample = min(2, wl["n_layers"])
+    d = synth.Dims(n_layers=nl_sample)
+    w = make_host_weights(d)
+    import oracle
+    ctx0 = wl["prompt"] or wl["kv"]
+    total = args.warmup + args.steps
+    max_pos = ctx0 + wl["seg"] + 1
+    orc = oracle.Oracle(w, max_pos, precision=wl["precision"])
+    k, v = synth.make_kv_prefix(d, ctx0, max_pos)
+    orc.set_kv(k, v, ctx0)
+    scale = step_bytes(d_full, wl["precision"], ctx0 + wl["seg"] // 2) / step_bytes(d, wl["precision"], ctx0 + wl["seg"] // 2)
+    codes = np.full(d.n_cb, 1024, np.int32)
+    times = []
+    frame = 0
+    for i in range(total):
+        if frame == wl["seg"]:
+            orc.set_kv(k, v, ctx0)
+            orc.set_frame(0)
+            frame = 0
+        t0 = time.perf_counter()
+        codes, _, _ = orc.decode_step(codes)
+        times.append(time.perf_counter() - t0)
+        frame += 1
+    timed = sum(times[args.warmup:]) * scale
+    ms = timed / args.steps * 1e3
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    value = 1e3 / ms
+    sample = (f"each step: one decode frame of a {nl_sample}-layer full-width prefix of the model plus the "
+              f"head on the CPU oracle (fp64), time scaled by the algorithmic-byte ratio {scale:.2f} to "
+              f"{wl['n_layers']} layers")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl_name, "layers": wl["n_layers"],
+                       "precision": "fp8-e4m3-w8a8" if wl["precision"] else "bf16-w16"},
+            "cpu_baseline": {"value": value, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# The GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args, wl_name, wl):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+
+    import ar_decode_step_gb300.build as build
+    build.build()
+    import ar_decode_step_gb300 as ads
+    import synth
+
+    d = dims_for(wl["n_layers"])
+    t_gen = time.time()
+    host_w = make_host_weights(d)
+    dw = ads.DeviceWeights(host_w, precision=wl["precision"])
+    gen_s = time.time() - t_gen
+    seg = wl["seg"]
+    ctx0 = wl["prompt"] or wl["kv"]
+    max_pos = ctx0 + seg + 8
+    dec = ads.Decoder(ads.Dims(**{f: getattr(d, f) for f in ("n_layers", "hidden", "n_q", "n_kv", "head_dim",
+                                                              "inter", "n_cb", "cb_vocab")}),
+                      dw, max_pos)
+    prefill_ms = None
+    if wl["prompt"]:
+        prompt = synth.delayed_prompt_codes(wl["prompt"])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dec.prefill(prompt)
+        prefill_ms = (time.perf_counter() - t0) * 1e3
+    else:
+        k, v = synth.make_kv_prefix(d, wl["kv"], wl["kv"])
+        kd = torch.from_numpy(k.view(np.int16)).cuda()
+        vd = torch.from_numpy(v.view(np.int16)).cuda()
+        dec.set_kv(kd, vd, wl["kv"])
+        del kd, vd, k, v
+
+    seg_t = [0]  # frames decoded in the current segment
+
+    def run_frames(n):
+        """n frames in segments of `seg`, rewinding to the prompt between segments."""
+        done = 0
+        while done < n:
+            if seg_t[0] >= seg:
+                dec.rewind(ctx0, 0)
+                seg_t[0] = 0
+            m = min(seg - seg_t[0], n - done)
+            dec.decode_steps(m)
+            seg_t[0] += m
+            done += m
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    run_frames(args.warmup)
+    dec.rewind(ctx0, 0)
+    seg_t[0] = 0
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record()
+    run_frames(args.steps)
+    ev1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    time.sleep(0.25)
+    clocks.stop()
+    clock_info = clocks.summary(t_wall0 - 0.05, t_wall1 + 0.05)
+
+    ms_per_step = ms_total / args.steps
+    value = world * args.steps / (ms_total / 1e3)
+
+    # roofline of the dominant kernel (gate/up GEMV, about half the step's bytes)
+    kind = 2
+    reps = 3
+    dec.time_gemv(kind, 1)
+    ms_launch = dec.time_gemv(kind, reps)
+    gb = gemv_bytes(d, wl["precision"], kind)
+    peak, peak_kind = read_peaks()
+    achieved = gb / (ms_launch * 1e-3) / 1e9
+    per_kind = {}
+    for kk, name in enumerate(["qkv", "o_proj", "gate_up", "down", "head"]):
+        ms_k = dec.time_gemv(kk, 2)
+        per_kind[name] = {"ms": ms_k, "GB/s": gemv_bytes(d, wl["precision"], kk) / (ms_k * 1e-3) / 1e9}
+
+    # whole-step roofline: mean algorithmic bytes over the timed contexts
+    ctxs = []
+    t = 0
+    for _ in range(args.steps):
+        if t == seg:
+            t = 0
+        ctxs.append(ctx0 + t + 1)
+        t += 1
+    mean_bytes = float(np.mean([step_bytes(d, wl["precision"], c) for c in ctxs]))
+    step_gbs = mean_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public C ABI with host buffers: each frame copies
+    # its 8 input codes host->device and reads the state (codes) back
+    dec.rewind(ctx0, 0)
+    codes = np.full(d.n_cb, 1024, np.int32)
+    n_e2e = min(args.steps, 256)
+    torch.cuda.synchronize()
+    te0 = time.perf_counter()
+    for i in range(n_e2e):
+        if i and i % seg == 0:
+            dec.rewind(ctx0, 0)
+        codes = dec.decode_step(codes)
+    te1 = time.perf_counter()
+    e2e_fps = world * n_e2e / (te1 - te0)
+
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        s_per_frame, nfr = oracle_frame_seconds(host_w, wl, frames=20, budget_s=args.cpu_budget)
+        cpu_baseline = {"value": 1.0 / s_per_frame, "unit": "frames/s",
+                        "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
+                        "kind": "oracle",
+                        "sample": f"{nfr} whole decode frames of the same {wl['n_layers']}-layer model "
+                                  f"(same weights) at context {ctx0 + 1}..{ctx0 + nfr}, fp64 C oracle"}
+
+    launches_per_step = 1 + 5 * d.n_layers + 1
+    line = {
+        "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl["precision"] == 0 else "fp8-e4m3", "data": "synthetic",
+        "config": {"workload": wl_name, "layers": d.n_layers, "hidden": d.hidden, "heads": f"{d.n_q}q/{d.n_kv}kv",
+                   "inter": d.inter, "codebooks": f"{d.n_cb}x{d.cb_vocab}", "start_context": ctx0,
+                   "frames_per_segment": seg, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (all weights streamed every frame)",
+                   "weights": "seeded N(0,0.02)", "graph": "one CUDA graph per frame"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "gate/up GEMV + SwiGLU",
+                     "bytes_per_launch": gb, "ms_per_launch": ms_launch, "peak_source": peak_kind},
+        "step_roofline": {"bytes_per_step": mean_bytes, "achieved_GBps": step_gbs, "frac": step_gbs / peak},
+        "per_kernel": per_kind,
+        "clocks": clock_info,
+        "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 4 * d.n_cb,
+                "d2h_bytes_per_step": 64, "frames": n_e2e},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu_baseline,
+        "prefill_ms": prefill_ms,
+        "setup_s": gen_s,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args, args.workload, wl)
+        return
+    run_gpu(args, args.workload, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * tts_decode.h -- C ABI of the GB300 (sm_103a) batch-1 decode-step library for
+ * a Higgs-Audio-style TTS backbone.
+ *
+ * The backbone is a dense Qwen3-4B-shaped decoder (36 layers, hidden 2560, GQA
+ * 32 query / 8 key-value heads, head_dim 128, SwiGLU, RoPE theta 1e6, per-head
+ * q/k RMSNorm), fed by a fused embedding of 8 codebooks under a delay pattern
+ * and read out by a fused 8 x 1026 codebook head with a per-codebook greedy
+ * argmax ("Higgs Audio v3 TTS-4B on FlashRT (RTX 5090 / SM120)", page header
+ * and section 5 "What runs under the hood"; the SGLang-Omni Higgs Audio v3
+ * post, architecture paragraph).
+ *
+ * Conventions for every entry point:
+ *  - Return value: TTS_OK (0) or a negative TTS_ERR_* code.  On error the
+ *    decode position is left unchanged.  tts_status_str() names a code.
+ *  - "device" pointers are CUDA global-memory addresses on the current
+ *    device; "host" pointers are ordinary CPU memory.  Pointers are borrowed:
+ *    the library copies host arrays before returning and never frees caller
+ *    memory.  Device weight buffers must stay valid until tts_shutdown().
+ *  - All work runs on the stream given in tts_config (NULL = legacy default
+ *    stream).  Entry points that return host results synchronise that stream.
+ *  - One context per stream; a context is not thread-safe.
+ *
+ * Layouts (all row-major):
+ *  - bf16 matrices are [out][in]; FP8 matrices are E4M3 bytes [out][in] with
+ *    one fp32 scale per output row (value = byte_value * scale).
+ *  - Wqkv rows: query heads (head*D + d), then key heads, then value heads.
+ *  - Wgu rows: the gate matrix [inter][hidden] followed by the up matrix.
+ *  - Codebook head rows: codebook k, code v at row k*cb_vocab + v.
+ *  - KV cache: bf16 [n_layers][n_kv_heads][max_pos][head_dim], owned by the
+ *    library.
+ */
+#ifndef TTS_DECODE_H
+#define TTS_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    TTS_OK = 0,
+    TTS_ERR_ARG = -1,         /* NULL pointer, bad size, unsupported dimensions */
+    TTS_ERR_CODE = -2,        /* an input code outside [0, cb_vocab) */
+    TTS_ERR_FULL = -3,        /* the step would write at or past max_pos */
+    TTS_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+    TTS_ERR_DEVICE = -5,      /* a kernel recorded a bounds or wait failure */
+    TTS_ERR_STATE = -6,       /* context not initialised / already shut down */
+    TTS_ERR_UNSUPPORTED = -7  /* valid request this build does not implement */
+};
+
+enum { TTS_BF16 = 0, TTS_FP8 = 1 };
+
+typedef struct tts_ctx tts_ctx;
+
+/* Model and run configuration.  Supported shapes: head_dim 128; n_q_heads a
+ * multiple of n_kv_heads with 1, 2, 4 or 8 query heads per key-value head;
+ * hidden, inter and n_q_heads*128 multiples of 256 and at most 12288;
+ * n_codebooks 1..8; cb_vocab >= 2 (codes
+ * cb_vocab-2 and cb_vocab-1 are BOS-pad and EOC, i.e. 1024 and 1025 for the
+ * 1026-entry codebooks); 1 <= max_pos <= 65536. */
+typedef struct {
+    int n_layers;      /* 36 for the full backbone */
+    int hidden;        /* 2560 */
+    int n_q_heads;     /* 32 */
+    int n_kv_heads;    /* 8 */
+    int head_dim;      /* 128 */
+    int inter;         /* 9728 */
+    int n_codebooks;   /* 8 */
+    int cb_vocab;      /* 1026 */
+    int max_pos;       /* KV-cache capacity in positions */
+    float rms_eps;     /* 1e-6 */
+    float rope_theta;  /* 1e6 */
+    int precision;     /* TTS_BF16 (W16, fp32 activations) or TTS_FP8 (E4M3 W8A8) */
+    void* stream;      /* cudaStream_t; NULL = default stream */
+} tts_config;
+
+/* Device pointers to the weights (borrowed).  The per-layer members are HOST
+ * arrays of n_layers device pointers.  wqkv/wo/wgu/wd point to bf16 matrices
+ * when precision == TTS_BF16 and to E4M3 matrices when precision == TTS_FP8;
+ * sqkv/so/sgu/sd (fp32 per-output-row scales) are used only for TTS_FP8 and
+ * may be NULL otherwise.  Norm gains are bf16.  The codebook embedding and
+ * head are bf16 in both precisions. */
+typedef struct {
+    const void* embed;        /* bf16 [n_codebooks][cb_vocab][hidden] */
+    const void* head;         /* bf16 [n_codebooks*cb_vocab][hidden] */
+    const void* final_norm;   /* bf16 [hidden] */
+    const void* const* wqkv;  /* [(n_q+2*n_kv)*head_dim][hidden] */
+    const void* const* wo;    /* [hidden][n_q*head_dim] */
+    const void* const* wgu;   /* [2*inter][hidden] */
+    const void* const* wd;    /* [hidden][inter] */
+    const float* const* sqkv; /* [(n_q+2*n_kv)*head_dim] */
+    const float* const* so;   /* [hidden] */
+    const float* const* sgu;  /* [2*inter] */
+    const float* const* sd;   /* [hidden] */
+    const void* const* ln_in;   /* [hidden]   input RMSNorm gain */
+    const void* const* ln_post; /* [hidden]   post-attention RMSNorm gain */
+    const void* const* q_norm;  /* [head_dim] per-head query RMSNorm gain */
+    const void* const* k_norm;  /* [head_dim] per-head key RMSNorm gain */
+} tts_weights;
+
+/* Create a context: validates the configuration, allocates the KV cache, the
+ * RoPE table and all step scratch, and captures the decode step as one CUDA
+ * graph that reads the position from device memory (so it replays at any
+ * position).  Position, frame and EOC state start at 0, 0, none.
+ * Source: FlashRT page, Performance ("position-agnostic CUDA graph") and
+ * section 7; the graph-lifetime rule (graph destroyed before memory is freed)
+ * follows the TTS-Audio-Suite report on CUDA-graph teardown. */
+int tts_init(const tts_config* cfg, const tts_weights* w, tts_ctx** out);
+
+/* Destroy the graph, then free everything the library allocated.  NULL is a
+ * no-op.  The context pointer is invalid afterwards. */
+int tts_shutdown(tts_ctx* ctx);
+
+/* Rewind: position 0, frame 0, no EOC.  KV contents are left stale (they are
+ * overwritten as positions are re-filled). */
+int tts_reset(tts_ctx* ctx);
+
+/* Batched prefill of P positions (FlashRT page, section 7 "Prefill is one
+ * batched M=P forward").  codes: HOST int32 [P][n_codebooks], each in
+ * [0, cb_vocab).  Runs the layer stack for positions pos..pos+P-1 and writes
+ * their K/V; no head, frame counter unchanged.  Afterwards the next decode
+ * step's input is the all-BOS frame.  Errors: TTS_ERR_FULL if pos+P > max_pos.
+ * Synchronises the stream. */
+int tts_prefill(tts_ctx* ctx, const int32_t* codes, int P);
+
+/* One decode step (FlashRT page, section 5).  codes_in: HOST int32
+ * [n_codebooks], the frame fed to the embedding (NULL = use the codes the
+ * previous step produced, or the all-BOS frame after a reset/prefill).
+ * codes_out: HOST int32 [n_codebooks], the step's greedy codes under the
+ * delay pattern (section 4, sampling policy).  Advances position and frame by
+ * one.  Errors: TTS_ERR_CODE, TTS_ERR_FULL.  Synchronises the stream. */
+int tts_decode_step(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out);
+
+/* n decode steps with device-side feedback: each step embeds the codes the
+ * previous one produced, without a host round trip (SGLang-Omni post, "AR
+ * backbone": one transfer per step batched away).  codes_out: HOST int32
+ * [n][n_codebooks] (may be NULL), copied back once at the end.  Errors:
+ * TTS_ERR_FULL if pos+n > max_pos.  Synchronises the stream. */
+int tts_decode_steps(tts_ctx* ctx, int n, int32_t* codes_out);
+
+/* Rewind to position pos (0 <= pos <= current position) and frame t, with no
+ * EOC: cache positions [0, pos) are kept and later ones are overwritten as
+ * decoding proceeds, so a prompt prefilled once can start many utterances
+ * (FlashRT page, section 4: a shared preamble's KV is reused and only new
+ * input is processed).  The next decode step's input is the all-BOS frame. */
+int tts_rewind(tts_ctx* ctx, int pos, int t);
+
+/* Copy a KV prefix into the cache and set the position to len.  k, v: DEVICE
+ * bf16 [n_layers][n_kv_heads][len_stride][head_dim] with len <= len_stride;
+ * positions [0, len) are copied.  Frame and EOC state are not changed. */
+int tts_set_kv(tts_ctx* ctx, const void* k, const void* v, int len, int len_stride);
+
+/* Copy cache positions [p0, p1) of every layer and kv head to HOST bf16
+ * buffers [n_layers][n_kv_heads][p1-p0][head_dim] (either may be NULL). */
+int tts_get_kv(tts_ctx* ctx, void* k_host, void* v_host, int p0, int p1);
+
+/* HOST fp32 [n_codebooks*cb_vocab]: the logits of the last decode step. */
+int tts_get_logits(tts_ctx* ctx, float* logits_host);
+
+/* HOST fp32 [hidden]: the residual stream after the last step or prefill
+ * position (the input of the final RMSNorm). */
+int tts_get_hidden(tts_ctx* ctx, float* hidden_host);
+
+/* Set the frame index and the EOC frame (-1 = none) used by the delay mask. */
+int tts_set_frame(tts_ctx* ctx, int t, int eoc_frame);
+
+/* Read position, frame index and EOC frame (any pointer may be NULL). */
+int tts_get_state(tts_ctx* ctx, int* pos, int* t, int* eoc_frame);
+
+/* Device time of the last tts_decode_steps() call in milliseconds, measured
+ * with CUDA events around the graph replays (inputs already resident). */
+int tts_last_steps_ms(tts_ctx* ctx, float* ms);
+
+/* Measurement hook (not part of the step): launch the GEMV of one projection
+ * kind -- 0 QKV, 1 O-proj, 2 gate/up, 3 down-proj, 4 codebook head (logits
+ * only, no argmax) -- once per layer's weights (the head n_layers times),
+ * `reps` rounds back to back on the context's stream with the step's launch
+ * configuration, and return the mean device time of one launch from CUDA
+ * events.  Overwrites step scratch (not the KV cache or the state): call it
+ * between steps.  Synchronises the stream. */
+int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch);
+
+/* Per-output-row FP8 weight quantisation on the GPU (FlashRT page,
+ * Performance "FP8 W8A8"; section 8, scale amax/448): for each row n,
+ * s[n] = max_k |W[n][k]| / 448 (1 if the row is zero) and
+ * W8[n][k] = E4M3(W[n][k] / s[n]) rounded to nearest even, saturating.
+ * W: DEVICE bf16 [N][K]; W8: DEVICE uint8 [N][K]; s: DEVICE fp32 [N].
+ * stream: cudaStream_t or NULL.  Asynchronous. */
+int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream);
+
+/* Name of a status code (static string). */
+const char* tts_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTS_DECODE_H */

@@ -1,0 +1,170 @@
+"""GPU parity of the decode step against the CPU oracle, through the C ABI.
+
+Reduced-width backbones (two layers, same head structure) exercise several
+attention splits, the ragged last split, the delay mask and the FP8 path in
+seconds; the single-layer full-width case is the one-layer workload (hidden
+2560, 32q/8kv, 9728, 8 x 1026 head, 64 cached positions).  Inputs are seeded
+synthetic draws (synth); the oracle sees exactly the same inputs."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import check_frame, reduced_dims, to_binding_dims, upload_kv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ads():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import ar_decode_step_gb300.build as b
+    b.build()
+    import ar_decode_step_gb300 as m
+    m.load()
+    return m
+
+
+def make_pair(ads, dims, max_pos, precision, gamma_variant=False, std=0.02):
+    w = synth.make_weights(dims, std=std, gamma_variant=gamma_variant)
+    dw = ads.DeviceWeights(w, precision=precision)
+    dec = ads.Decoder(to_binding_dims(dims), dw, max_pos)
+    orc = oracle.Oracle(w, max_pos, precision=precision)
+    return w, dec, orc
+
+
+def run_teacher_forced(dec, orc, codes, t0, fp8, where):
+    dec.set_frame(t0)
+    orc.set_frame(t0)
+    stats = []
+    for f, cin in enumerate(codes):
+        t = t0 + f
+        eoc = orc.st.eoc
+        g_codes = dec.decode_step(cin)
+        g_logits = dec.get_logits()
+        o_codes, o_logits, o_gaps = orc.decode_step(cin)
+        stats.append(check_frame(g_codes, g_logits, o_codes, o_logits, o_gaps, fp8, t, eoc,
+                                 f"{where} frame {f}"))
+    return stats
+
+
+@pytest.mark.parametrize("precision", [0, 1], ids=["bf16", "fp8"])
+def test_reduced_teacher_forced_with_kv_prefix(ads, precision):
+    d = reduced_dims(2)
+    max_pos = 64
+    w, dec, orc = make_pair(ads, d, max_pos, precision, gamma_variant=True)
+    k, v = synth.make_kv_prefix(d, 40, max_pos)
+    kd, vd = upload_kv(k, v, 40)
+    dec.set_kv(kd, vd, 40)
+    orc.set_kv(k, v, 40)
+    codes = synth.random_codes(6, seed=2, stream=1)
+    stats = run_teacher_forced(dec, orc, codes, 3, precision == 1, "reduced")
+    assert sum(s[2] for s in stats) >= 24
+    assert dec.state()[0] == orc.pos == 46
+    # the K/V rows the GPU wrote match the oracle's to within one bf16 rounding
+    gk, gv = dec.get_kv(40, 46)
+    ok, ov = orc.k[:, :, 40:46], orc.v[:, :, 40:46]
+    f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.allclose(f(gk), f(ok), rtol=2 ** -6, atol=1e-3)
+    assert np.allclose(f(gv), f(ov), rtol=2 ** -6, atol=1e-3)
+    # the untouched prefix is byte-identical
+    gk0, _ = dec.get_kv(0, 40)
+    assert np.array_equal(gk0, k[:, :, :40])
+    dec.close()
+
+
+def test_reduced_from_empty_cache_and_eoc(ads):
+    """Positions 0.. (single split, the new row only) and a forced EOC."""
+    d = reduced_dims(2)
+    w, dec, orc = make_pair(ads, d, 32, 0)
+    codes = synth.random_codes(5, seed=2, stream=2)
+    run_teacher_forced(dec, orc, codes[:2], 0, False, "empty")
+    # pretend codebook 0 emitted EOC at frame 1: the mask forces 1025 from t >= 1 + k
+    dec.set_frame(4, 1)
+    orc.set_frame(4, 1)
+    for f in range(3):
+        g = dec.decode_step(codes[2 + f])
+        o, ol, og = orc.decode_step(codes[2 + f])
+        check_frame(g, dec.get_logits(), o, ol, og, False, 4 + f, 1, f"eoc frame {f}")
+        assert (g[: 4 + f - 1 + 1] == 1025).all()
+    dec.close()
+
+
+def test_free_run_equals_stepwise(ads):
+    d = reduced_dims(2)
+    w = synth.make_weights(d)
+    dw = ads.DeviceWeights(w)
+    a = ads.Decoder(to_binding_dims(d), dw, 48)
+    b = ads.Decoder(to_binding_dims(d), dw, 48)
+    prompt = synth.delayed_prompt_codes(5)
+    a.prefill(prompt)
+    b.prefill(prompt)
+    run = a.decode_steps(12)
+    steps = np.stack([b.decode_step() for _ in range(12)])
+    assert np.array_equal(run, steps)
+    assert a.state() == b.state() == (17, 12, a.state()[2])
+    # delay pattern on the free run: codebook k is BOS-pad for t < k
+    for t in range(8):
+        assert (run[t, t + 1:] == 1024).all()
+    assert np.array_equal(a.get_logits(), b.get_logits())
+    a.close()
+    b.close()
+
+
+def test_prefill_matches_oracle(ads):
+    d = reduced_dims(2)
+    w, dec, orc = make_pair(ads, d, 40, 0, gamma_variant=True)
+    prompt = synth.delayed_prompt_codes(9, stream=1)
+    dec.prefill(prompt[:4])
+    dec.prefill(prompt[4:])
+    orc.prefill(prompt)
+    assert dec.state()[0] == orc.pos == 9
+    gk, gv = dec.get_kv(0, 9)
+    f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.allclose(f(gk), f(orc.k[:, :, :9]), rtol=2 ** -6, atol=1e-3)
+    assert np.allclose(f(gv), f(orc.v[:, :, :9]), rtol=2 ** -6, atol=1e-3)
+    # the frame after a prefill is the all-BOS frame at t = 0
+    g = dec.decode_step()
+    o, ol, og = orc.decode_step(np.full(8, 1024, np.int32))
+    check_frame(g, dec.get_logits(), o, ol, og, False, 0, -1, "after prefill")
+    dec.close()
+
+
+@pytest.mark.parametrize("t0", [0, 8])
+def test_one_layer_full_width(ads, t0):
+    """One full-width layer, 64 cached N(0,1) positions, one step from random codes."""
+    d = synth.Dims(n_layers=1)
+    w, dec, orc = make_pair(ads, d, 128, 0)
+    k, v = synth.make_kv_prefix(d, 64, 128)
+    kd, vd = upload_kv(k, v, 64)
+    dec.set_kv(kd, vd, 64)
+    orc.set_kv(k, v, 64)
+    codes = synth.random_codes(2, seed=2)
+    stats = run_teacher_forced(dec, orc, codes, t0, False, f"one-layer t0={t0}")
+    print("one-layer", stats)
+    dec.close()
+
+
+def test_errors_leave_state_unchanged(ads):
+    d = reduced_dims(1)
+    w = synth.make_weights(d)
+    dw = ads.DeviceWeights(w)
+    dec = ads.Decoder(to_binding_dims(d), dw, 4)
+    bad = np.zeros(8, np.int32)
+    bad[3] = 1026
+    with pytest.raises(ads.TtsError) as e:
+        dec.decode_step(bad)
+    assert e.value.status == -2
+    with pytest.raises(ads.TtsError) as e:
+        dec.prefill(np.zeros((5, 8), np.int32))
+    assert e.value.status == -3
+    assert dec.state()[0] == 0
+    dec.decode_steps(4)
+    with pytest.raises(ads.TtsError) as e:
+        dec.decode_step()
+    assert e.value.status == -3
+    assert dec.state()[0] == 4
+    dec.reset()
+    assert dec.state() == (0, 0, -1)
+    dec.close()
