@@ -66,6 +66,7 @@ SIGNATURES = {
     "tts_last_steps_ms": (_I, [_VP, _VP]),
     "tts_time_gemv": (_I, [_VP, _I, _I, _VP]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
+    "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_status_str": (ctypes.c_char_p, [_I]),
 }
 
@@ -127,6 +128,14 @@ def quantize_fp8_weight(w_dev, stream=None):
     _call("tts_quantize_fp8_weight", w_dev.data_ptr(), N, K, q.data_ptr(), s.data_ptr(),
           stream if stream is not None else None)
     return q, s
+
+
+def attention_decode(qkv, q_norm, k_norm, k_cache, v_cache, out, n_q: int, n_kv: int, pos: int,
+                     eps: float = 1e-6, rope_theta: float = 1e6, stream=None) -> None:
+    """tts_attention_decode on torch device tensors (fp32 qkv/out, int16 bf16 bits)."""
+    max_pos = k_cache.shape[-2]
+    _call("tts_attention_decode", qkv.data_ptr(), q_norm.data_ptr(), k_norm.data_ptr(), k_cache.data_ptr(),
+          v_cache.data_ptr(), out.data_ptr(), n_q, n_kv, max_pos, pos, eps, rope_theta, stream)
 
 
 @dataclass

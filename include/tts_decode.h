@@ -191,6 +191,25 @@ int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch);
  * stream: cudaStream_t or NULL.  Asynchronous. */
 int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream);
 
+/* One layer's decode attention as a standalone call, outside a context: the
+ * kernel the step uses ("Higgs Audio v3 TTS-4B on FlashRT", section 5: fused
+ * q/k-norm + RoPE, KV write, attention).  For position pos it RMS-normalises
+ * each query and key head over head_dim 128 (gains q_norm / k_norm), rotates
+ * them (rotate-half RoPE, inverse frequencies rope_theta^(-2i/128)), writes the
+ * key and value rows of pos to the caches in bf16, and attends the n_q query
+ * heads over positions [0, pos] (query head h reads key-value head
+ * h / (n_q/n_kv); scores scaled by 1/sqrt(128); softmax over positions).
+ * qkv: DEVICE fp32 [(n_q + 2*n_kv)*128] (queries, keys, values);
+ * q_norm, k_norm: DEVICE bf16 [128]; k_cache, v_cache: DEVICE bf16
+ * [n_kv][max_pos][128] (row pos of each head is overwritten);
+ * out: DEVICE fp32 [n_q*128].  n_q/n_kv in {1,2,4,8}; 0 <= pos < max_pos <=
+ * 65536 (TTS_ERR_FULL otherwise).  Scratch for the split partials is taken
+ * from the stream-ordered allocator and released before returning.
+ * Synchronises the stream. */
+int tts_attention_decode(const float* qkv, const void* q_norm, const void* k_norm, void* k_cache,
+                         void* v_cache, float* out, int n_q, int n_kv, int max_pos, int pos, float eps,
+                         float rope_theta, void* stream);
+
 /* Name of a status code (static string). */
 const char* tts_status_str(int status);
 
