@@ -67,6 +67,7 @@ SIGNATURES = {
     "tts_time_gemv": (_I, [_VP, _I, _I, _VP]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
+    "tts_attention_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_status_str": (ctypes.c_char_p, [_I]),
 }
 

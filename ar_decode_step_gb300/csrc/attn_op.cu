@@ -3,6 +3,7 @@
 // plain pointers, outside a context.
 #include <cmath>
 #include <cstdio>
+#include <mutex>
 
 #include "kernels.h"
 #include "tts_decode.h"
@@ -117,4 +118,77 @@ extern "C" int tts_attention_decode(const float* qkv, const void* q_norm, const 
     if (cudaStreamSynchronize(s) != cudaSuccess) return TTS_ERR_CUDA;
     if (e != cudaSuccess) std::fprintf(stderr, "tts: attention launch failed: %s\n", cudaGetErrorString(e));
     return rc;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot allocate device memory at the
+// point of the call: code running inside another runtime's memory budget, a
+// caller holding no allocator of its own (an embedded or real-time host loop
+// that must never hit cudaMalloc's implicit synchronisation or failure), or a
+// process whose allocations are frozen after start-up.  This entry point takes
+// its scratch from one fixed array in device global memory instead.  The
+// array exists on every GPU that loads the library and stays there until the
+// process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;  // 2 MiB
+__device__ __align__(256) char g_attn_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+int static_scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TTS_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TTS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+        if (e != cudaSuccess) {
+            std::fprintf(stderr, "tts: cudaGetSymbolAddress of the static scratch failed: %s\n",
+                         cudaGetErrorString(e));
+            return TTS_ERR_CUDA;
+        }
+        g_static_addr[dev] = p;
+    }
+    *out = g_static_addr[dev];
+    return TTS_OK;
+}
+
+}  // namespace
+
+extern "C" int tts_attention_decode_noalloc(const float* qkv, const void* q_norm, const void* k_norm,
+                                            void* k_cache, void* v_cache, float* out, int n_q, int n_kv,
+                                            int max_pos, int pos, float eps, float rope_theta, void* stream) {
+    int rc = check_args(qkv, q_norm, k_norm, k_cache, v_cache, out, n_q, n_kv, max_pos, pos);
+    if (rc != TTS_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int S = attn_splits_for(max_pos);
+    const AttnScratch L = scratch_layout(n_q, n_kv, S);
+    if (L.total > kStaticScratchBytes) {
+        std::fprintf(stderr,
+                     "tts_attention_decode_noalloc: n_q=%d, max_pos=%d needs %zu bytes of scratch; "
+                     "the static array holds %zu\n",
+                     n_q, max_pos, L.total, kStaticScratchBytes);
+        return TTS_ERR_ARG;
+    }
+    void* base = nullptr;
+    rc = static_scratch_address(&base);
+    if (rc != TTS_OK) return rc;
+    char* scratch = static_cast<char*>(base);
+    // run_attention zeroes the tickets and the state word before the launch;
+    // the partial buffers are fully written before they are read.
+    const cudaError_t e = run_attention(scratch, L, qkv, q_norm, k_norm, k_cache, v_cache, out, n_q, n_kv,
+                                        max_pos, pos, eps, rope_theta, S, s);
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "tts: attention launch failed: %s\n", cudaGetErrorString(e));
+        return TTS_ERR_CUDA;
+    }
+    return read_err(scratch, L, s);
 }

@@ -210,6 +210,27 @@ int tts_attention_decode(const float* qkv, const void* q_norm, const void* k_nor
                          void* v_cache, float* out, int n_q, int n_kv, int max_pos, int pos, float eps,
                          float rope_theta, void* stream);
 
+/* tts_attention_decode without any allocation, for callers that cannot
+ * allocate device memory during the call: code running under another
+ * runtime's fixed memory budget, host loops that must not block on or fail in
+ * cudaMalloc, or processes that freeze allocation after start-up.  The paper
+ * has no counterpart; this is a library-level variant.
+ * Same arguments, layouts and result as tts_attention_decode.  Its scratch (the
+ * split partials, tickets, a state word and the RoPE row) lives in one static
+ * device array of 2 MiB per GPU, held from library load until process exit.
+ * Requests needing more (about n_q * min(64, ceil(max_pos/16)) * 520 bytes)
+ * are rejected with TTS_ERR_ARG and a message on stderr; nothing is launched.
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it: make that first call before any stream
+ * capture.  Every call shares the one array, and each call clears the tickets
+ * and state word before launching, so calls that overlap on the GPU (on
+ * different streams, or without ordering) race on it: serialise them.  No
+ * cudaMalloc, cudaFree or other allocating routine is called.  Synchronises
+ * the stream. */
+int tts_attention_decode_noalloc(const float* qkv, const void* q_norm, const void* k_norm, void* k_cache,
+                                 void* v_cache, float* out, int n_q, int n_kv, int max_pos, int pos,
+                                 float eps, float rope_theta, void* stream);
+
 /* Name of a status code (static string). */
 const char* tts_status_str(int status);
 
