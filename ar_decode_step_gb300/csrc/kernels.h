@@ -25,6 +25,22 @@ struct GemvParams {
     int n_cb, cb_vocab;
     int* hist;                  // code history ring [hist_cap][n_cb]
     int hist_cap;
+    int* err;                   // error word (DevState::err), may be NULL
+    // L2 prefetch of the next projection's weights once this kernel's copies are out:
+    // rows split over the grid like this kernel's; next_pf bytes per CTA (0 = none)
+    const void* next_W;
+    int next_N;
+    size_t next_rowb;
+    size_t next_pf;
+    // ring geometry, filled in by launch_gemv
+    int rs, nstages, part_bytes;
+};
+
+// Shared-memory geometry of one GEMV launch: rows per ring stage, ring stages,
+// bytes of the per-(row, segment) partial sums, total dynamic smem.
+struct GemvGeom {
+    int rs, nstages, part_bytes, smem;
+    bool ok;
 };
 
 struct LaunchCfg {
@@ -33,7 +49,8 @@ struct LaunchCfg {
     bool pdl;
 };
 
-int gemv_smem_bytes(int prec, int K);
+GemvGeom gemv_geom(int prec, int epi, int N, int K, int grid);
+cudaError_t gemv_prepare();  // raise the dynamic shared-memory limit of every variant
 cudaError_t launch_gemv(int prec, int pro, int epi, const GemvParams& p, const LaunchCfg& lc,
                         cudaStream_t s);
 

@@ -124,22 +124,62 @@ int dalloc(tts_ctx* c, T** p, size_t count) {
         if (r_ != TTS_OK) return r_; \
     } while (0)
 
-LaunchCfg gemv_cfg(const tts_ctx* c, bool pdl) { return LaunchCfg{c->num_sms, 256, pdl}; }
+LaunchCfg gemv_cfg(const tts_ctx* c, bool pdl) { return LaunchCfg{c->num_sms, 0, pdl}; }
+
+enum Proj { kQKV = 0, kO = 1, kGU = 2, kDown = 3, kHead = 4 };
+
+// Parameters of projection `kind` of layer l (kHead ignores l).
+GemvParams proj_params(const tts_ctx* c, int kind, int l) {
+    const tts_config& k = c->cfg;
+    GemvParams g{};
+    g.eps = k.rms_eps;
+    g.err = &c->st->err;
+    if (kind == kHead) {
+        g.W = c->head; g.x = c->h; g.gamma = c->final_norm; g.y = c->logits;
+        g.N = k.n_codebooks * k.cb_vocab; g.K = k.hidden;
+        return g;
+    }
+    const LayerW& w = c->L[l];
+    switch (kind) {
+        case kQKV: g.W = w.wqkv; g.wscale = w.sqkv; g.x = c->h; g.gamma = w.ln_in; g.y = c->qkv;
+                   g.N = c->qkv_rows; g.K = k.hidden; break;
+        case kO:   g.W = w.wo; g.wscale = w.so; g.x = c->attn; g.y = c->h; g.N = k.hidden; g.K = c->attn_dim; break;
+        case kGU:  g.W = w.wgu; g.wscale = w.sgu; g.x = c->h; g.gamma = w.ln_post; g.y = c->act;
+                   g.N = k.inter; g.K = k.hidden; break;
+        default:   g.W = w.wd; g.wscale = w.sd; g.x = c->act; g.y = c->h; g.N = k.hidden; g.K = k.inter; break;
+    }
+    return g;
+}
+
+// Point g's L2 prefetch at projection `kind` of layer l (the one launched next).
+void set_next(const tts_ctx* c, GemvParams& g, int kind, int l, size_t pf_bytes) {
+    const GemvParams n = proj_params(c, kind, l);
+    const size_t wb = (kind == kHead || c->cfg.precision == TTS_BF16) ? 2 : 1;
+    g.next_W = n.W;
+    g.next_N = n.N;
+    g.next_rowb = (size_t)n.K * wb;
+    g.next_pf = pf_bytes;
+}
+
+size_t env_kb(const char* name, size_t dflt) {
+    const char* v = std::getenv(name);
+    return (v && *v) ? (size_t)std::strtoul(v, nullptr, 10) * 1024 : dflt * 1024;
+}
 
 // Enqueue one position through the layer stack, then either the head (decode)
 // or the prefill advance.
 int record_step(tts_ctx* c, cudaStream_t s, bool decode) {
     const tts_config& k = c->cfg;
     const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    const size_t pf = env_kb("TTS_PF_KB", 96), pf_attn = env_kb("TTS_PF_ATTN_KB", 160);
     EmbedParams ep{c->embed, c->st, decode ? nullptr : c->prompt, c->h, k.n_codebooks, k.cb_vocab, k.hidden};
     TTS_CK(launch_embed(ep, LaunchCfg{0, 0, false}, s));
     for (int l = 0; l < k.n_layers; ++l) {
         const LayerW& w = c->L[l];
-        GemvParams g{};
-        g.eps = k.rms_eps;
+        const bool last = l + 1 == k.n_layers;
         // QKV: input RMSNorm (+ FP8 quant) fused in the prologue
-        g.W = w.wqkv; g.wscale = w.sqkv; g.x = c->h; g.gamma = w.ln_in; g.y = c->qkv;
-        g.N = c->qkv_rows; g.K = k.hidden;
+        GemvParams g = proj_params(c, kQKV, l);
+        set_next(c, g, kO, l, pf_attn);
         TTS_CK(launch_gemv(prec, kProRms, kEpiStore, g, gemv_cfg(c, c->pdl), s));
         // attention with q/k norm + RoPE + KV write
         AttnParams a{};
@@ -151,24 +191,22 @@ int record_step(tts_ctx* c, cudaStream_t s, bool decode) {
         a.n_q = k.n_q_heads; a.n_kv = k.n_kv_heads; a.max_pos = k.max_pos; a.S = c->S; a.eps = k.rms_eps;
         TTS_CK(launch_attention(a, LaunchCfg{0, 0, c->pdl}, s));
         // O-proj with residual add into h
-        g = GemvParams{};
-        g.W = w.wo; g.wscale = w.so; g.x = c->attn; g.y = c->h; g.N = k.hidden; g.K = c->attn_dim;
+        g = proj_params(c, kO, l);
+        set_next(c, g, kGU, l, pf);
         TTS_CK(launch_gemv(prec, kProPlain, kEpiResid, g, gemv_cfg(c, c->pdl), s));
         // post-attention RMSNorm + gate/up + SwiGLU
-        g = GemvParams{};
-        g.eps = k.rms_eps;
-        g.W = w.wgu; g.wscale = w.sgu; g.x = c->h; g.gamma = w.ln_post; g.y = c->act; g.N = k.inter; g.K = k.hidden;
+        g = proj_params(c, kGU, l);
+        set_next(c, g, kDown, l, pf);
         TTS_CK(launch_gemv(prec, kProRms, kEpiSwiglu, g, gemv_cfg(c, c->pdl), s));
         // down-proj with residual add into h
-        g = GemvParams{};
-        g.W = w.wd; g.wscale = w.sd; g.x = c->act; g.y = c->h; g.N = k.hidden; g.K = k.inter;
+        g = proj_params(c, kDown, l);
+        if (!last) set_next(c, g, kQKV, l + 1, pf);
+        else if (decode) set_next(c, g, kHead, 0, pf);
         TTS_CK(launch_gemv(prec, kProPlain, kEpiResid, g, gemv_cfg(c, c->pdl), s));
     }
     if (decode) {
-        GemvParams g{};
-        g.eps = k.rms_eps;
-        g.W = c->head; g.x = c->h; g.gamma = c->final_norm; g.y = c->logits;
-        g.N = k.n_codebooks * k.cb_vocab; g.K = k.hidden;
+        GemvParams g = proj_params(c, kHead, 0);
+        set_next(c, g, kQKV, 0, pf);  // the next frame starts with layer 0's QKV
         g.st = c->st; g.counter = c->counters + k.n_kv_heads; g.n_cb = k.n_codebooks; g.cb_vocab = k.cb_vocab;
         g.hist = c->hist; g.hist_cap = k.max_pos;
         TTS_CK(launch_gemv(kBF16, kProRms, kEpiLogits, g, gemv_cfg(c, c->pdl), s));
@@ -237,6 +275,7 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     c->pdl = !(nopdl && nopdl[0] == '1');
 
     TTS_CK(cudaGetDevice(&c->device));
+    TTS_CK(gemv_prepare());
     TTS_CK(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
     TTS_CK(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking));
     TTS_CK(cudaEventCreate(&c->ev0));
@@ -342,6 +381,9 @@ int tts_shutdown(tts_ctx* ctx) {
 
 int tts_reset(tts_ctx* ctx) {
     if (!ctx) return TTS_ERR_STATE;
+    // tickets are zero after every complete step; clear them in case a step
+    // was cut short by a device error
+    TTS_CK(cudaMemsetAsync(ctx->counters, 0, 2 * ctx->cfg.n_kv_heads * sizeof(unsigned), ctx->stream));
     return push_state(ctx, bos_state(ctx, 0, 0, -1));
 }
 
@@ -494,27 +536,16 @@ int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch) {
     if (!ctx) return TTS_ERR_STATE;
     if (kind < 0 || kind > 4 || reps < 1 || !ms_per_launch) return TTS_ERR_ARG;
     const tts_config& k = ctx->cfg;
-    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    const int prec = (kind == kHead || k.precision == TTS_BF16) ? kBF16 : kFP8;
+    const int pro = (kind == kO || kind == kDown) ? kProPlain : kProRms;
+    const int epi = kind == kGU ? kEpiSwiglu : ((kind == kO || kind == kDown) ? kEpiResid : kEpiStore);
+    const size_t pf = env_kb("TTS_PF_KB", 96);
     TTS_CK(cudaEventRecord(ctx->ev0, ctx->stream));
     for (int r = 0; r < reps; ++r)
         for (int l = 0; l < k.n_layers; ++l) {
-            const LayerW& w = ctx->L[l];
-            GemvParams g{};
-            g.eps = k.rms_eps;
-            int pro = kProRms, epi = kEpiStore, p = prec;
-            switch (kind) {
-                case 0: g.W = w.wqkv; g.wscale = w.sqkv; g.x = ctx->h; g.gamma = w.ln_in; g.y = ctx->qkv;
-                        g.N = ctx->qkv_rows; g.K = k.hidden; break;
-                case 1: g.W = w.wo; g.wscale = w.so; g.x = ctx->attn; g.y = ctx->h; g.N = k.hidden;
-                        g.K = ctx->attn_dim; pro = kProPlain; epi = kEpiResid; break;
-                case 2: g.W = w.wgu; g.wscale = w.sgu; g.x = ctx->h; g.gamma = w.ln_post; g.y = ctx->act;
-                        g.N = k.inter; g.K = k.hidden; epi = kEpiSwiglu; break;
-                case 3: g.W = w.wd; g.wscale = w.sd; g.x = ctx->act; g.y = ctx->h; g.N = k.hidden;
-                        g.K = k.inter; pro = kProPlain; epi = kEpiResid; break;
-                default: g.W = ctx->head; g.x = ctx->h; g.gamma = ctx->final_norm; g.y = ctx->logits;
-                         g.N = k.n_codebooks * k.cb_vocab; g.K = k.hidden; p = kBF16; break;
-            }
-            TTS_CK(launch_gemv(p, pro, epi, g, gemv_cfg(ctx, ctx->pdl && (r | l)), ctx->stream));
+            GemvParams g = proj_params(ctx, kind, l);
+            set_next(ctx, g, kind, (l + 1) % k.n_layers, pf);
+            TTS_CK(launch_gemv(prec, pro, epi, g, gemv_cfg(ctx, ctx->pdl && (r | l)), ctx->stream));
         }
     TTS_CK(cudaEventRecord(ctx->ev1, ctx->stream));
     TTS_CK(cudaEventSynchronize(ctx->ev1));
