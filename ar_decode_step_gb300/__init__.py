@@ -65,6 +65,7 @@ SIGNATURES = {
     "tts_get_state": (_I, [_VP, _VP, _VP, _VP]),
     "tts_last_steps_ms": (_I, [_VP, _VP]),
     "tts_time_gemv": (_I, [_VP, _I, _I, _VP]),
+    "tts_trace_step": (_I, [_VP, _VP, _I, _VP, _VP]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_attention_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -293,6 +294,17 @@ class Decoder:
         ms = ctypes.c_float()
         _call("tts_time_gemv", self._ctx, kind, reps, ctypes.byref(ms))
         return ms.value
+
+    def trace_step(self, n_sms_max: int = 1024):
+        """One decode step with the persistent kernel's phase trace: uint64 ns
+        stamps shaped [n_cta][stride]."""
+        cap = n_sms_max * (8 + 27 * self.dims.n_layers) + 2 * 4 * 2048
+        buf = np.zeros(cap, np.uint64)
+        st, nc = ctypes.c_int(), ctypes.c_int()
+        _call("tts_trace_step", self._ctx, _ptr(buf), cap, ctypes.byref(st), ctypes.byref(nc))
+        n = st.value * nc.value
+        self.last_stage_trace = buf[n: n + 2 * 4 * 2048].reshape(2, 2048, 4)
+        return buf[:n].reshape(nc.value, st.value)
 
     def last_steps_ms(self) -> float:
         ms = ctypes.c_float()

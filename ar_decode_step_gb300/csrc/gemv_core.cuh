@@ -1,0 +1,644 @@
+// Building blocks of the M = 1 weight-streaming projections, shared by the
+// per-projection GEMV kernel (gemv.cu) and the persistent decode-step kernel
+// (step.cu).  A CTA = one producer warp + kConsumerWarps consumer warps.
+//
+// Producer: streams the CTA's row range of a weight matrix through a ring of
+// shared-memory stages.  A stage is a group of RS whole rows (RS a power of
+// two, up to 40 KB) filled by one bulk copy on the TMA engine (two for
+// gate/up: RS/2 gate rows and the matching RS/2 up rows); completion is
+// counted on the slot's "full" mbarrier, consumers free the slot on its
+// "empty" mbarrier.
+//
+// Consumers: warp w owns column segment w % WPR of row slot w / WPR (WPR
+// segments per row, stage_geom); a stage's rows are taken one row slot per
+// pass: equal bytes per warp, direct activation indexing, one shuffle
+// reduction per row.  Per-(row, segment) partials are summed in segment order
+// (deterministic) before the epilogue.
+//
+// Activations: staged in shared memory once per projection, fp32 planes for
+// bf16 weights, f16 planes (exact E4M3 values) for FP8 weights, which are
+// multiplied with the mixed-precision f16 x f16 + f32 FMA.
+#pragma once
+
+#include <type_traits>
+
+#include "kernels.h"
+
+namespace tts {
+namespace core {
+
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp (the last)
+constexpr int kMaxStages = 8;
+constexpr int kBarrierBytes = 128;         // room for 8 full + 8 empty barriers
+
+// ---- chunk dot products ------------------------------------------------------
+// BF16: 8 weights x fp32 activations held as two float4 planes; two
+// independent FMA chains (even / odd elements) for instruction-level overlap.
+__device__ __forceinline__ void dot_bf16(const uint4 w, const float4 a, const float4 b, float& e, float& o) {
+    e = fmaf(bf16lo(w.x), a.x, e);
+    o = fmaf(bf16hi(w.x), a.y, o);
+    e = fmaf(bf16lo(w.y), a.z, e);
+    o = fmaf(bf16hi(w.y), a.w, o);
+    e = fmaf(bf16lo(w.z), b.x, e);
+    o = fmaf(bf16hi(w.z), b.y, o);
+    e = fmaf(bf16lo(w.w), b.z, e);
+    o = fmaf(bf16hi(w.w), b.w, o);
+}
+
+// Two E4M3 weights (low 16 bits of w) times two f16 activations, f32 accumulate.
+__device__ __forceinline__ float fma2_e4m3_f16(uint32_t w16, uint32_t x2, float acc) {
+    const __half2_raw wh = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w16 & 0xffffu), __NV_E4M3);
+    const uint32_t w2 = (uint32_t)wh.x | ((uint32_t)wh.y << 16);
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w2), "r"(x2));
+    return acc;
+}
+
+// FP8: 16 weights x f16 activations held as two planes of 8 f16; two chains.
+__device__ __forceinline__ void dot_fp8(const uint4 w, const uint4 a, const uint4 b, float& e, float& o) {
+    e = fma2_e4m3_f16(w.x, a.x, e);
+    o = fma2_e4m3_f16(w.x >> 16, a.y, o);
+    e = fma2_e4m3_f16(w.y, a.z, e);
+    o = fma2_e4m3_f16(w.y >> 16, a.w, o);
+    e = fma2_e4m3_f16(w.z, b.x, e);
+    o = fma2_e4m3_f16(w.z >> 16, b.y, o);
+    e = fma2_e4m3_f16(w.w, b.z, e);
+    o = fma2_e4m3_f16(w.w >> 16, b.w, o);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Barrier among the consumer warps only (the producer warp does not take part).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+__device__ __forceinline__ float consumer_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum(v);
+    consumer_sync();
+    if (lane == 0) red[warp] = v;
+    consumer_sync();
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) s += red[i];  // fixed order: deterministic
+    consumer_sync();
+    return s;
+}
+__device__ __forceinline__ float consumer_max(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max(v);
+    consumer_sync();
+    if (lane == 0) red[warp] = v;
+    consumer_sync();
+    float s = red[0];
+#pragma unroll
+    for (int i = 1; i < kConsumerWarps; ++i) s = fmaxf(s, red[i]);
+    consumer_sync();
+    return s;
+}
+
+// ---- one projection as seen by one CTA ---------------------------------------
+struct Proj {
+    const unsigned char* W;  // [rows][K] weights (gate/up: 2N rows)
+    const float* wscale;     // FP8 per-row scales
+    float* y;                // output (or the residual stream for kEpiResid)
+    int N, K;                // outputs, inner dimension
+    int rs;                  // rows per ring stage
+    int wpr;                 // column segments per row
+    int fp8;                 // weights are E4M3 (else bf16)
+    int swiglu;              // rows [0,N) gate, [N,2N) up
+    int r0, r1;              // this CTA's output rows [r0, r1) (proj_split_rows)
+};
+
+// Output rows of this CTA: an even split of N over the grid.
+__device__ __forceinline__ void proj_split_rows(Proj& j) {
+    j.r0 = (int)((long long)blockIdx.x * j.N / gridDim.x);
+    j.r1 = (int)((long long)(blockIdx.x + 1) * j.N / gridDim.x);
+}
+
+// Hides v's value from the optimiser: what is derived from it is computed
+// where it is used instead of being hoisted out of loops and kept in registers.
+__device__ __forceinline__ int opaque(int v) {
+    asm volatile("" : "+r"(v));
+    return v;
+}
+__device__ __forceinline__ unsigned char* opaque_ptr(unsigned char* v) {
+    asm volatile("" : "+l"(v));
+    return v;
+}
+
+__device__ __forceinline__ int proj_cpr(const Proj& j) { return j.K / (j.fp8 ? 16 : 8); }
+__device__ __forceinline__ int proj_opst(const Proj& j) { return j.swiglu ? j.rs / 2 : j.rs; }
+__device__ __forceinline__ void proj_rows(const Proj& j, int& r0, int& r1) {
+    r0 = j.r0;
+    r1 = j.r1;
+}
+__device__ __forceinline__ int proj_stages(const Proj& j) {
+    int r0, r1;
+    proj_rows(j, r0, r1);
+    const int opst = proj_opst(j);
+    return (r1 - r0 + opst - 1) / opst;
+}
+
+// Ring of shared-memory stages; `it` counts stages since the ring was set up
+// (producer and consumers each keep their own copy, in step).
+struct Ring {
+    uint64_t* full;
+    uint64_t* empty;
+    unsigned char* buf;
+    uint32_t slot_bytes;
+    int ns;
+};
+
+__device__ __forceinline__ void ring_init(const Ring& r) {
+    for (int s = 0; s < r.ns; ++s) {
+        mbar_init(&r.full[s], 1);
+        mbar_init(&r.empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+}
+
+// Producer (one thread): copy stage s of projection j into the next ring slot
+// (advancing it).  Returns false (and sets *abort) if a wait ran out.
+__device__ __forceinline__ bool produce_stage(const Proj& j, int s, const Ring& ring, int& it, uint64_t pol,
+                                              volatile int* abort, int* err, unsigned long long* wait_ns = nullptr,
+                                              unsigned long long* stage_tr = nullptr, int stage_tr_n = 0) {
+    int r0, r1;
+    proj_rows(j, r0, r1);
+    const size_t rowb = (size_t)proj_cpr(j) * 16;
+    const int opst = proj_opst(j);
+    const int slot = it % ring.ns;
+    const uint64_t tw = wait_ns ? globaltimer_ns() : 0;
+    const bool got = mbar_wait_or_abort(&ring.empty[slot], ((it / ring.ns) & 1) ^ 1, abort);
+    if (wait_ns) *wait_ns += globaltimer_ns() - tw;
+    if (!got) {
+        if (err) atomicOr(err, kErrTimeout);
+        *abort = 1;
+        return false;
+    }
+    const int o0 = r0 + s * opst;
+    const int no = min(opst, r1 - o0);
+    unsigned char* dst = ring.buf + (size_t)slot * ring.slot_bytes;
+    if (stage_tr && it < stage_tr_n) stage_tr[4 * it] = globaltimer_ns();
+    if (j.swiglu) {
+        mbar_arrive_expect_tx(&ring.full[slot], (uint32_t)(2 * no * rowb));
+        bulk_g2s(dst, j.W + (size_t)o0 * rowb, (uint32_t)(no * rowb), &ring.full[slot], pol);
+        bulk_g2s(dst + (size_t)opst * rowb, j.W + ((size_t)j.N + o0) * rowb, (uint32_t)(no * rowb),
+                 &ring.full[slot], pol);
+    } else {
+        mbar_arrive_expect_tx(&ring.full[slot], (uint32_t)(no * rowb));
+        bulk_g2s(dst, j.W + (size_t)o0 * rowb, (uint32_t)(no * rowb), &ring.full[slot], pol);
+    }
+    ++it;
+    return true;
+}
+
+// Producer (one thread): stream projection j's rows of this CTA into the ring.
+// Returns false (and sets *abort) if a wait ran out.
+__device__ __forceinline__ bool produce(const Proj& j, const Ring& ring, int& it, uint64_t pol,
+                                        volatile int* abort, int* err) {
+    int r0, r1;
+    proj_rows(j, r0, r1);
+    const size_t rowb = (size_t)proj_cpr(j) * 16;
+    const int opst = proj_opst(j);
+    const int nst = (r1 - r0 + opst - 1) / opst;
+    for (int s = 0; s < nst; ++s, ++it) {
+        const int slot = it % ring.ns;
+        if (!mbar_wait_or_abort(&ring.empty[slot], ((it / ring.ns) & 1) ^ 1, abort)) {
+            if (err) atomicOr(err, kErrTimeout);
+            *abort = 1;
+            return false;
+        }
+        const int o0 = r0 + s * opst;
+        const int no = min(opst, r1 - o0);
+        unsigned char* dst = ring.buf + (size_t)slot * ring.slot_bytes;
+        if (j.swiglu) {
+            mbar_arrive_expect_tx(&ring.full[slot], (uint32_t)(2 * no * rowb));
+            bulk_g2s(dst, j.W + (size_t)o0 * rowb, (uint32_t)(no * rowb), &ring.full[slot], pol);
+            bulk_g2s(dst + (size_t)opst * rowb, j.W + ((size_t)j.N + o0) * rowb, (uint32_t)(no * rowb),
+                     &ring.full[slot], pol);
+        } else {
+            mbar_arrive_expect_tx(&ring.full[slot], (uint32_t)(no * rowb));
+            bulk_g2s(dst, j.W + (size_t)o0 * rowb, (uint32_t)(no * rowb), &ring.full[slot], pol);
+        }
+    }
+    return true;
+}
+
+// Producer after an abort: wait (bounded) for the copies still in flight.
+__device__ __forceinline__ void drain(const Ring& ring, int it) {
+    for (int i = it > ring.ns ? it - ring.ns : 0; i < it; ++i) mbar_wait(&ring.full[i % ring.ns], (i / ring.ns) & 1);
+}
+
+// Stage the activation vector for a projection with inner dimension K:
+//   x (fp32, global, written by other CTAs: read through L2) -> optional
+//   RMSNorm with gain gamma -> shared memory, fp32 planes (bf16 weights) or,
+//   with FP8 weights, per-token E4M3 quantisation with scale amax/448 stored
+//   as f16 planes.  Returns the activation scale (1 for bf16).  Consumers only.
+template <bool FP8, bool RMS>
+__device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* gamma, int K, float eps,
+                                         unsigned char* xs, float* red) {
+    const int cpr = K / (FP8 ? 16 : 8);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    float scale_in = 1.0f;
+    if constexpr (RMS) {
+        float ss = 0.f;
+        for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
+            const float4 v = __ldcg(x4 + i);
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        ss = consumer_sum(ss, red);
+        scale_in = 1.0f / sqrtf(ss / (float)K + eps);
+    }
+    auto load = [&](int i) {
+        float4 v = __ldcg(x4 + i);
+        if constexpr (RMS) {
+            const uint2 g = *reinterpret_cast<const uint2*>(gamma + 4 * i);
+            v.x = v.x * scale_in * bf16lo(g.x);
+            v.y = v.y * scale_in * bf16hi(g.x);
+            v.z = v.z * scale_in * bf16lo(g.y);
+            v.w = v.w * scale_in * bf16hi(g.y);
+        }
+        return v;
+    };
+    float sa = 1.0f;
+    if constexpr (!FP8) {
+        float4* xs4 = reinterpret_cast<float4*>(xs);
+        for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
+            const int e = 4 * i;  // chunk e/8, plane (e%8)/4
+            xs4[((e & 7) >> 2) * cpr + (e >> 3)] = load(i);
+        }
+    } else {
+        // normalise, amax, then quantise (the normalised values are recomputed)
+        float amax = 0.f;
+        for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
+            const float4 v = load(i);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        amax = consumer_max(amax, red);
+        sa = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+        uint2* xs2 = reinterpret_cast<uint2*>(xs);  // 4 f16 per uint2
+        for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
+            const float4 v = load(i);
+            const __half2 h01 = __floats2half2_rn(quant_e4m3(__fdiv_rn(v.x, sa)), quant_e4m3(__fdiv_rn(v.y, sa)));
+            const __half2 h23 = __floats2half2_rn(quant_e4m3(__fdiv_rn(v.z, sa)), quant_e4m3(__fdiv_rn(v.w, sa)));
+            const int e = 4 * i;  // chunk e/16, plane (e%16)/8, half (e%8)/4
+            uint2 packed;
+            packed.x = *reinterpret_cast<const uint32_t*>(&h01);
+            packed.y = *reinterpret_cast<const uint32_t*>(&h23);
+            xs2[(((e & 15) >> 3) * cpr + (e >> 4)) * 2 + ((e & 7) >> 2)] = packed;
+        }
+    }
+    consumer_sync();
+    return sa;
+}
+
+// ---- activation segments in registers -----------------------------------------
+// A consumer warp's column segment [c0, c1) of a projection is the same in
+// every stage, so each lane keeps the activations of its chunks c0 + lane +
+// 32 i (at most kMaxLaneChunks) in registers: two planes per chunk, fp32
+// (bf16 weights) or f16 (FP8 weights).
+template <bool FP8>
+struct XSeg {
+    using V = typename std::conditional<FP8, uint4, float4>::type;
+    V a[kMaxLaneChunks], b[kMaxLaneChunks];
+};
+
+// This warp's segment of projection j.
+__device__ __forceinline__ void proj_segment(const Proj& j, int warp, int& rslot, int& sg, int& c0, int& c1) {
+    const int CPR = proj_cpr(j), WPR = j.wpr;
+    rslot = warp / WPR;
+    sg = warp % WPR;
+    c0 = (int)((long long)sg * CPR / WPR);
+    c1 = (int)((long long)(sg + 1) * CPR / WPR);
+}
+
+// Segment from the shared-memory planes written by stage_x.
+template <bool FP8>
+__device__ __forceinline__ void load_xseg_smem(const unsigned char* xs, int CPR, int c0, int c1, XSeg<FP8>& x) {
+    using V = typename XSeg<FP8>::V;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < kMaxLaneChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        x.a[i] = c < c1 ? reinterpret_cast<const V*>(xs)[c] : V{};
+        x.b[i] = c < c1 ? reinterpret_cast<const V*>(xs)[CPR + c] : V{};
+    }
+}
+
+// Statistics a phase publishes for the next phase's activation staging.
+struct XStats {
+    const float2* h;   // per producing CTA: {sum of squares, max |h * gamma_next|} (RMSNorm inputs)
+    const float* mx;   // per producing unit: max |x| (plain FP8 inputs)
+    int n;             // entries
+};
+
+// Stage an activation vector whose statistics the producing phase published,
+// into the shared planes of stage_x, with no block-wide reduction.
+//   RMS:   x = h * r * gamma, r = 1/sqrt(sum(h^2)/K + eps)   (K <= kMaxRmsK)
+//   FP8:   sa = max(amax, 1e-12)/448, amax = r * max|h*gamma| (RMS) or max|x|;
+//          x8 = e4m3(x/sa) stored as f16
+//   plain bf16: a permuted copy, issued as asynchronous 16-byte copies.
+// x is read through L2 (other CTAs wrote it).  The first batch of x is loaded
+// together with the statistics (one memory round trip); every warp reduces the
+// statistics itself (fixed order), so the only synchronisation is the final
+// barrier.  Returns sa (1 for bf16).
+template <bool FP8, bool RMS>
+__device__ __forceinline__ float stage_x_stats(const float* x, const __nv_bfloat16* gamma, int K, float eps,
+                                               const XStats& st, unsigned char* xs) {
+    const int lane = threadIdx.x & 31;
+    const int cpr = K / (FP8 ? 16 : 8);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int n4 = K / 4;
+    if constexpr (!FP8 && !RMS) {
+        // plain bf16 input: float4 i goes to plane i % 2, chunk i / 2
+        for (int i = threadIdx.x; i < n4; i += kConsumers)
+            cp_async16(xs + 16 * ((i & 1) * cpr + (i >> 1)), x4 + i);
+        cp_async_wait_all();
+        consumer_sync();
+        return 1.0f;
+    }
+    // a batch: kB float4 per thread; RMS inputs fit one batch
+    constexpr int kB = kMaxRmsK / 4 / kConsumers;
+    float4 v[kB];
+    uint2 g[kB];
+    auto load = [&](int base) {
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+            const int i = base + threadIdx.x + k * kConsumers;
+            if (i < n4) {
+                v[k] = __ldcg(x4 + i);
+                if constexpr (RMS) g[k] = *reinterpret_cast<const uint2*>(gamma + 4 * i);
+            }
+        }
+    };
+    load(0);
+    float r = 1.0f, sa = 1.0f;
+    {
+        constexpr int kMaxStatLoads = 8;  // 256 entries
+        float ss = 0.f, am = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxStatLoads; ++k) {
+            const int i = lane + 32 * k;
+            if (i < st.n) {
+                if constexpr (RMS) {
+                    const float2 w = __ldcg(st.h + i);
+                    ss += w.x;
+                    am = fmaxf(am, w.y);
+                } else {
+                    am = fmaxf(am, __ldcg(st.mx + i));
+                }
+            }
+        }
+        if constexpr (RMS) {
+            ss = warp_sum(ss);
+            r = 1.0f / sqrtf(ss / (float)K + eps);
+        }
+        if constexpr (FP8) {
+            am = warp_max(am);
+            if constexpr (RMS) am *= r;
+            sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+        }
+    }
+    for (int base = 0; base < n4; base += kB * kConsumers) {
+        if (base > 0) load(base);
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+            const int i = base + threadIdx.x + k * kConsumers;
+            if (i < n4) {
+                float4 u = v[k];
+                if constexpr (RMS) {
+                    u.x = u.x * r * bf16lo(g[k].x);
+                    u.y = u.y * r * bf16hi(g[k].x);
+                    u.z = u.z * r * bf16lo(g[k].y);
+                    u.w = u.w * r * bf16hi(g[k].y);
+                }
+                const int e = 4 * i;
+                if constexpr (!FP8) {
+                    reinterpret_cast<float4*>(xs)[((e & 7) >> 2) * cpr + (e >> 3)] = u;
+                } else {
+                    const __half2 h01 =
+                        __floats2half2_rn(quant_e4m3(__fdiv_rn(u.x, sa)), quant_e4m3(__fdiv_rn(u.y, sa)));
+                    const __half2 h23 =
+                        __floats2half2_rn(quant_e4m3(__fdiv_rn(u.z, sa)), quant_e4m3(__fdiv_rn(u.w, sa)));
+                    uint2 packed;
+                    packed.x = *reinterpret_cast<const uint32_t*>(&h01);
+                    packed.y = *reinterpret_cast<const uint32_t*>(&h23);
+                    reinterpret_cast<uint2*>(xs)[(((e & 15) >> 3) * cpr + (e >> 4)) * 2 + ((e & 7) >> 2)] = packed;
+                }
+            }
+        }
+    }
+    consumer_sync();
+    return sa;
+}
+
+// What the epilogue publishes for the next phase (all optional).
+struct StatsOut {
+    float2* h;                     // kEpiResid: this CTA's {sum y^2, max |y * gamma|} at [blockIdx.x]
+    const __nv_bfloat16* gamma;    //   gain of the next RMSNorm (for the max)
+    float* mx;                     // kEpiSwiglu: this CTA's max |y| at [blockIdx.x]
+    float* rows;                   // kEpiResid: shared-memory copy of this CTA's rows of y (read and
+                                   //   updated instead of global memory), or null
+};
+
+// Consumers: reduce projection j's stages from the ring against the lane's
+// activation registers, then apply the epilogue to this CTA's outputs (and
+// publish statistics).  `part` holds proj_stages(j) * rs * wpr floats.  `red` is
+// shared scratch for the statistics reduction.  Returns false if a wait ran out.
+template <bool FP8, int EPI>
+__device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it, const XSeg<FP8>& xr, float sa,
+                                        float* part, volatile int* abort, int* err,
+                                        unsigned long long* wait_ns = nullptr, const StatsOut* so = nullptr,
+                                        float* red = nullptr, unsigned long long* stage_tr = nullptr,
+                                        int stage_tr_n = 0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int r0, r1;
+    proj_rows(j, r0, r1);
+    const int nrows = r1 - r0;
+    const int CPR = proj_cpr(j), RS = j.rs, WPR = j.wpr, SLOTS = kConsumerWarps / WPR, NP = RS / SLOTS;
+    const size_t rowb = (size_t)CPR * 16;
+    const int opst = proj_opst(j);
+    const int nst = (nrows + opst - 1) / opst;
+    int rslot, sg, c0, c1;
+    proj_segment(j, warp, rslot, sg, c0, c1);
+
+    bool ok = true;
+    unsigned long long waited = 0;  // ns spent waiting for data (traced runs; stored once at the end)
+    for (int s = 0; s < nst; ++s, ++it) {
+        const int slot = it % ring.ns;
+        const uint64_t tw = wait_ns ? globaltimer_ns() : 0;
+        const bool got = mbar_wait_or_abort(&ring.full[slot], (it / ring.ns) & 1, abort);
+        if (wait_ns) waited += globaltimer_ns() - tw;
+        if (!got) {
+            if (lane == 0 && err) atomicOr(err, kErrTimeout);
+            *abort = 1;
+            ok = false;
+            break;
+        }
+        const long long clk0 = stage_tr ? clock64() : 0;
+        unsigned long long* str = nullptr;  // traced warps: 0 (first row of the trace), the last (second row)
+        if (stage_tr && lane == 0 && it < stage_tr_n && (warp == 0 || warp == kConsumerWarps - 1))
+            str = stage_tr + (warp == 0 ? 0 : stage_tr_n * 4) + 4 * it;
+        if (str) str[1] = globaltimer_ns();
+        const unsigned char* sbuf = ring.buf + (size_t)slot * ring.slot_bytes;
+        for (int ps = 0; ps < NP; ++ps) {
+            const int r = ps * SLOTS + rslot;          // row of the stage
+            const int orow = j.swiglu ? r % opst : r;  // its output row within the stage
+            if (s * opst + orow < nrows) {
+                const uint4* wrow = reinterpret_cast<const uint4*>(sbuf + r * rowb);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < kMaxLaneChunks; ++i) {
+                    const int c = c0 + lane + 32 * i;
+                    if (c < c1) {
+                        const uint4 w = wrow[c];
+                        if constexpr (!FP8) dot_bf16(w, xr.a[i], xr.b[i], acc[2 * (i & 1)], acc[2 * (i & 1) + 1]);
+                        else dot_fp8(w, xr.a[i], xr.b[i], acc[2 * (i & 1)], acc[2 * (i & 1) + 1]);
+                    }
+                }
+                const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+                if (lane == 0) part[(s * RS + r) * WPR + sg] = v;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[slot]);
+        if (str) {
+            str[2] = globaltimer_ns();
+            str[3] = (unsigned long long)(clock64() - clk0);  // SM cycles of this stage
+        }
+    }
+    if (wait_ns) *wait_ns += waited;
+    consumer_sync();
+    if (!ok || *abort) return false;
+
+    // per-row sums over segments (in segment order) and the epilogue
+    float st_ss = 0.f, st_mx = 0.f;
+    for (int r = threadIdx.x; r < nrows; r += kConsumers) {
+        const int n = r0 + r;
+        const int s = r / opst, jj = r % opst;
+        auto row_sum = [&](int rs_) {
+            const float* pr = part + (s * RS + rs_) * WPR;
+            float acc = 0.f;
+            for (int q = 0; q < WPR; ++q) acc += pr[q];
+            return acc;
+        };
+        if constexpr (EPI == kEpiSwiglu) {
+            float g = row_sum(jj), u = row_sum(RS / 2 + jj);
+            float m;
+            if constexpr (FP8) {
+                g = round_bf16(g * (sa * j.wscale[n]));
+                u = round_bf16(u * (sa * j.wscale[j.N + n]));
+                m = round_bf16(silu(g) * u);
+            } else {
+                m = silu(g) * u;
+            }
+            j.y[n] = m;
+            st_mx = fmaxf(st_mx, fabsf(m));
+        } else {
+            float o = row_sum(jj);
+            if constexpr (FP8) o = round_bf16(o * (sa * j.wscale[n]));
+            if constexpr (EPI == kEpiResid) {
+                if (so && so->rows) {
+                    o = so->rows[r] + o;
+                    so->rows[r] = o;
+                } else {
+                    o = __ldcg(j.y + n) + o;
+                }
+                if (so && so->h) {
+                    st_ss += o * o;
+                    if (so->gamma) st_mx = fmaxf(st_mx, fabsf(o * __bfloat162float(so->gamma[n])));
+                }
+            }
+            j.y[n] = o;
+        }
+    }
+    if (so && red) {
+        if (so->h) {
+            const float ss = consumer_sum(st_ss, red);
+            const float mx = consumer_max(st_mx, red);
+            if (threadIdx.x == 0) so->h[blockIdx.x] = make_float2(ss, mx);
+        } else if (so->mx) {
+            const float mx = consumer_max(st_mx, red);
+            if (threadIdx.x == 0) so->mx[blockIdx.x] = mx;
+        }
+    }
+    return true;
+}
+
+// load_xseg_smem + consume as a separate (not inlined) function: its
+// registers are allocated on their own, so the state the caller keeps across
+// phases cannot push the stage loop's activation registers into local memory.
+// Returns the advanced stage counter, or -1 if a wait ran out.
+template <bool FP8, int EPI>
+__device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, const unsigned char* xs, float sa,
+                                        float* part, volatile int* abort, int* err, unsigned long long* wait_ns,
+                                        const StatsOut* so, float* red, unsigned long long* stage_tr,
+                                        int stage_tr_n) {
+    int rslot, sg, c0, c1;
+    proj_segment(j, threadIdx.x >> 5, rslot, sg, c0, c1);
+    XSeg<FP8> xr;
+    load_xseg_smem<FP8>(xs, proj_cpr(j), c0, c1, xr);
+    return consume<FP8, EPI>(j, ring, it, xr, sa, part, abort, err, wait_ns, so, red, stage_tr, stage_tr_n) ? it
+                                                                                                             : -1;
+}
+
+// Codebook head, after every CTA stored its logits: the last CTA to arrive
+// takes the per-codebook greedy argmax (ties: lowest code) under the delay
+// mask (codebook k is BOS-pad before frame k and EOC from frame eoc + k on;
+// "Higgs Audio v3 TTS-4B on FlashRT", section 4 sampling policy and section 5),
+// records the codes (next step's input and the history ring) and advances the
+// position and frame.  Consumers only.
+__device__ __forceinline__ void head_tail(const float* logits, int n_cb, int V, DevState* st, unsigned* counter,
+                                          int* hist, int hist_cap, int* s_last, int* s_codes) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __threadfence();
+    consumer_sync();
+    if (threadIdx.x == 0) *s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
+    consumer_sync();
+    if (!*s_last) return;
+    __threadfence();
+    const int t = st->t, eoc = st->eoc;
+    for (int k = warp; k < n_cb; k += kConsumerWarps) {
+        float best = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int v = lane; v < V; v += 32) {
+            const float x = __ldcg(logits + (size_t)k * V + v);
+            if (x > best) { best = x; bi = v; }  // increasing v: first maximum kept
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+        }
+        if (bi == 0x7fffffff) bi = 0;  // all NaN: take code 0
+        if (lane == 0) {
+            int c = bi;
+            if (t < k) c = V - 2;
+            else if (eoc >= 0 && t >= eoc + k) c = V - 1;
+            s_codes[k] = c;
+        }
+    }
+    consumer_sync();
+    if (threadIdx.x == 0) {
+        if (eoc < 0 && s_codes[0] == V - 1) st->eoc = t;
+        int* hrow = hist + (size_t)(st->hist_idx % hist_cap) * n_cb;
+        for (int k = 0; k < n_cb; ++k) {
+            st->codes[k] = s_codes[k];
+            hrow[k] = s_codes[k];
+        }
+        st->hist_idx += 1;
+        st->t = t + 1;
+        st->pos += 1;
+        *counter = 0u;
+    }
+}
+
+}  // namespace core
+}  // namespace tts

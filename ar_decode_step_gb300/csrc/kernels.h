@@ -9,6 +9,48 @@ enum Prec { kBF16 = 0, kFP8 = 1 };
 enum Pro { kProPlain = 0, kProRms = 1 };
 enum Epi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiLogits = 3 };
 
+// ---- weight-streaming geometry (host and device) ------------------------------
+// A CTA = kConsumerWarps consumer warps + one producer warp.  Eight consumer
+// warps keep the register budget at 168 per thread (nine warps: at most three
+// per SM sub-partition).  A lane holds the activations of up to
+// kMaxLaneChunks 16-byte weight chunks of its column segment and reduces them
+// against up to four rows per ring stage at once.
+#ifndef TTS_CONSUMER_WARPS
+#define TTS_CONSUMER_WARPS 8
+#endif
+#ifndef TTS_MAX_LANE_CHUNKS
+#define TTS_MAX_LANE_CHUNKS 10
+#endif
+constexpr int kConsumerWarps = TTS_CONSUMER_WARPS;
+constexpr int kMaxLaneChunks = TTS_MAX_LANE_CHUNKS;
+constexpr int kStageTarget = 40 * 1024;  // bytes per ring stage, at most (unless one row is longer)
+constexpr int kMaxRmsK = 4096;            // persistent step: longest normalised activation (hidden)
+constexpr int kMaxPlainK = 12288;         // longest plain activation (attention output, MLP activation)
+
+// How one projection with inner dimension K is cut: each row is split into
+// wpr column segments (one warp each), so kConsumerWarps / wpr rows are reduced
+// side by side ("row slots"); a ring stage holds rs whole rows, 1, 2 or 4 per
+// row slot (a warp reduces its rows of a stage together).  wpr is the smallest
+// power of two whose segments fit a lane's registers and whose row slots fit
+// one stage.
+struct StageGeom {
+    int rs, wpr;
+    bool ok;  // segments fit the lane registers and every warp has a chunk
+};
+inline __host__ __device__ StageGeom stage_geom(int prec, int epi, int K) {
+    const int cpr = K / (prec == kBF16 ? 8 : 16);
+    const long long rowb = (long long)cpr * 16;
+    auto lane_chunks = [&](int w) { return ((cpr + w - 1) / w + 31) / 32; };
+    int wpr = 1;
+    while (wpr < kConsumerWarps && lane_chunks(wpr) > kMaxLaneChunks) wpr *= 2;
+    while (wpr < kConsumerWarps && (long long)(kConsumerWarps / wpr) * rowb > kStageTarget) wpr *= 2;
+    const int slots = kConsumerWarps / wpr;
+    int rs = slots;
+    while (rs < 4 * slots && 2LL * rs * rowb <= kStageTarget) rs *= 2;  // up to four rows per warp and stage
+    if (epi == kEpiSwiglu && rs < 2) rs = 2;
+    return StageGeom{rs, wpr, K % 256 == 0 && cpr >= wpr && lane_chunks(wpr) <= kMaxLaneChunks};
+}
+
 // y = epilogue(W . prologue(x)) for one activation vector (M = 1).
 struct GemvParams {
     const void* W;              // [rows][K], bf16 or E4M3 bytes, row-major
@@ -33,13 +75,13 @@ struct GemvParams {
     size_t next_rowb;
     size_t next_pf;
     // ring geometry, filled in by launch_gemv
-    int rs, nstages, part_bytes;
+    int rs, wpr, nstages, part_bytes;
 };
 
 // Shared-memory geometry of one GEMV launch: rows per ring stage, ring stages,
 // bytes of the per-(row, segment) partial sums, total dynamic smem.
 struct GemvGeom {
-    int rs, nstages, part_bytes, smem;
+    int rs, wpr, nstages, part_bytes, smem;
     bool ok;
 };
 
@@ -87,6 +129,78 @@ cudaError_t launch_embed(const EmbedParams& p, const LaunchCfg& lc, cudaStream_t
 
 // st->pos += 1, st->prefill_row += 1 (end of one prefill position).
 cudaError_t launch_advance(DevState* st, const LaunchCfg& lc, cudaStream_t s);
+
+// The persistent decode-step kernel (one launch per step or prefill position).
+struct StepLayer {
+    const void* wqkv;
+    const void* wo;
+    const void* wgu;
+    const void* wd;
+    const float* sqkv;
+    const float* so;
+    const float* sgu;
+    const float* sd;
+    const __nv_bfloat16* ln_in;
+    const __nv_bfloat16* ln_post;
+    const __nv_bfloat16* qn;
+    const __nv_bfloat16* kn;
+};
+
+struct StepParams {
+    const StepLayer* layers;  // device array [n_layers]
+    int n_layers;
+    const __nv_bfloat16* embed;
+    const __nv_bfloat16* head;
+    const __nv_bfloat16* final_norm;
+    const float2* rope;
+    __nv_bfloat16* kc;  // [n_layers][n_kv][max_pos][128]
+    __nv_bfloat16* vc;
+    DevState* st;
+    const int* prompt;  // prefill rows [P][n_cb]
+    int decode;         // 1: head + argmax + advance; 0: prefill position advance
+    float *h, *qkv, *attn, *act, *logits;
+    float *part_o, *part_ml;                  // attention split partials
+    unsigned *att_counter, *head_counter;     // last-arriver tickets
+    unsigned* gbar;                           // grid-barrier arrivals, zero at launch
+    float2* h_stats;                          // [grid]: per CTA {sum h^2, max |h * gamma_next|}
+    float* attn_mx;                           // [n_kv]: max |attn| of each kv head's outputs (FP8)
+    float* act_mx;                            // [grid]: per CTA max |act| (FP8)
+    int* hist;
+    int hist_cap;
+    int hidden, n_q, n_kv, inter, n_cb, cb_vocab, max_pos;
+    int S;  // attention splits per kv head (allocation stride), at most
+    float eps;
+    int rs[5];   // rows per ring stage: QKV, O, gate/up, down, head
+    int wpr[5];  // column segments (warps) per row, same order
+    int ns, slot_bytes, xs_bytes, part_bytes;
+    int pf_stages;  // how many stages the L2 prefetch runs ahead of the ring copies
+    // optional phase trace: per CTA, trace_stride globaltimer stamps (ns)
+    unsigned long long* trace;
+    int trace_stride;
+    // optional per-stage trace of CTA 0: for ring stage i, [4 i] copy issued,
+    // [4 i + 1] data seen, [4 i + 2] released, [4 i + 3] SM cycles in between,
+    // by consumer warp 0 (first stage_trace_stride entries) and by the last
+    // consumer warp (next stage_trace_stride entries; no issue time)
+    unsigned long long* stage_trace;
+    int stage_trace_stride;
+};
+
+// Phase-trace layout of the persistent kernel, per CTA (see step.cu):
+//   [0] consumer start; [1 + 14 l + k] layer l, event k (after: 0 QKV norm,
+//   1 QKV reduce, 2 barrier, 3 attention, 4 barrier, 5 O stage, 6 O reduce,
+//   7 barrier, 8 gate/up norm, 9 gate/up reduce, 10 barrier, 11 down stage,
+//   12 down reduce, 13 barrier); [1 + 14 L + 0..2] head norm, reduce, tail;
+//   [4 + 14 L + 5 l + k] producer: last copy of layer l's projection k issued
+//   (k = 4: head), [4 + 19 L + 1] producer done; [8 + 19 L + 4 l + k] ns the
+//   consumers waited for ring data in layer l's projection k; [8 + 23 L +
+//   4 l + k] ns the producer waited for free slots (the head adds to the last
+//   layer's down-proj slot).
+inline int step_trace_stride(int n_layers) { return 8 + 27 * n_layers; }
+
+cudaError_t step_prepare(int prec, int G, int smem);
+int step_attn_scratch_bytes(int G);
+int step_threads();
+cudaError_t launch_step(const StepParams& p, int prec, int G, int grid, int smem, cudaStream_t s);
 
 // Per-row E4M3 weight quantisation.
 cudaError_t launch_quantize_weight(const __nv_bfloat16* W, int N, int K, uint8_t* W8, float* s,

@@ -1,0 +1,721 @@
+// The whole decode step (or one prefill position) as one persistent kernel.
+//
+// One CTA per SM, all co-resident (cooperative launch).  The producer warp of
+// each CTA streams, back to back, every weight range the CTA owns over the
+// whole step -- QKV, O-proj, gate/up, down-proj of layer 0, then layer 1, ...,
+// then the codebook head -- through its ring of shared-memory stages, never
+// waiting on anything but free ring slots.  The sixteen consumer warps walk
+// the phases of the step ("Higgs Audio v3 TTS-4B on FlashRT", section 5):
+//
+//   embed:   h = sum_k E_k[c_k] (this CTA's slice)               -> grid barrier
+//   per layer l:
+//     QKV:   x = RMSNorm(h) (+FP8 quant); qkv rows                 -> grid barrier
+//     attn:  per (kv head, split) unit: q/k RMSNorm + RoPE, bf16 KV write,
+//            online-softmax attention over the split, last unit merges -> barrier
+//     O:     x = attn (+quant); h += W_o x                         -> grid barrier
+//     GU:    x = RMSNorm(h) (+quant); act = silu(gate) * up        -> grid barrier
+//     down:  x = act (+quant); h += W_d x                          -> grid barrier
+//   head:    x = RMSNorm(h); logits; last CTA: greedy argmax under the delay
+//            mask, codes, position and frame advance (prefill: advance only)
+//
+// A grid barrier only stops the consumers: the producer keeps the ring full
+// with the next phase's weights, so HBM streams through barriers, norms and
+// attention.  Barrier waits are bounded (kWaitLimitNs) and stop early once any
+// CTA has recorded an error; on expiry the kernel records kErrTimeout, lets
+// its in-flight copies land and returns.
+#pragma once
+
+#include "gemv_core.cuh"
+
+namespace tts {
+
+namespace {
+
+using namespace core;
+
+constexpr int kMaxHRows = 256;     // rows of h one CTA owns, at most
+constexpr int kAttnMinChunk = 128;  // positions per attention split, at least (no merge below)
+
+// Grid barrier among the consumer warps of all CTAs.  `gbar` counts arrivals
+// over the launch (zeroed before it); barrier k (1-based) waits for
+// k * gridDim.x.  Returns false if the wait ran out or another CTA failed.
+__device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned target, DevState* st, volatile int* abort) {
+    consumer_sync();  // every consumer thread's writes of this phase precede the release below
+    if (threadIdx.x == 0) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
+        uint64_t t0 = 0;
+        unsigned spins = 0;
+        while (ld_acquire_u32(gbar) < target) {
+            if ((++spins & 63) == 0) {
+                if (*reinterpret_cast<volatile int*>(&st->err) & kErrTimeout) {
+                    *abort = 1;
+                    break;
+                }
+                const uint64_t t = globaltimer_ns();
+                if (!t0) t0 = t;
+                else if (t - t0 > kWaitLimitNs) {
+                    atomicOr(&st->err, kErrTimeout);
+                    *abort = 1;
+                    break;
+                }
+            }
+        }
+    }
+    consumer_sync();  // the acquire above precedes every consumer thread's reads of the next phase
+    return !*abort;
+}
+
+template <int G>
+struct AttnSmem {
+    float qs[G][kHeadDim];  // normalised, rotated, pre-scaled queries
+    float knew[kHeadDim], vnew[kHeadDim];
+    float wm[kConsumerWarps][G], wl[kConsumerWarps][G];
+    float wo[kConsumerWarps][G][kHeadDim];
+};
+
+// One (kv head g, split) unit of the decode attention of one layer, run by the
+// consumer warps of this CTA (no waits inside).
+template <int G, bool FP8>
+__device__ __forceinline__ void attention_unit(const StepParams& p, const StepLayer& L, int layer, int pos, int g,
+                                               int split, int nsplit, int chunk, unsigned char* scratch, int* s_last,
+                                               float* red) {
+    AttnSmem<G>& sm = *reinterpret_cast<AttnSmem<G>*>(scratch);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int len = pos + 1;
+    const int t0 = split * chunk, t1 = min(len, t0 + chunk);
+    const bool has_new = t1 == len;
+    const float2* rope = p.rope + (size_t)pos * (kHeadDim / 2);
+    const float scale = 1.0f / sqrtf((float)kHeadDim);
+    const size_t cache_off = ((size_t)layer * p.n_kv + g) * p.max_pos * kHeadDim;
+    __nv_bfloat16* kc = p.kc + cache_off;
+    __nv_bfloat16* vc = p.vc + cache_off;
+
+    // q/k RMSNorm over head_dim then rotate-half RoPE: lane l holds dims
+    // 4l..4l+3; its rotation partner dims (+-64) sit in lane l^16.
+    auto norm_rope = [&](const float* src, const __nv_bfloat16* gamma, float* dst, float post) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+        const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+        const float r = 1.0f / sqrtf(ss / (float)kHeadDim + p.eps);
+        const uint2 gb = *reinterpret_cast<const uint2*>(gamma + 4 * lane);
+        const float a[4] = {v.x * r * bf16lo(gb.x), v.y * r * bf16hi(gb.x), v.z * r * bf16lo(gb.y),
+                            v.w * r * bf16hi(gb.y)};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const float partner = __shfl_xor_sync(0xffffffffu, a[jj], 16);
+            const float2 cs = rope[(4 * lane + jj) & 63];
+            dst[4 * lane + jj] = (lane < 16 ? a[jj] * cs.x - partner * cs.y : a[jj] * cs.x + partner * cs.y) * post;
+        }
+    };
+    // The cached rows do not depend on this step: issue their loads first so
+    // they overlap the q/k loads (one memory round trip for both).
+    const int tcache_end = has_new ? t1 - 1 : t1;  // cached rows; the new row comes from smem
+    constexpr int kBatch = 4;                       // rows per warp per round trip
+    uint2 ka[kBatch], va[kBatch];
+    auto load_rows = [&](int tb) {
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int t = tb + b * kConsumerWarps;
+            if (t < tcache_end) {
+                ka[b] = *reinterpret_cast<const uint2*>(kc + (size_t)t * kHeadDim + 4 * lane);
+                va[b] = *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane);
+            }
+        }
+    };
+    load_rows(t0 + warp);
+    if (warp < G) norm_rope(p.qkv + (size_t)(g * G + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
+    if (has_new && warp == G) {
+        norm_rope(p.qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
+        __syncwarp();
+        const float* vsrc = p.qkv + (size_t)(p.n_q + p.n_kv + g) * kHeadDim;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int d = 4 * lane + jj;
+            const __nv_bfloat16 kb = __float2bfloat16_rn(sm.knew[d]);
+            const __nv_bfloat16 vb = __float2bfloat16_rn(__ldcg(vsrc + d));
+            kc[(size_t)pos * kHeadDim + d] = kb;
+            vc[(size_t)pos * kHeadDim + d] = vb;
+            sm.knew[d] = __bfloat162float(kb);
+            sm.vnew[d] = __bfloat162float(vb);
+        }
+    }
+    consumer_sync();
+
+    float m[G], l[G], o[G][4], qr[G][4];
+#pragma unroll
+    for (int jj = 0; jj < G; ++jj) {
+        m[jj] = -INFINITY;
+        l[jj] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { o[jj][i] = 0.f; qr[jj][i] = sm.qs[jj][4 * lane + i]; }
+    }
+    auto consume_pos = [&](const float* k4, const float* v4) {
+        float s[G];
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj)
+            s[jj] = warp_sum(qr[jj][0] * k4[0] + qr[jj][1] * k4[1] + qr[jj][2] * k4[2] + qr[jj][3] * k4[3]);
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj) {
+            const float mn = fmaxf(m[jj], s[jj]);
+            const float corr = __expf(m[jj] - mn);
+            const float pj = __expf(s[jj] - mn);
+            l[jj] = l[jj] * corr + pj;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[jj][i] = o[jj][i] * corr + pj * v4[i];
+            m[jj] = mn;
+        }
+    };
+    for (int tb = t0 + warp; tb < tcache_end; tb += kBatch * kConsumerWarps) {
+        if (tb != t0 + warp) load_rows(tb);
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (tb + b * kConsumerWarps < tcache_end) {
+                const float k4[4] = {bf16lo(ka[b].x), bf16hi(ka[b].x), bf16lo(ka[b].y), bf16hi(ka[b].y)};
+                const float v4[4] = {bf16lo(va[b].x), bf16hi(va[b].x), bf16lo(va[b].y), bf16hi(va[b].y)};
+                consume_pos(k4, v4);
+            }
+        }
+    }
+    if (has_new && warp == (t1 - 1 - t0) % kConsumerWarps) {
+        float k4[4], v4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { k4[i] = sm.knew[4 * lane + i]; v4[i] = sm.vnew[4 * lane + i]; }
+        consume_pos(k4, v4);
+    }
+#pragma unroll
+    for (int jj = 0; jj < G; ++jj) {
+        if (lane == 0) { sm.wm[warp][jj] = m[jj]; sm.wl[warp][jj] = l[jj]; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sm.wo[warp][jj][4 * lane + i] = o[jj][i];
+    }
+    consumer_sync();
+
+    // merge the warps; a single split writes the output directly
+    float mx = 0.f;  // max |output| (FP8 scale of the O-proj input)
+    float* po = p.part_o + (((size_t)g * p.S + split) * G) * kHeadDim;
+    float* pml = p.part_ml + (((size_t)g * p.S + split) * G) * 2;
+    for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kConsumers) {
+        const int jj = idx / kHeadDim, d = idx % kHeadDim;
+        float M = -INFINITY;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.wm[w][jj]);
+        float Ls = 0.f, O = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float c = sm.wm[w][jj] == -INFINITY ? 0.f : __expf(sm.wm[w][jj] - M);
+            Ls += sm.wl[w][jj] * c;
+            O += sm.wo[w][jj][d] * c;
+        }
+        if (nsplit == 1) {
+            const float a = O / Ls;
+            p.attn[(size_t)(g * G + jj) * kHeadDim + d] = a;
+            mx = fmaxf(mx, fabsf(a));
+        } else {
+            po[idx] = O;
+            if (d == 0) { pml[2 * jj] = M; pml[2 * jj + 1] = Ls; }
+        }
+    }
+    if (nsplit == 1) {
+        if constexpr (FP8) {
+            mx = consumer_max(mx, red);
+            if (threadIdx.x == 0) p.attn_mx[g] = mx;
+        }
+        consumer_sync();
+        return;
+    }
+    // the last split of this kv head merges all splits
+    __threadfence();
+    consumer_sync();
+    if (threadIdx.x == 0) *s_last = atomicAdd(&p.att_counter[g], 1u) == (unsigned)(nsplit - 1);
+    consumer_sync();
+    if (*s_last) {
+        __threadfence();
+        // all splits' (max, sum) pairs into shared memory first: one parallel round trip
+        const float* po0 = p.part_o + ((size_t)g * p.S * G) * kHeadDim;
+        const float* pml0 = p.part_ml + ((size_t)g * p.S * G) * 2;
+        float* mlw = &sm.wo[0][0][0];  // reuse: [nsplit][G][2] pairs, then [nsplit][G] weights
+        for (int i = threadIdx.x; i < nsplit * G * 2; i += kConsumers) mlw[i] = __ldcg(pml0 + i);
+        consumer_sync();
+        float* wgt = mlw + nsplit * G * 2;
+        float* lsum = wgt + nsplit * G;
+        if (threadIdx.x < G) {
+            const int jj = threadIdx.x;
+            float M = -INFINITY;
+            for (int s = 0; s < nsplit; ++s) M = fmaxf(M, mlw[(s * G + jj) * 2]);
+            float Ls = 0.f;
+            for (int s = 0; s < nsplit; ++s) {
+                const float c = __expf(mlw[(s * G + jj) * 2] - M);
+                wgt[s * G + jj] = c;
+                Ls += mlw[(s * G + jj) * 2 + 1] * c;
+            }
+            lsum[jj] = Ls;
+        }
+        consumer_sync();
+        for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kConsumers) {
+            const int jj = idx / kHeadDim, d = idx % kHeadDim;
+            float O = 0.f;
+#pragma unroll 8
+            for (int s = 0; s < nsplit; ++s) O += __ldcg(po0 + ((size_t)s * G + jj) * kHeadDim + d) * wgt[s * G + jj];
+            const float a = O / lsum[jj];
+            p.attn[(size_t)(g * G + jj) * kHeadDim + d] = a;
+            mx = fmaxf(mx, fabsf(a));
+        }
+        if constexpr (FP8) {
+            mx = consumer_max(mx, red);
+            if (threadIdx.x == 0) p.attn_mx[g] = mx;
+        }
+        if (threadIdx.x == 0) p.att_counter[g] = 0u;
+    }
+    consumer_sync();
+}
+
+// Per-CTA constants of one launch, worked out once at kernel start and kept
+// in shared memory: the phase functions read them there instead of holding
+// them in registers across the step.
+struct CtaState {
+    int pos, nsplit, chunk, nunits;
+    int rows[5][2];                // this CTA's output rows per projection kind
+    unsigned long long* cwait;     // traced runs: consumer wait per projection (thread 0), else null
+    unsigned long long* cstr;      // traced runs: this CTA's per-stage trace, else null
+    int cstr_n;
+};
+
+// Dynamic shared memory: barriers | per-layer pointer table | activation /
+// attention scratch | partials | ring.
+struct StepSmem {
+    StepLayer* sl;
+    unsigned char* xs;
+    float* part;
+    Ring ring;
+};
+__device__ __forceinline__ StepSmem step_smem(unsigned char* smem, const StepParams& p) {
+    StepSmem m;
+    const int tbl_bytes = (p.n_layers * (int)sizeof(StepLayer) + 127) & ~127;
+    m.sl = reinterpret_cast<StepLayer*>(smem + kBarrierBytes);
+    m.xs = smem + kBarrierBytes + tbl_bytes;
+    m.part = reinterpret_cast<float*>(m.xs + p.xs_bytes);
+    m.ring = Ring{reinterpret_cast<uint64_t*>(smem), reinterpret_cast<uint64_t*>(smem) + p.ns,
+                  m.xs + p.xs_bytes + p.part_bytes, (uint32_t)p.slot_bytes, p.ns};
+    return m;
+}
+
+// Projection `kind` (0 QKV, 1 O, 2 gate/up, 3 down, 4 head) of layer l as this CTA sees it.
+__device__ __forceinline__ Proj step_proj(const StepParams& p, const StepLayer* sl, const CtaState& cs, int kind,
+                                          int l, bool fp8) {
+    Proj j{};
+    j.fp8 = (fp8 && kind != 4) ? 1 : 0;
+    j.rs = p.rs[kind];
+    j.wpr = p.wpr[kind];
+    j.r0 = cs.rows[kind][0];
+    j.r1 = cs.rows[kind][1];
+    const int A = p.n_q * kHeadDim;
+    if (kind == 4) {
+        j.W = reinterpret_cast<const unsigned char*>(p.head);
+        j.y = p.logits;
+        j.N = p.n_cb * p.cb_vocab;
+        j.K = p.hidden;
+        return j;
+    }
+    const StepLayer& L = sl[l];
+    switch (kind) {
+        case 0: j.W = static_cast<const unsigned char*>(L.wqkv); j.wscale = L.sqkv; j.y = p.qkv;
+                j.N = A + 2 * p.n_kv * kHeadDim; j.K = p.hidden; break;
+        case 1: j.W = static_cast<const unsigned char*>(L.wo); j.wscale = L.so; j.y = p.h;
+                j.N = p.hidden; j.K = A; break;
+        case 2: j.W = static_cast<const unsigned char*>(L.wgu); j.wscale = L.sgu; j.y = p.act;
+                j.N = p.inter; j.K = p.hidden; j.swiglu = 1; break;
+        default: j.W = static_cast<const unsigned char*>(L.wd); j.wscale = L.sd; j.y = p.h;
+                 j.N = p.hidden; j.K = p.inter; break;
+    }
+    return j;
+}
+
+template <bool TRACE>
+__device__ __forceinline__ void trace_mark(const StepParams& p, int ev) {
+    if constexpr (TRACE)
+        if (threadIdx.x == 0) p.trace[(size_t)blockIdx.x * p.trace_stride + ev] = globaltimer_ns();
+}
+
+// One projection phase of the consumers: stage the activation vector (with
+// the norm / quantisation its kind needs), reduce this CTA's stages from the
+// ring, apply the epilogue.  Not inlined: its registers are allocated on their
+// own, free of the state the step keeps across phases.  Returns the advanced
+// stage counter, or -1 if a wait ran out.
+template <bool FP8_, int KIND, bool TRACE>
+__device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l, int it,
+                                       float* red, volatile int* abort, float* s_hrows) {
+    constexpr bool FP8 = FP8_ && KIND != 4;  // the head is bf16 in both precisions
+    const StepSmem m = step_smem(smem, p);
+    const Proj j = step_proj(p, m.sl, cs, KIND, l, FP8);
+    const int ev = 1 + 14 * l + (KIND == 0 ? 0 : KIND == 1 ? 5 : KIND == 2 ? 8 : KIND == 3 ? 11 : 0);
+    const int A = p.n_q * kHeadDim;
+    float sa;
+    if constexpr (KIND == 0) {
+        // warm L2 with the cache rows this CTA's attention unit of this layer will read
+        if (threadIdx.x == 0 && (int)blockIdx.x < cs.nunits) {
+            const int g = blockIdx.x / cs.nsplit, sp = blockIdx.x % cs.nsplit;
+            const int a0 = sp * cs.chunk, a1 = min(cs.pos, a0 + cs.chunk);  // rows before pos are cached
+            if (a1 > a0) {
+                const size_t off = (((size_t)l * p.n_kv + g) * p.max_pos + a0) * kHeadDim;
+                prefetch_l2_bulk(p.kc + off, (uint32_t)((a1 - a0) * kHeadDim * 2));
+                prefetch_l2_bulk(p.vc + off, (uint32_t)((a1 - a0) * kHeadDim * 2));
+            }
+        }
+        sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_in, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},
+                                      m.xs);
+    } else if constexpr (KIND == 1) {
+        sa = stage_x_stats<FP8, false>(p.attn, nullptr, A, p.eps, XStats{nullptr, p.attn_mx, p.n_kv}, m.xs);
+    } else if constexpr (KIND == 2) {
+        sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_post, p.hidden, p.eps,
+                                      XStats{p.h_stats, nullptr, (int)gridDim.x}, m.xs);
+    } else if constexpr (KIND == 3) {
+        sa = stage_x_stats<FP8, false>(p.act, nullptr, p.inter, p.eps, XStats{nullptr, p.act_mx, (int)gridDim.x},
+                                       m.xs);
+    } else {
+        sa = stage_x_stats<false, true>(p.h, p.final_norm, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},
+                                        m.xs);
+    }
+    if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers);
+    else trace_mark<TRACE>(p, ev);
+
+    int rslot, sg, c0, c1;
+    proj_segment(j, threadIdx.x >> 5, rslot, sg, c0, c1);
+    XSeg<FP8> xr;
+    load_xseg_smem<FP8>(m.xs, proj_cpr(j), c0, c1, xr);
+    unsigned long long* cw = (TRACE && KIND < 4) ? cs.cwait + 4 * l + KIND : nullptr;
+    unsigned long long* cstr = TRACE ? cs.cstr : nullptr;
+    bool ok;
+    if constexpr (KIND == 1 || KIND == 3) {
+        // residual add; publish h's statistics for the next RMSNorm (FP8: max |h * gamma_next|)
+        const __nv_bfloat16* gnext = KIND == 1 ? m.sl[l].ln_post : (l + 1 < p.n_layers ? m.sl[l + 1].ln_in : p.final_norm);
+        const StatsOut so{p.h_stats, FP8 ? gnext : nullptr, nullptr, s_hrows};
+        ok = consume<FP8, kEpiResid>(j, m.ring, it, xr, sa, m.part, abort, &p.st->err, cw, &so, red, cstr,
+                                     cs.cstr_n);
+    } else if constexpr (KIND == 2) {
+        const StatsOut so{nullptr, nullptr, FP8 ? p.act_mx : nullptr, nullptr};
+        ok = consume<FP8, kEpiSwiglu>(j, m.ring, it, xr, sa, m.part, abort, &p.st->err, cw, &so, red, cstr,
+                                      cs.cstr_n);
+    } else {
+        ok = consume<FP8, kEpiStore>(j, m.ring, it, xr, sa, m.part, abort, &p.st->err, cw, nullptr, nullptr,
+                                     cstr, cs.cstr_n);
+    }
+    if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 1);
+    else trace_mark<TRACE>(p, ev + 1);
+    return ok ? it : -1;
+}
+
+// This CTA's attention unit of layer l (no-op for CTAs without one).  Not inlined.
+template <int G, bool FP8>
+__device__ __noinline__ void attn_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l,
+                                        int* s_last, float* red) {
+    if ((int)blockIdx.x >= cs.nunits) return;
+    const StepSmem m = step_smem(smem, p);
+    attention_unit<G, FP8>(p, m.sl[l], l, cs.pos, blockIdx.x / cs.nsplit, blockIdx.x % cs.nsplit, cs.nsplit,
+                           cs.chunk, m.xs, s_last, red);
+}
+
+template <int PREC, int G, bool TRACE>
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p_in) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(16) StepParams s_p;  // the launch parameters, for the phase functions
+    __shared__ CtaState s_cs;
+    __shared__ float red[32];
+    __shared__ int s_last;
+    __shared__ int s_codes[kMaxCodebooks];
+    __shared__ volatile int s_abort;
+    __shared__ float s_hrows[kMaxHRows];  // this CTA's rows of the residual stream h
+
+    constexpr bool FP8 = PREC == kFP8;
+    const StepParams& p = p_in;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const StepSmem m = step_smem(smem, p);
+    {
+        // parameters and the layer pointer table (read on every stage) into shared memory
+        static_assert(sizeof(StepParams) % 8 == 0, "StepParams is copied in 8-byte words");
+        const unsigned long long* ps = reinterpret_cast<const unsigned long long*>(&p_in);
+        unsigned long long* pd = reinterpret_cast<unsigned long long*>(&s_p);
+        for (int i = threadIdx.x; i < (int)(sizeof(StepParams) / 8); i += blockDim.x) pd[i] = ps[i];
+        const unsigned long long* src = reinterpret_cast<const unsigned long long*>(p.layers);
+        unsigned long long* dst = reinterpret_cast<unsigned long long*>(m.sl);
+        for (int i = threadIdx.x; i < p.n_layers * (int)(sizeof(StepLayer) / 8); i += blockDim.x) dst[i] = src[i];
+    }
+    const int A = p.n_q * kHeadDim;
+    if (threadIdx.x < 5) {
+        const int N = threadIdx.x == 0 ? A + 2 * p.n_kv * kHeadDim
+                    : threadIdx.x == 2 ? p.inter
+                    : threadIdx.x == 4 ? p.n_cb * p.cb_vocab
+                                       : p.hidden;
+        s_cs.rows[threadIdx.x][0] = (int)((long long)blockIdx.x * N / gridDim.x);
+        s_cs.rows[threadIdx.x][1] = (int)((long long)(blockIdx.x + 1) * N / gridDim.x);
+    }
+    if (threadIdx.x == 0) {
+        ring_init(m.ring);
+        s_abort = 0;
+        const int pos = p.st->pos;
+        s_cs.pos = pos;
+        // attention work split for this position
+        const int len = pos + 1;
+        int S = gridDim.x / p.n_kv;
+        if (S > p.S) S = p.S;
+        if (S < 1) S = 1;
+        int chunk = (len + S - 1) / S;
+        if (chunk < kAttnMinChunk) chunk = kAttnMinChunk;
+        s_cs.chunk = chunk;
+        s_cs.nsplit = (len + chunk - 1) / chunk;
+        s_cs.nunits = p.n_kv * s_cs.nsplit;
+        s_cs.cwait = TRACE ? p.trace + (size_t)blockIdx.x * p.trace_stride + 8 + 19 * p.n_layers : nullptr;
+        s_cs.cstr = (TRACE && p.stage_trace && blockIdx.x == 0) ? p.stage_trace : nullptr;
+        s_cs.cstr_n = p.stage_trace_stride / 4;
+    }
+    __syncthreads();
+    const int pos = s_cs.pos;
+
+    // ---- warm L2 with every layer's small parameters ---------------------------
+    // Norm gains, FP8 scales and this position's RoPE row are read on the
+    // consumers' critical path right after a barrier; a first touch would queue
+    // behind the saturated weight stream.  The idle lanes of the producer warp
+    // spread L2 prefetches of all of them over the CTAs at kernel start.
+    if (warp == kConsumerWarps && lane > 0) {
+        const int n_items = 8 * p.n_layers + 2;
+        const int A2 = A + 2 * p.n_kv * kHeadDim;
+        for (int item = blockIdx.x * 31 + (lane - 1); item < n_items; item += gridDim.x * 31) {
+            const void* ptr = nullptr;
+            uint32_t bytes = 0;
+            if (item < 8 * p.n_layers) {
+                const StepLayer& L = m.sl[item / 8];
+                switch (item % 8) {
+                    case 0: ptr = L.ln_in; bytes = p.hidden * 2; break;
+                    case 1: ptr = L.ln_post; bytes = p.hidden * 2; break;
+                    case 2: ptr = L.qn; bytes = kHeadDim * 2; break;
+                    case 3: ptr = L.kn; bytes = kHeadDim * 2; break;
+                    case 4: ptr = L.sqkv; bytes = A2 * 4; break;
+                    case 5: ptr = L.so; bytes = p.hidden * 4; break;
+                    case 6: ptr = L.sgu; bytes = 2 * p.inter * 4; break;
+                    default: ptr = L.sd; bytes = p.hidden * 4; break;
+                }
+            } else if (item == 8 * p.n_layers) {
+                ptr = p.final_norm;
+                bytes = p.hidden * 2;
+            } else if (pos >= 0 && pos < p.max_pos) {
+                ptr = p.rope + (size_t)pos * (kHeadDim / 2);
+                bytes = kHeadDim / 2 * sizeof(float2);
+            }
+            if (ptr)
+                for (uint32_t off = 0; off < bytes; off += 32768)
+                    prefetch_l2_bulk(static_cast<const unsigned char*>(ptr) + off, min(32768u, bytes - off));
+        }
+    }
+
+    // ---- producer warp: every weight range of the step, in phase order --------
+    // Two cursors walk the same stage sequence: the copy cursor fills ring
+    // slots as they free up; the prefetch cursor runs up to p.pf_stages stages
+    // ahead asking L2 for the data.  A projection's byte ranges are worked out
+    // once when a cursor enters it; per stage the producer only adds offsets
+    // (it is a single thread: integer divisions per stage would throttle it).
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            struct Seg {  // this CTA's part of one projection
+                const unsigned char* a;  // first row of its range (gate rows for gate/up)
+                const unsigned char* b;  // matching up rows, or null
+                uint32_t stage_bytes;    // bytes of a full stage, per range
+                uint32_t last_bytes;     // bytes of the last stage, per range
+                uint32_t b_off;          // offset of the up rows inside a slot
+                int nst;
+            };
+            const Ring& ring = m.ring;
+            const int nkinds = p.decode ? 4 * p.n_layers + 1 : 4 * p.n_layers;
+            auto seg_of = [&](int q) {
+                const int kind = q == 4 * p.n_layers ? 4 : q % 4;
+                const Proj j = step_proj(p, m.sl, s_cs, kind, q == 4 * p.n_layers ? 0 : q / 4, FP8);
+                const uint32_t rowb = (uint32_t)proj_cpr(j) * 16u;
+                const int opst = proj_opst(j), nrows = j.r1 - j.r0;
+                Seg sg;
+                sg.a = j.W + (size_t)j.r0 * rowb;
+                sg.b = j.swiglu ? j.W + ((size_t)j.N + j.r0) * rowb : nullptr;
+                sg.nst = (nrows + opst - 1) / opst;
+                sg.stage_bytes = (uint32_t)opst * rowb;
+                sg.last_bytes = (uint32_t)(nrows - (sg.nst - 1) * opst) * rowb;
+                sg.b_off = (uint32_t)opst * rowb;
+                return sg;
+            };
+            const uint64_t pol = l2_evict_first_policy();
+            unsigned long long* tr = TRACE ? p.trace + (size_t)blockIdx.x * p.trace_stride + 4 + 14 * p.n_layers
+                                           : nullptr;
+            unsigned long long* str = TRACE ? s_cs.cstr : nullptr;
+            const int str_n = s_cs.cstr_n;
+
+            // prefetch cursor
+            int pq = 0, ps = 0, pidx = 0;
+            Seg psg = seg_of(0);
+            auto prefetch_upto = [&](int limit) {
+                while (pq < nkinds && pidx < limit) {
+                    if (psg.nst > 0) {
+                        const uint32_t bytes = ps + 1 < psg.nst ? psg.stage_bytes : psg.last_bytes;
+                        const size_t off = (size_t)ps * psg.stage_bytes;
+                        prefetch_l2_bulk(psg.a + off, bytes);
+                        if (psg.b) prefetch_l2_bulk(psg.b + off, bytes);
+                    }
+                    ++pidx;
+                    if (++ps >= psg.nst) {
+                        ps = 0;
+                        if (++pq < nkinds) psg = seg_of(pq);
+                    }
+                }
+            };
+
+            int it = 0, slot = 0;
+            uint32_t parity = 1;  // first pass over the ring: slots start free
+            bool ok = true;
+            for (int q = 0; q < nkinds && ok; ++q) {
+                const Seg sg = seg_of(q);
+                unsigned long long* pw = TRACE && q < 4 * p.n_layers
+                                             ? p.trace + (size_t)blockIdx.x * p.trace_stride + 8 + 23 * p.n_layers + q
+                                             : nullptr;
+                unsigned long long waited = 0;  // stored once per projection (traced runs)
+                for (int s2 = 0; s2 < sg.nst; ++s2) {
+                    prefetch_upto(it + p.pf_stages);
+                    const uint64_t tw = pw ? globaltimer_ns() : 0;
+                    if (!mbar_wait_or_abort(&ring.empty[slot], parity, &s_abort)) {
+                        atomicOr(&p.st->err, kErrTimeout);
+                        s_abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (pw) waited += globaltimer_ns() - tw;
+                    if (str && it < str_n) str[4 * it] = globaltimer_ns();
+                    const uint32_t bytes = s2 + 1 < sg.nst ? sg.stage_bytes : sg.last_bytes;
+                    const size_t off = (size_t)s2 * sg.stage_bytes;
+                    unsigned char* dst = ring.buf + (size_t)slot * ring.slot_bytes;
+                    mbar_arrive_expect_tx(&ring.full[slot], sg.b ? 2 * bytes : bytes);
+                    bulk_g2s(dst, sg.a + off, bytes, &ring.full[slot], pol);
+                    if (sg.b) bulk_g2s(dst + sg.b_off, sg.b + off, bytes, &ring.full[slot], pol);
+                    ++it;
+                    if (++slot == ring.ns) {
+                        slot = 0;
+                        parity ^= 1;
+                    }
+                }
+                if (pw) *pw = waited;
+                if (tr) tr[q == 4 * p.n_layers ? 5 * (p.n_layers - 1) + 4 : 5 * (q / 4) + q % 4] = globaltimer_ns();
+            }
+            if (tr) tr[5 * p.n_layers + 1] = globaltimer_ns();
+            if (!ok) drain(ring, it);
+        }
+        return;
+    }
+
+    // ---- consumer warps ------------------------------------------------------------
+    trace_mark<TRACE>(p, 0);
+    if (pos < 0 || pos >= p.max_pos) {
+        if (threadIdx.x == 0) {
+            atomicOr(&p.st->err, kErrPos | kErrTimeout);  // kErrTimeout stops the others' barriers early
+            s_abort = 1;
+        }
+        return;
+    }
+    unsigned nbar = 0;
+    auto barrier = [&]() { return grid_barrier(p.gbar, ++nbar * gridDim.x, p.st, &s_abort); };
+
+    // embed: this CTA's slice of h = sum_k E_k[c_k]
+    {
+        if (threadIdx.x < p.n_cb) {
+            int c = p.decode ? p.st->codes[threadIdx.x] : p.prompt[(size_t)p.st->prefill_row * p.n_cb + threadIdx.x];
+            if (c < 0 || c >= p.cb_vocab) {
+                atomicOr(&p.st->err, kErrCode);
+                c = 0;
+            }
+            s_codes[threadIdx.x] = c;
+        }
+        consumer_sync();
+        const int i0 = (int)((long long)blockIdx.x * p.hidden / gridDim.x);
+        const int i1 = (int)((long long)(blockIdx.x + 1) * p.hidden / gridDim.x);
+        float ss = 0.f, mxg = 0.f;
+        const __nv_bfloat16* g0 = m.sl[0].ln_in;
+        for (int i = i0 + threadIdx.x; i < i1; i += kConsumers) {
+            float acc = 0.f;
+            for (int k = 0; k < p.n_cb; ++k)
+                acc += __bfloat162float(p.embed[((size_t)k * p.cb_vocab + s_codes[k]) * p.hidden + i]);
+            p.h[i] = acc;
+            s_hrows[i - i0] = acc;
+            ss += acc * acc;
+            mxg = fmaxf(mxg, fabsf(acc * __bfloat162float(g0[i])));
+        }
+        ss = consumer_sum(ss, red);
+        mxg = consumer_max(mxg, red);
+        if (threadIdx.x == 0) p.h_stats[blockIdx.x] = make_float2(ss, mxg);
+    }
+    if (!barrier()) return;
+
+    // per layer: QKV | attention | O-proj | gate/up | down, a grid barrier after each
+    int it = 0;
+    for (int l = 0; l < p.n_layers; ++l) {
+        const int ev = 1 + 14 * l;
+        if ((it = proj_phase<FP8, 0, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
+        if (!barrier()) return;
+        trace_mark<TRACE>(p, ev + 2);
+        attn_phase<G, FP8>(s_p, s_cs, smem, l, &s_last, red);
+        trace_mark<TRACE>(p, ev + 3);
+        if (!barrier()) return;
+        trace_mark<TRACE>(p, ev + 4);
+        if ((it = proj_phase<FP8, 1, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
+        if (!barrier()) return;
+        trace_mark<TRACE>(p, ev + 7);
+        if ((it = proj_phase<FP8, 2, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
+        if (!barrier()) return;
+        trace_mark<TRACE>(p, ev + 10);
+        if ((it = proj_phase<FP8, 3, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
+        if (!barrier()) return;
+        trace_mark<TRACE>(p, ev + 13);
+    }
+    if (p.decode) {
+        if ((it = proj_phase<FP8, 4, TRACE>(s_p, s_cs, smem, 0, it, red, &s_abort, s_hrows)) < 0) return;
+        head_tail(p.logits, p.n_cb, p.cb_vocab, p.st, p.head_counter, p.hist, p.hist_cap, &s_last, s_codes);
+        trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 2);
+    }
+    if (!p.decode && blockIdx.x == 0 && threadIdx.x == 0) {
+        p.st->pos = pos + 1;
+        p.st->prefill_row += 1;
+    }
+}
+
+template <int PREC, int G>
+cudaError_t launch_step_t(const StepParams& p, int grid, int smem, cudaStream_t s) {
+    auto kern = p.trace ? step_kernel<PREC, G, true> : step_kernel<PREC, G, false>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Per-precision entry points (one translation unit each, compiled in parallel).
+template <int PREC>
+cudaError_t step_prepare_prec(int G, int smem) {
+#define TTS_STEP_PREP(GG)                                                                                  \
+    if (G == GG) {                                                                                         \
+        cudaError_t e = cudaFuncSetAttribute(step_kernel<PREC, GG, false>,                                 \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);           \
+        if (e == cudaSuccess)                                                                              \
+            e = cudaFuncSetAttribute(step_kernel<PREC, GG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                     smem);                                                                \
+        return e;                                                                                          \
+    }
+    TTS_STEP_PREP(1) TTS_STEP_PREP(2) TTS_STEP_PREP(4) TTS_STEP_PREP(8)
+#undef TTS_STEP_PREP
+    return cudaErrorInvalidValue;
+}
+
+template <int PREC>
+cudaError_t launch_step_prec(const StepParams& p, int G, int grid, int smem, cudaStream_t s) {
+    if (G == 1) return launch_step_t<PREC, 1>(p, grid, smem, s);
+    if (G == 2) return launch_step_t<PREC, 2>(p, grid, smem, s);
+    if (G == 4) return launch_step_t<PREC, 4>(p, grid, smem, s);
+    if (G == 8) return launch_step_t<PREC, 8>(p, grid, smem, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace tts

@@ -10,6 +10,7 @@
 // launch edges so each can start streaming its weights before its producer
 // ends.  The graph is destroyed before any buffer it references is freed (the
 // TTS-Audio-Suite report's CUDA-graph teardown hazard).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -54,6 +55,13 @@ struct tts_ctx {
 
     DevState* h_in = nullptr;   // pinned staging, host -> device
     DevState* h_out = nullptr;  // pinned staging, device -> host
+
+    // persistent step kernel
+    bool persistent = true;
+    StepLayer* d_layers = nullptr;
+    unsigned* gbar = nullptr;
+    StepParams sp{};
+    int step_smem = 0;
 
     cudaGraphExec_t step_exec = nullptr;     // one decode step
     cudaGraphExec_t prefill_exec = nullptr;  // one prefill position (no head)
@@ -104,7 +112,8 @@ int validate(const tts_config* c, const tts_weights* w) {
         if (!aligned16(w->ln_in[l]) || !aligned16(w->ln_post[l]) || !aligned16(w->q_norm[l]) ||
             !aligned16(w->k_norm[l]))
             return TTS_ERR_ARG;
-        if (fp8 && (!w->sqkv[l] || !w->so[l] || !w->sgu[l] || !w->sd[l])) return TTS_ERR_ARG;
+        if (fp8 && (!aligned16(w->sqkv[l]) || !aligned16(w->so[l]) || !aligned16(w->sgu[l]) || !aligned16(w->sd[l])))
+            return TTS_ERR_ARG;
     }
     return TTS_OK;
 }
@@ -166,9 +175,20 @@ size_t env_kb(const char* name, size_t dflt) {
     return (v && *v) ? (size_t)std::strtoul(v, nullptr, 10) * 1024 : dflt * 1024;
 }
 
+// Persistent form: zero the grid-barrier counter, then one cooperative launch.
+int record_step_persistent(tts_ctx* c, cudaStream_t s, bool decode) {
+    StepParams p = c->sp;
+    p.decode = decode ? 1 : 0;
+    TTS_CK(cudaMemsetAsync(c->gbar, 0, sizeof(unsigned), s));
+    const int prec = c->cfg.precision == TTS_FP8 ? kFP8 : kBF16;
+    TTS_CK(launch_step(p, prec, c->G, c->num_sms, c->step_smem, s));
+    return TTS_OK;
+}
+
 // Enqueue one position through the layer stack, then either the head (decode)
 // or the prefill advance.
 int record_step(tts_ctx* c, cudaStream_t s, bool decode) {
+    if (c->persistent) return record_step_persistent(c, s, decode);
     const tts_config& k = c->cfg;
     const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
     const size_t pf = env_kb("TTS_PF_KB", 96), pf_attn = env_kb("TTS_PF_ATTN_KB", 160);
@@ -263,6 +283,89 @@ DevState bos_state(const tts_ctx* c, int pos, int t, int eoc) {
     return s;
 }
 
+int round128i(int x) { return (x + 127) & ~127; }
+
+// Shared-memory geometry of the persistent step kernel and its parameter block.
+int setup_persistent(tts_ctx* c) {
+    const tts_config& k = c->cfg;
+    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    const int H = k.hidden, A = c->attn_dim, I = k.inter, grid = c->num_sms;
+    struct KindShape { int N, K, prec, epi; };
+    const KindShape kinds[5] = {{c->qkv_rows, H, prec, kEpiStore}, {H, A, prec, kEpiResid},
+                                {I, H, prec, kEpiSwiglu},          {H, I, prec, kEpiResid},
+                                {k.n_codebooks * k.cb_vocab, H, kBF16, kEpiStore}};
+    StepParams& p = c->sp;
+    int slot = 0, part = 0;
+    for (int i = 0; i < 5; ++i) {
+        const KindShape& ks = kinds[i];
+        const StageGeom g = stage_geom(ks.prec, ks.epi, ks.K);
+        if (!g.ok) return TTS_ERR_ARG;  // segments must fit the lane registers
+        const int rowb = ks.K / (ks.prec == kBF16 ? 8 : 16) * 16;
+        p.rs[i] = g.rs;
+        p.wpr[i] = g.wpr;
+        slot = std::max(slot, g.rs * rowb);
+        const int opst = ks.epi == kEpiSwiglu ? g.rs / 2 : g.rs;
+        const int rows_max = (ks.N + grid - 1) / grid;
+        part = std::max(part, (rows_max + opst - 1) / opst * g.rs * g.wpr * (int)sizeof(float));
+    }
+    // shared scratch: the staged activation vector, or the attention unit's state
+    const int xb = prec == kBF16 ? 4 : 2;
+    int xs = std::max({H * xb, A * xb, I * xb, H * 4, step_attn_scratch_bytes(c->G)});
+    xs = round128i(xs);
+    part = round128i(part);
+    const int budget = 225 * 1024;
+    if ((H + grid - 1) / grid > 256) return TTS_ERR_ARG;           // rows of h per CTA kept in shared memory
+    const int tbl = round128i(k.n_layers * (int)sizeof(StepLayer));  // per-layer pointer table
+    int ns = (budget - 128 - tbl - xs - part) / slot;
+    if (ns > 8) ns = 8;
+    if (ns < 2) return TTS_ERR_ARG;
+    c->step_smem = 128 + tbl + xs + part + ns * slot;
+    p.ns = ns;
+    p.slot_bytes = slot;
+    p.xs_bytes = xs;
+    p.part_bytes = part;
+
+    std::vector<StepLayer> layers(k.n_layers);
+    for (int l = 0; l < k.n_layers; ++l) {
+        const LayerW& w = c->L[l];
+        layers[l] = StepLayer{w.wqkv, w.wo, w.wgu, w.wd, w.sqkv, w.so, w.sgu, w.sd, w.ln_in, w.ln_post, w.qn, w.kn};
+    }
+    TTS_TRY(dalloc(c, &c->d_layers, (size_t)k.n_layers));
+    TTS_CK(cudaMemcpy(c->d_layers, layers.data(), layers.size() * sizeof(StepLayer), cudaMemcpyHostToDevice));
+    TTS_TRY(dalloc(c, &c->gbar, 1));
+    TTS_TRY(dalloc(c, &p.h_stats, (size_t)grid));
+    TTS_TRY(dalloc(c, &p.attn_mx, (size_t)k.n_kv_heads));
+    TTS_TRY(dalloc(c, &p.act_mx, (size_t)grid));
+    TTS_CK(step_prepare(prec, c->G, c->step_smem));
+
+    p.layers = c->d_layers;
+    p.n_layers = k.n_layers;
+    p.embed = c->embed;
+    p.head = c->head;
+    p.final_norm = c->final_norm;
+    p.rope = c->rope;
+    p.kc = c->kc;
+    p.vc = c->vc;
+    p.st = c->st;
+    p.prompt = c->prompt;
+    p.h = c->h; p.qkv = c->qkv; p.attn = c->attn; p.act = c->act; p.logits = c->logits;
+    p.part_o = c->part_o; p.part_ml = c->part_ml;
+    p.att_counter = c->counters;
+    p.head_counter = c->counters + k.n_kv_heads;
+    p.gbar = c->gbar;
+    p.hist = c->hist;
+    p.hist_cap = k.max_pos;
+    p.hidden = H; p.n_q = k.n_q_heads; p.n_kv = k.n_kv_heads; p.inter = I;
+    p.n_cb = k.n_codebooks; p.cb_vocab = k.cb_vocab; p.max_pos = k.max_pos;
+    p.S = c->S;
+    p.eps = k.rms_eps;
+    {
+        const char* v = std::getenv("TTS_PF_STAGES");
+        p.pf_stages = (v && *v) ? std::atoi(v) : 8;
+    }
+    return TTS_OK;
+}
+
 int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     c->cfg = *cfg;
     const tts_config& k = c->cfg;
@@ -332,6 +435,14 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
             }
         TTS_CK(cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
     }
+    {
+        const char* mode = std::getenv("TTS_STEP_MODE");
+        c->persistent = !(mode && std::strcmp(mode, "kernels") == 0);
+    }
+    // the persistent kernel keeps a normalised activation in registers while
+    // its statistics arrive: longer hidden sizes take the graph of kernels
+    if (c->cfg.hidden > kMaxRmsK || c->attn_dim > kMaxPlainK || c->cfg.inter > kMaxPlainK) c->persistent = false;
+    if (c->persistent) TTS_TRY(setup_persistent(c));
     TTS_TRY(push_state(c, bos_state(c, 0, 0, -1)));
     TTS_TRY(capture(c, true, &c->step_exec));
     TTS_TRY(capture(c, false, &c->prefill_exec));
@@ -553,6 +664,37 @@ int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch) {
     TTS_CK(cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1));
     *ms_per_launch = ms / (float)(reps * k.n_layers);
     return TTS_OK;
+}
+
+int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, int* n_cta) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!ctx->persistent) return TTS_ERR_UNSUPPORTED;
+    const tts_config& k = ctx->cfg;
+    const int st = step_trace_stride(k.n_layers);
+    const size_t n = (size_t)st * ctx->num_sms;
+    if (!host_out || capacity < (long long)(n + 2 * 4 * 2048)) return TTS_ERR_ARG;
+    if (ctx->pos >= k.max_pos) return TTS_ERR_FULL;
+    unsigned long long* d = nullptr;
+    const int sstride = 4 * 2048;  // per-stage trace of two warps of CTA 0 (first 2048 stages)
+    const size_t ntot = n + 2 * (size_t)sstride;
+    TTS_CK(cudaMalloc(&d, ntot * sizeof(unsigned long long)));
+    TTS_CK(cudaMemsetAsync(d, 0, ntot * sizeof(unsigned long long), ctx->stream));
+    StepParams p = ctx->sp;
+    p.decode = 1;
+    p.trace = d;
+    p.trace_stride = st;
+    p.stage_trace = d + n;
+    p.stage_trace_stride = sstride;
+    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    cudaError_t e = cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream);
+    if (e == cudaSuccess) e = launch_step(p, prec, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, d, ntot * sizeof(unsigned long long), cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    cudaFree(d);
+    if (e != cudaSuccess) return report(e, "tts_trace_step");
+    if (stride) *stride = st;
+    if (n_cta) *n_cta = ctx->num_sms;
+    return pull_state(ctx);
 }
 
 int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream) {

@@ -183,6 +183,19 @@ int tts_last_steps_ms(tts_ctx* ctx, float* ms);
  * between steps.  Synchronises the stream. */
 int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch);
 
+/* Measurement hook (not part of the product path): run one decode step of
+ * the persistent step kernel with its phase trace enabled, outside the
+ * graph, and copy the trace to `host_out` (uint64 nanosecond timestamps,
+ * per CTA `stride` entries, followed by a per-ring-stage trace of two
+ * consumer warps of CTA 0, 2 x 2048 stages x 4 entries: copy issued, consumer
+ * start, consumer done (ns) and the stage's SM cycles; the layout is
+ * documented with the kernel).
+ * `capacity` is the number of uint64 the buffer holds; *stride and *n_cta
+ * receive the shape.  The step advances the position like tts_decode_step
+ * (input: the codes the previous step produced).  Returns TTS_ERR_UNSUPPORTED
+ * when the context runs the step as separate kernels. */
+int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, int* n_cta);
+
 /* Per-output-row FP8 weight quantisation on the GPU (FlashRT page,
  * Performance "FP8 W8A8"; section 8, scale amax/448): for each row n,
  * s[n] = max_k |W[n][k]| / 448 (1 if the row is zero) and
