@@ -82,12 +82,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
 
     pdl_wait();
     pdl_trigger();
-    const float sa = stage_x<FP8, PRO == kProRms>(p.x, p.gamma, p.K, p.eps, xs, red);
     XSeg<FP8> xr;
+    float sa = 1.0f;
     {
         int rslot, sg, c0, c1;
         proj_segment(j, warp, rslot, sg, c0, c1);
-        load_xseg_smem<FP8>(xs, cpr, c0, c1, xr);
+        if constexpr (!FP8 && PRO == kProPlain) {
+            load_xseg_plain(p.x, c0, c1, xr);  // plain bf16 input: straight into registers
+        } else {
+            sa = stage_x<FP8, PRO == kProRms>(p.x, p.gamma, p.K, p.eps, xs, red);
+            load_xseg_smem<FP8>(xs, cpr, c0, c1, xr);
+        }
     }
     int it = 0;
     constexpr int CEPI = EPI == kEpiLogits ? kEpiStore : EPI;

@@ -33,17 +33,26 @@ constexpr int kMaxStages = 8;
 constexpr int kBarrierBytes = 128;         // room for 8 full + 8 empty barriers
 
 // ---- chunk dot products ------------------------------------------------------
+// Two fp32 FMAs in one instruction (packed f32x2): (e, o) += (a0, a1) * (b0, b1),
+// each rounded like fmaf.
+__device__ __forceinline__ void ffma2(float& e, float& o, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 pa, pb, pc;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%0, %1};\n\t"
+        "fma.rn.f32x2 pc, pa, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pc;\n\t}"
+        : "+f"(e), "+f"(o)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // BF16: 8 weights x fp32 activations held as two float4 planes; two
-// independent FMA chains (even / odd elements) for instruction-level overlap.
+// independent FMA chains (even / odd elements), issued as packed pairs.
 __device__ __forceinline__ void dot_bf16(const uint4 w, const float4 a, const float4 b, float& e, float& o) {
-    e = fmaf(bf16lo(w.x), a.x, e);
-    o = fmaf(bf16hi(w.x), a.y, o);
-    e = fmaf(bf16lo(w.y), a.z, e);
-    o = fmaf(bf16hi(w.y), a.w, o);
-    e = fmaf(bf16lo(w.z), b.x, e);
-    o = fmaf(bf16hi(w.z), b.y, o);
-    e = fmaf(bf16lo(w.w), b.z, e);
-    o = fmaf(bf16hi(w.w), b.w, o);
+    ffma2(e, o, bf16lo(w.x), bf16hi(w.x), a.x, a.y);
+    ffma2(e, o, bf16lo(w.y), bf16hi(w.y), a.z, a.w);
+    ffma2(e, o, bf16lo(w.z), bf16hi(w.z), b.x, b.y);
+    ffma2(e, o, bf16lo(w.w), bf16hi(w.w), b.z, b.w);
 }
 
 // Two E4M3 weights (low 16 bits of w) times two f16 activations, f32 accumulate.
@@ -331,6 +340,21 @@ __device__ __forceinline__ void load_xseg_smem(const unsigned char* xs, int CPR,
     }
 }
 
+// A plain (un-normalised) fp32 activation vector for bf16 weights: the lane's
+// segment straight from global memory (through L2: other CTAs wrote it) into
+// registers, all loads in flight at once.  Needs no shared staging and no
+// block barrier.  Same values and layout as load_xseg_smem after stage_x.
+__device__ __forceinline__ void load_xseg_plain(const float* x, int c0, int c1, XSeg<false>& xr) {
+    const int lane = threadIdx.x & 31;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+#pragma unroll
+    for (int i = 0; i < kMaxLaneChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        xr.a[i] = c < c1 ? __ldcg(x4 + 2 * c) : float4{};
+        xr.b[i] = c < c1 ? __ldcg(x4 + 2 * c + 1) : float4{};
+    }
+}
+
 // Statistics a phase publishes for the next phase's activation staging.
 struct XStats {
     const float2* h;   // per producing CTA: {sum of squares, max |h * gamma_next|} (RMSNorm inputs)
@@ -575,15 +599,22 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
 // registers are allocated on their own, so the state the caller keeps across
 // phases cannot push the stage loop's activation registers into local memory.
 // Returns the advanced stage counter, or -1 if a wait ran out.
+// `xplain`: bf16 weights only, a plain activation vector read from global
+// memory directly (then xs is not used); else the shared planes in xs.
 template <bool FP8, int EPI>
 __device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, const unsigned char* xs, float sa,
                                         float* part, volatile int* abort, int* err, unsigned long long* wait_ns,
                                         const StatsOut* so, float* red, unsigned long long* stage_tr,
-                                        int stage_tr_n) {
+                                        int stage_tr_n, const float* xplain = nullptr) {
     int rslot, sg, c0, c1;
     proj_segment(j, threadIdx.x >> 5, rslot, sg, c0, c1);
     XSeg<FP8> xr;
-    load_xseg_smem<FP8>(xs, proj_cpr(j), c0, c1, xr);
+    if constexpr (!FP8) {
+        if (xplain) load_xseg_plain(xplain, c0, c1, xr);
+        else load_xseg_smem<false>(xs, proj_cpr(j), c0, c1, xr);
+    } else {
+        load_xseg_smem<true>(xs, proj_cpr(j), c0, c1, xr);
+    }
     return consume<FP8, EPI>(j, ring, it, xr, sa, part, abort, err, wait_ns, so, red, stage_tr, stage_tr_n) ? it
                                                                                                              : -1;
 }

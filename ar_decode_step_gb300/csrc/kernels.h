@@ -174,6 +174,7 @@ struct StepParams {
     int wpr[5];  // column segments (warps) per row, same order
     int ns, slot_bytes, xs_bytes, part_bytes;
     int pf_stages;  // how many stages the L2 prefetch runs ahead of the ring copies
+    int pf_max;     // ... and how far it may run ahead while the ring is full
     // optional phase trace: per CTA, trace_stride globaltimer stamps (ns)
     unsigned long long* trace;
     int trace_stride;

@@ -361,13 +361,17 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
         sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_in, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},
                                       m.xs);
     } else if constexpr (KIND == 1) {
-        sa = stage_x_stats<FP8, false>(p.attn, nullptr, A, p.eps, XStats{nullptr, p.attn_mx, p.n_kv}, m.xs);
+        // bf16: the attention output goes straight from L2 into the lanes' registers
+        sa = FP8 ? stage_x_stats<FP8, false>(p.attn, nullptr, A, p.eps, XStats{nullptr, p.attn_mx, p.n_kv}, m.xs)
+                 : 1.0f;
     } else if constexpr (KIND == 2) {
         sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_post, p.hidden, p.eps,
                                       XStats{p.h_stats, nullptr, (int)gridDim.x}, m.xs);
     } else if constexpr (KIND == 3) {
-        sa = stage_x_stats<FP8, false>(p.act, nullptr, p.inter, p.eps, XStats{nullptr, p.act_mx, (int)gridDim.x},
-                                       m.xs);
+        // bf16: the MLP activation goes straight from L2 into the lanes' registers
+        sa = FP8 ? stage_x_stats<FP8, false>(p.act, nullptr, p.inter, p.eps,
+                                             XStats{nullptr, p.act_mx, (int)gridDim.x}, m.xs)
+                 : 1.0f;
     } else {
         sa = stage_x_stats<false, true>(p.h, p.final_norm, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},
                                         m.xs);
@@ -375,27 +379,24 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
     if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers);
     else trace_mark<TRACE>(p, ev);
 
-    int rslot, sg, c0, c1;
-    proj_segment(j, threadIdx.x >> 5, rslot, sg, c0, c1);
-    XSeg<FP8> xr;
-    load_xseg_smem<FP8>(m.xs, proj_cpr(j), c0, c1, xr);
-    unsigned long long* cw = (TRACE && KIND < 4) ? cs.cwait + 4 * l + KIND : nullptr;
-    unsigned long long* cstr = TRACE ? cs.cstr : nullptr;
-    bool ok;
+    // the stage loop and epilogue in a function of their own (consume_call):
+    // allocated apart from the staging code above, it keeps the activation
+    // segment and the loop state in registers
     if constexpr (KIND == 1 || KIND == 3) {
         // residual add; publish h's statistics for the next RMSNorm (FP8: max |h * gamma_next|)
         const __nv_bfloat16* gnext = KIND == 1 ? m.sl[l].ln_post : (l + 1 < p.n_layers ? m.sl[l + 1].ln_in : p.final_norm);
         const StatsOut so{p.h_stats, FP8 ? gnext : nullptr, nullptr, s_hrows};
-        ok = consume<FP8, kEpiResid>(j, m.ring, it, xr, sa, m.part, abort, &p.st->err, cw, &so, red, cstr,
-                                     cs.cstr_n);
+        it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, &so, red,
+                                          nullptr, 0, FP8 ? nullptr : (KIND == 1 ? p.attn : p.act));
     } else if constexpr (KIND == 2) {
         const StatsOut so{nullptr, nullptr, FP8 ? p.act_mx : nullptr, nullptr};
-        ok = consume<FP8, kEpiSwiglu>(j, m.ring, it, xr, sa, m.part, abort, &p.st->err, cw, &so, red, cstr,
-                                      cs.cstr_n);
+        it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, &so, red,
+                                           nullptr, 0);
     } else {
-        ok = consume<FP8, kEpiStore>(j, m.ring, it, xr, sa, m.part, abort, &p.st->err, cw, nullptr, nullptr,
-                                     cstr, cs.cstr_n);
+        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, nullptr,
+                                          nullptr, nullptr, 0);
     }
+    const bool ok = it >= 0;
     if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 1);
     else trace_mark<TRACE>(p, ev + 1);
     return ok ? it : -1;
@@ -572,7 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 for (int s2 = 0; s2 < sg.nst; ++s2) {
                     prefetch_upto(it + p.pf_stages);
                     const uint64_t tw = pw ? globaltimer_ns() : 0;
-                    if (!mbar_wait_or_abort(&ring.empty[slot], parity, &s_abort)) {
+                    // While the slot is still busy (the consumers are in a norm, a
+                    // barrier or attention) keep HBM streaming: run the L2 prefetch
+                    // further ahead, up to p.pf_max stages past the copy cursor.
+                    bool got = mbar_try_wait(&ring.empty[slot], parity);
+                    while (!got && pq < nkinds && pidx < it + p.pf_max) {
+                        prefetch_upto(pidx + 1);
+                        got = mbar_try_wait(&ring.empty[slot], parity);
+                    }
+                    if (!got && !mbar_wait_or_abort(&ring.empty[slot], parity, &s_abort)) {
                         atomicOr(&p.st->err, kErrTimeout);
                         s_abort = 1;
                         ok = false;

@@ -309,8 +309,10 @@ int setup_persistent(tts_ctx* c) {
         part = std::max(part, (rows_max + opst - 1) / opst * g.rs * g.wpr * (int)sizeof(float));
     }
     // shared scratch: the staged activation vector, or the attention unit's state
-    const int xb = prec == kBF16 ? 4 : 2;
-    int xs = std::max({H * xb, A * xb, I * xb, H * 4, step_attn_scratch_bytes(c->G)});
+    // bf16: plain inputs (attention output, MLP activation) are read into
+    // registers directly, only RMSNorm inputs are staged; FP8 stages all (quantised)
+    int xs = prec == kBF16 ? std::max(H * 4, step_attn_scratch_bytes(c->G))
+                           : std::max({H * 2, A * 2, I * 2, H * 4, step_attn_scratch_bytes(c->G)});
     xs = round128i(xs);
     part = round128i(part);
     const int budget = 225 * 1024;
@@ -360,8 +362,11 @@ int setup_persistent(tts_ctx* c) {
     p.S = c->S;
     p.eps = k.rms_eps;
     {
+        // L2 prefetch lookahead in ring stages: steady state, and while the ring is full
         const char* v = std::getenv("TTS_PF_STAGES");
-        p.pf_stages = (v && *v) ? std::atoi(v) : 8;
+        p.pf_stages = (v && *v) ? std::max(0, std::atoi(v)) : 4;
+        const char* vm = std::getenv("TTS_PF_MAX");
+        p.pf_max = std::max(p.pf_stages, (vm && *vm) ? std::atoi(vm) : 12);
     }
     return TTS_OK;
 }
