@@ -68,20 +68,32 @@ def step_bytes(d, precision: int, ctx_len: int) -> float:
     return d.n_layers * (per_layer + kv_read + kv_write) + head + embed
 
 
-def gemv_bytes(d, precision: int, kind: int) -> float:
-    """Algorithmic bytes of one GEMV launch: weights (+ FP8 scales) plus the
-    input and output vectors."""
-    H, I, D = d.hidden, d.inter, d.head_dim
-    qkv = (d.n_q + 2 * d.n_kv) * D
-    wb = 1 if precision == 1 else 2
-    rows, K, nout = {0: (qkv, H, qkv), 1: (H, d.n_q * D, H), 2: (2 * I, H, I), 3: (H, I, H),
-                     4: (d.n_cb * d.cb_vocab, H, d.n_cb * d.cb_vocab)}[kind]
-    if kind == 4:
-        wb = 2
-    b = rows * K * wb + K * 4 + nout * 4
-    if precision == 1 and kind != 4:
-        b += rows * 4
-    return b
+def source_digest() -> str:
+    """Hash of the step kernel's sources: a stored ncu traffic figure is only
+    used while the kernel it was taken from is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ar_decode_step_gb300", "csrc")
+    for name in ("step_kernel.cuh", "gemv_core.cuh", "common.cuh", "kernels.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(wl_name: str):
+    """DRAM bytes (read + write) per launch of step_kernel for this workload,
+    from the ncu summary under profiles/ (null when absent or stale)."""
+    p = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None, "no ncu capture"
+    with open(p) as f:
+        j = json.load(f)
+    if j.get("source_digest") != source_digest():
+        return None, "kernel changed since the ncu capture"
+    w = j.get("workloads", {}).get(wl_name)
+    if not w:
+        return None, "workload not captured"
+    return float(w["bytes_per_launch"]), j.get("method", "ncu")
 
 
 class ClockSampler:
@@ -254,7 +266,7 @@ def run_gpu(args, wl_name, wl):
     max_pos = ctx0 + seg + 8
     dec = ads.Decoder(ads.Dims(**{f: getattr(d, f) for f in ("n_layers", "hidden", "n_q", "n_kv", "head_dim",
                                                               "inter", "n_cb", "cb_vocab")}),
-                      dw, max_pos)
+                      dw, max_pos, stream=torch.cuda.current_stream().cuda_stream)
     prefill_ms = None
     if wl["prompt"]:
         prompt = synth.delayed_prompt_codes(wl["prompt"])
@@ -313,20 +325,11 @@ def run_gpu(args, wl_name, wl):
     ms_per_step = ms_total / args.steps
     value = world * args.steps / (ms_total / 1e3)
 
-    # roofline of the dominant kernel (gate/up GEMV, about half the step's bytes)
-    kind = 2
-    reps = 3
-    dec.time_gemv(kind, 1)
-    ms_launch = dec.time_gemv(kind, reps)
-    gb = gemv_bytes(d, wl["precision"], kind)
-    peak, peak_kind = read_peaks()
-    achieved = gb / (ms_launch * 1e-3) / 1e9
-    per_kind = {}
-    for kk, name in enumerate(["qkv", "o_proj", "gate_up", "down", "head"]):
-        ms_k = dec.time_gemv(kk, 2)
-        per_kind[name] = {"ms": ms_k, "GB/s": gemv_bytes(d, wl["precision"], kk) / (ms_k * 1e-3) / 1e9}
-
-    # whole-step roofline: mean algorithmic bytes over the timed contexts
+    # roofline of the dominant kernel.  Persistent mode: the step is one launch
+    # of step_kernel per frame, so its mean duration is the timed region / frames
+    # (each frame also carries a 4-byte memset of the grid-barrier counter and
+    # the graph-launch gap, both counted against the kernel).  Algorithmic bytes
+    # per launch: the mean over the timed contexts.
     ctxs = []
     t = 0
     for _ in range(args.steps):
@@ -335,7 +338,15 @@ def run_gpu(args, wl_name, wl):
         ctxs.append(ctx0 + t + 1)
         t += 1
     mean_bytes = float(np.mean([step_bytes(d, wl["precision"], c) for c in ctxs]))
-    step_gbs = mean_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = read_peaks()
+    persistent = os.environ.get("TTS_STEP_MODE", "") != "kernels"
+    achieved = mean_bytes / (ms_per_step * 1e-3) / 1e9
+    traffic, traffic_note = read_traffic(wl_name) if persistent else (None, "not captured for separate kernels")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "kernel": "step_kernel (whole decode step, one launch per frame)"
+                if persistent else "whole step as separate kernels (per-frame graph)",
+                "bytes_per_launch": mean_bytes, "ms_per_launch": ms_per_step, "peak_source": peak_kind,
+                "traffic_source": traffic_note}
 
     # end to end through the public C ABI with host buffers: each frame copies
     # its 8 input codes host->device and reads the state (codes) back
@@ -360,7 +371,7 @@ def run_gpu(args, wl_name, wl):
                         "sample": f"{nfr} whole decode frames of the same {wl['n_layers']}-layer model "
                                   f"(same weights) at context {ctx0 + 1}..{ctx0 + nfr}, fp64 C oracle"}
 
-    launches_per_step = 1 + 5 * d.n_layers + 1
+    launches_per_step = 1 if persistent else 1 + 5 * d.n_layers + 1
     line = {
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -370,11 +381,7 @@ def run_gpu(args, wl_name, wl):
                    "frames_per_segment": seg, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (all weights streamed every frame)",
                    "weights": "seeded N(0,0.02)", "graph": "one CUDA graph per frame"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "gate/up GEMV + SwiGLU",
-                     "bytes_per_launch": gb, "ms_per_launch": ms_launch, "peak_source": peak_kind},
-        "step_roofline": {"bytes_per_step": mean_bytes, "achieved_GBps": step_gbs, "frac": step_gbs / peak},
-        "per_kernel": per_kind,
+        "roofline": roofline,
         "clocks": clock_info,
         "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 4 * d.n_cb,
                 "d2h_bytes_per_step": 64, "frames": n_e2e},
@@ -399,10 +406,14 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's depth (small profiling cases only; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers > 0:
+        wl["n_layers"] = args.layers
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:
             return
