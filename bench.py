@@ -83,7 +83,7 @@ def source_digest() -> str:
 def read_traffic(wl_name: str):
     """DRAM bytes (read + write) per launch of step_kernel for this workload,
     from the ncu summary under profiles/ (null when absent or stale)."""
-    p = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+    p = os.path.join(ROOT, "profiles", "step_kernel_traffic.txt")
     if not os.path.exists(p):
         return None, "no ncu capture"
     with open(p) as f:
