@@ -82,6 +82,10 @@ def lib():
                                          ctypes.POINTER(_State), vp, vp, vp, vp]),
                 "or_prefill": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
                                      ctypes.POINTER(_State), vp, i32, i32]),
+                "or_layer": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
+                                   ctypes.POINTER(_State), i32, i32, vp]),
+                "or_head": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
+                                  ctypes.POINTER(_State), vp, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -267,6 +271,33 @@ class Oracle:
                                   ctypes.byref(self.st), _p(c), _p(out), _p(logits), _p(gaps))
         if rc:
             raise ValueError(f"or_decode_step failed ({rc})")
+        return out, logits, gaps
+
+    def embed(self, codes_in) -> np.ndarray:
+        """The step's input residual stream for these codes."""
+        return embed(self.w.embed, codes_in)
+
+    def layer(self, layer: int, pos: int, h) -> np.ndarray:
+        """Layer `layer` at position pos applied to the residual stream h
+        (returns the layer's output; writes that layer's K/V at pos)."""
+        x = np.ascontiguousarray(h, np.float64).copy()
+        rc = lib().or_layer(ctypes.byref(self.cdims), ctypes.byref(self.cw), ctypes.byref(self.st),
+                            int(layer), int(pos), _p(x))
+        if rc:
+            raise ValueError(f"or_layer failed ({rc})")
+        return x
+
+    def head(self, h):
+        """(codes, logits, gaps) of the head on the final residual stream h at
+        the current frame (no state change)."""
+        x = np.ascontiguousarray(h, np.float64)
+        out = np.empty(self.dims.n_cb, np.int32)
+        logits = np.empty((self.dims.n_cb, self.dims.cb_vocab), np.float64)
+        gaps = np.empty(self.dims.n_cb, np.float64)
+        rc = lib().or_head(ctypes.byref(self.cdims), ctypes.byref(self.cw), ctypes.byref(self.st), _p(x),
+                           _p(out), _p(logits), _p(gaps))
+        if rc:
+            raise ValueError(f"or_head failed ({rc})")
         return out, logits, gaps
 
     def prefill(self, codes, a16: bool = False):

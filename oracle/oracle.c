@@ -270,10 +270,11 @@ static int check_dims(const or_dims* d) {
 
 static double round_bf16(double x) { return or_bf16_to_f64(or_f64_to_bf16(x)); }
 
-/* One position through all layers: h holds the embedded input on entry and
- * the last layer's residual stream on exit.  Writes K/V at `pos`. */
-static void layer_stack(const or_dims* d, const or_weights* w, or_state* st, int pos,
-                        double* h, int a16) {
+/* One position through layers [l0, l1): h holds that layer's input
+ * residual stream on entry and layer l1-1's output on exit.  Writes K/V of
+ * those layers at `pos`. */
+static void stack_layers(const or_dims* d, const or_weights* w, or_state* st, int pos,
+                         double* h, int a16, int l0, int l1) {
     const int H = d->hidden, D = d->head_dim, NQ = d->n_q, NKV = d->n_kv, I = d->inter;
     const int QKV = (NQ + 2 * NKV) * D, A = NQ * D;
     const int fp8 = d->precision == 1;
@@ -288,7 +289,7 @@ static void layer_stack(const or_dims* d, const or_weights* w, or_state* st, int
     if (I > maxv) maxv = I;
     uint8_t* q8 = (uint8_t*)malloc((size_t)maxv);
 
-    for (int l = 0; l < d->n_layers; ++l) {
+    for (int l = l0; l < l1; ++l) {
         size_t cache_off = (size_t)l * NKV * d->max_pos * D;
         uint16_t* Kl = st->k + cache_off;
         uint16_t* Vl = st->v + cache_off;
@@ -364,27 +365,22 @@ static void layer_stack(const or_dims* d, const or_weights* w, or_state* st, int
     free(a); free(qkv); free(attn); free(o); free(gu); free(m); free(tmp); free(q8);
 }
 
-int or_decode_step(const or_dims* d, const or_weights* w, or_state* st,
-                   const int32_t* codes_in, int32_t* codes_out,
-                   double* logits, double* gaps) {
-    if (check_dims(d) || !w || !st || !codes_in || !codes_out) return -1;
-    if (st->pos < 0 || st->pos >= d->max_pos) return -1;
-    for (int k = 0; k < d->n_cb; ++k)
-        if (codes_in[k] < 0 || codes_in[k] >= d->cb_vocab) return -1;
+static void layer_stack(const or_dims* d, const or_weights* w, or_state* st, int pos,
+                        double* h, int a16) {
+    stack_layers(d, w, st, pos, h, a16, 0, d->n_layers);
+}
+
+/* Final RMSNorm, fused codebook head and per-codebook greedy argmax under the
+ * delay pattern at frame st->t (bf16 weights in both precisions, no
+ * activation quantisation) [FlashRT s5 "fused 8-codebook head"; FlashRT s4,
+ * s5 sampling].  Reads the state, changes nothing. */
+static void head_codes(const or_dims* d, const or_weights* w, const or_state* st, const double* h,
+                       int32_t* codes_out, double* logits, double* gaps) {
     const int H = d->hidden, V = d->cb_vocab, C = d->n_cb;
-    double* h = (double*)malloc(sizeof(double) * H);
     double* f = (double*)malloc(sizeof(double) * H);
     double* lg = (double*)malloc(sizeof(double) * (size_t)C * V);
-
-    or_embed(w->embed, C, V, H, codes_in, h);
-    layer_stack(d, w, st, st->pos, h, 0);
-
-    /* final RMSNorm and the fused codebook head (bf16 weights in both
-     * precisions, no activation quantisation) [FlashRT s5 "fused 8-codebook head"] */
     or_rmsnorm(h, w->final_norm, H, d->rms_eps, f);
     or_linear_bf16(w->head, C * V, H, f, lg);
-
-    /* per-codebook greedy argmax under the delay pattern [FlashRT s4, s5] */
     int t = st->t, eoc = st->eoc;
     for (int k = 0; k < C; ++k) {
         const double* row = lg + (size_t)k * V;
@@ -397,11 +393,41 @@ int or_decode_step(const or_dims* d, const or_weights* w, or_state* st,
         }
         codes_out[k] = or_delay_code(k, t, eoc, am);
     }
-    if (eoc < 0 && codes_out[0] == 1025) st->eoc = t;
     if (logits) memcpy(logits, lg, sizeof(double) * (size_t)C * V);
+    free(f);
+    free(lg);
+}
+
+int or_layer(const or_dims* d, const or_weights* w, or_state* st, int layer, int pos, double* h) {
+    if (check_dims(d) || !w || !st || !h || layer < 0 || layer >= d->n_layers || pos < 0 || pos >= d->max_pos)
+        return -1;
+    stack_layers(d, w, st, pos, h, 0, layer, layer + 1);
+    return 0;
+}
+
+int or_head(const or_dims* d, const or_weights* w, const or_state* st, const double* h,
+            int32_t* codes_out, double* logits, double* gaps) {
+    if (check_dims(d) || !w || !st || !h || !codes_out) return -1;
+    head_codes(d, w, st, h, codes_out, logits, gaps);
+    return 0;
+}
+
+int or_decode_step(const or_dims* d, const or_weights* w, or_state* st,
+                   const int32_t* codes_in, int32_t* codes_out,
+                   double* logits, double* gaps) {
+    if (check_dims(d) || !w || !st || !codes_in || !codes_out) return -1;
+    if (st->pos < 0 || st->pos >= d->max_pos) return -1;
+    for (int k = 0; k < d->n_cb; ++k)
+        if (codes_in[k] < 0 || codes_in[k] >= d->cb_vocab) return -1;
+    const int H = d->hidden, V = d->cb_vocab, C = d->n_cb;
+    double* h = (double*)malloc(sizeof(double) * H);
+    or_embed(w->embed, C, V, H, codes_in, h);
+    layer_stack(d, w, st, st->pos, h, 0);
+    head_codes(d, w, st, h, codes_out, logits, gaps);
+    if (st->eoc < 0 && codes_out[0] == 1025) st->eoc = st->t;
     st->pos += 1;
     st->t += 1;
-    free(h); free(f); free(lg);
+    free(h);
     return 0;
 }
 

@@ -94,6 +94,17 @@ int or_decode_step(const or_dims* d, const or_weights* w, or_state* st,
                    const int32_t* codes_in, int32_t* codes_out,
                    double* logits, double* gaps);
 
+/* One layer `layer` at position pos (layer-level checks): h holds the
+ * layer's input residual stream on entry and its output on exit; writes that
+ * layer's K/V at pos.  Changes neither pos nor t.  Returns 0 or -1. */
+int or_layer(const or_dims* d, const or_weights* w, or_state* st, int layer, int pos, double* h);
+
+/* The head of the step on a given final residual stream h: final RMSNorm,
+ * codebook logits, argmax under the delay mask at frame st->t (codes_out,
+ * logits and gaps as in or_decode_step).  Changes nothing.  Returns 0 or -1. */
+int or_head(const or_dims* d, const or_weights* w, const or_state* st, const double* h,
+            int32_t* codes_out, double* logits, double* gaps);
+
 /* Prefill: runs the layer stack at positions st->pos .. st->pos+P-1 with the
  * given codes (row p = the n_cb codes of position p), writing K/V; no head.
  * a16 != 0 rounds the input of every projection to bf16 (the tensor-core

@@ -212,3 +212,29 @@ def test_oracle_rejects_bad_input():
         orc.decode_step(np.array([0, 0, 0, 1026, 0, 0, 0, 0], np.int32))
     with pytest.raises(ValueError):
         orc.prefill(np.zeros((MAXPOS + 1, 8), np.int32))
+
+
+@pytest.mark.parametrize("precision", [0, 1])
+def test_step_equals_embed_layers_head(precision):
+    """The layer-level entry points compose to the step exactly (same logits,
+    codes, gaps and KV rows): what the full-depth GPU checks build on."""
+    w = synth.make_weights(TINY, gamma_variant=True)
+    a = oracle.Oracle(w, MAXPOS, precision=precision)
+    b = oracle.Oracle(w, MAXPOS, precision=precision)
+    k, v = synth.make_kv_prefix(TINY, 5, MAXPOS)
+    a.set_kv(k, v, 5)
+    b.set_kv(k, v, 5)
+    a.set_frame(3)
+    b.set_frame(3)
+    codes = synth.random_codes(1, seed=2, stream=5)[0]
+    ca, la, ga = a.decode_step(codes)
+    h = b.embed(codes)
+    for l in range(TINY.n_layers):
+        h = b.layer(l, 5, h)
+    cb, lb, gb = b.head(h)
+    assert np.array_equal(ca, cb)
+    assert np.array_equal(la, lb)
+    assert np.array_equal(ga, gb)
+    assert np.array_equal(a.k[:, :, :6], b.k[:, :, :6]) and np.array_equal(a.v[:, :, :6], b.v[:, :, :6])
+    # the layer call leaves the position alone; the step advanced it
+    assert b.pos == 5 and a.pos == 6
