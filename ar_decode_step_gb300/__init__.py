@@ -66,6 +66,7 @@ SIGNATURES = {
     "tts_last_steps_ms": (_I, [_VP, _VP]),
     "tts_time_gemv": (_I, [_VP, _I, _I, _VP]),
     "tts_trace_step": (_I, [_VP, _VP, _I, _VP, _VP]),
+    "tts_debug_layer_states": (_I, [_VP, _VP, _VP, _VP, _I]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_attention_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -305,6 +306,17 @@ class Decoder:
         n = st.value * nc.value
         self.last_stage_trace = buf[n: n + 2 * 4 * 2048].reshape(2, 2048, 4)
         return buf[:n].reshape(nc.value, st.value)
+
+    def layer_states(self, codes_in=None):
+        """One decode step (as decode_step) through the traced step kernel,
+        returning (codes, hidden states [n_layers + 1][hidden]): the residual
+        stream after the embedding and after each layer."""
+        n = (self.dims.n_layers + 1) * self.dims.hidden
+        buf = np.zeros(n, np.float32)
+        out = np.empty(self.dims.n_cb, np.int32)
+        c = None if codes_in is None else np.ascontiguousarray(codes_in, np.int32)
+        _call("tts_debug_layer_states", self._ctx, None if c is None else _ptr(c), _ptr(out), _ptr(buf), n)
+        return out, buf.reshape(self.dims.n_layers + 1, self.dims.hidden)
 
     def last_steps_ms(self) -> float:
         ms = ctypes.c_float()

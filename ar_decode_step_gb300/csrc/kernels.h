@@ -184,6 +184,9 @@ struct StepParams {
     // consumer warp (next stage_trace_stride entries; no issue time)
     unsigned long long* stage_trace;
     int stage_trace_stride;
+    // optional (traced launches): the residual stream after the embedding and
+    // after every layer, [n_layers + 1][hidden] fp32
+    float* hsnap;
 };
 
 // Phase-trace layout of the persistent kernel, per CTA (see step.cu):

@@ -388,6 +388,12 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
         const StatsOut so{p.h_stats, FP8 ? gnext : nullptr, nullptr, s_hrows};
         it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, &so, red,
                                           nullptr, 0, FP8 ? nullptr : (KIND == 1 ? p.attn : p.act));
+        if constexpr (TRACE && KIND == 3) {
+            // layer-level checks: this CTA's rows of the residual stream after the layer
+            if (p.hsnap && it >= 0)
+                for (int r = threadIdx.x; r < j.r1 - j.r0; r += kConsumers)
+                    p.hsnap[(size_t)(l + 1) * p.hidden + j.r0 + r] = s_hrows[r];
+        }
     } else if constexpr (KIND == 2) {
         const StatsOut so{nullptr, nullptr, FP8 ? p.act_mx : nullptr, nullptr};
         it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, &so, red,
@@ -643,6 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 acc += __bfloat162float(p.embed[((size_t)k * p.cb_vocab + s_codes[k]) * p.hidden + i]);
             p.h[i] = acc;
             s_hrows[i - i0] = acc;
+            if constexpr (TRACE)
+                if (p.hsnap) p.hsnap[i] = acc;
             ss += acc * acc;
             mxg = fmaxf(mxg, fabsf(acc * __bfloat162float(g0[i])));
         }

@@ -702,6 +702,48 @@ int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, 
     return pull_state(ctx);
 }
 
+int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out, float* host_h,
+                           int capacity) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!ctx->persistent) return TTS_ERR_UNSUPPORTED;
+    const tts_config& k = ctx->cfg;
+    const size_t nh = (size_t)(k.n_layers + 1) * k.hidden;
+    if (!host_h || capacity < (long long)nh) return TTS_ERR_ARG;
+    if (ctx->pos >= k.max_pos) return TTS_ERR_FULL;
+    if (codes_in) {
+        for (int i = 0; i < k.n_codebooks; ++i)
+            if (codes_in[i] < 0 || codes_in[i] >= k.cb_vocab) return TTS_ERR_CODE;
+        std::memcpy(ctx->h_in->codes, codes_in, sizeof(int32_t) * k.n_codebooks);
+        TTS_CK(cudaMemcpyAsync(ctx->st->codes, ctx->h_in->codes, sizeof(int32_t) * k.n_codebooks,
+                               cudaMemcpyHostToDevice, ctx->stream));
+    }
+    const int st = step_trace_stride(k.n_layers);
+    const size_t nt = (size_t)st * ctx->num_sms;
+    unsigned long long* d = nullptr;
+    float* hs = nullptr;
+    TTS_CK(cudaMalloc(&d, nt * sizeof(unsigned long long)));
+    cudaError_t e = cudaMalloc(&hs, nh * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemsetAsync(hs, 0, nh * sizeof(float), ctx->stream);
+    StepParams p = ctx->sp;
+    p.decode = 1;
+    p.trace = d;
+    p.trace_stride = st;
+    p.stage_trace = nullptr;
+    p.stage_trace_stride = 0;
+    p.hsnap = hs;
+    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream);
+    if (e == cudaSuccess) e = launch_step(p, prec, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(host_h, hs, nh * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    cudaFree(d);
+    if (hs) cudaFree(hs);
+    if (e != cudaSuccess) return report(e, "tts_debug_layer_states");
+    const int rc = pull_state(ctx);
+    if (rc == TTS_OK && codes_out) std::memcpy(codes_out, ctx->h_out->codes, sizeof(int32_t) * k.n_codebooks);
+    return rc;
+}
+
 int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream) {
     if (!W || !W8 || !s || N <= 0 || K <= 0) return TTS_ERR_ARG;
     TTS_CK(launch_quantize_weight(static_cast<const __nv_bfloat16*>(W), N, K, static_cast<uint8_t*>(W8), s,

@@ -196,6 +196,18 @@ int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch);
  * when the context runs the step as separate kernels. */
 int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, int* n_cta);
 
+/* Test hook (not part of the product path): one decode step like
+ * tts_decode_step(ctx, codes_in, codes_out) (codes_in may be NULL: the
+ * device's own codes; codes_out may be NULL), run by the traced variant of the step kernel, which also
+ * records the fp32 residual stream after the embedding and after every layer
+ * into `host_h` ([n_layers + 1][hidden], row 0 = the embedding; caller-owned,
+ * `capacity` floats).  Lets a check start the CPU oracle's layer l from the
+ * GPU's own input to that layer ("Higgs Audio v3 TTS-4B on FlashRT", section
+ * 5, one layer of the chain).  Returns TTS_ERR_UNSUPPORTED when the step runs
+ * as separate kernels, TTS_ERR_ARG if capacity is short; synchronises. */
+int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out, float* host_h,
+                           int capacity);
+
 /* Per-output-row FP8 weight quantisation on the GPU (FlashRT page,
  * Performance "FP8 W8A8"; section 8, scale amax/448): for each row n,
  * s[n] = max_k |W[n][k]| / 448 (1 if the row is zero) and
