@@ -67,6 +67,7 @@ SIGNATURES = {
     "tts_time_gemv": (_I, [_VP, _I, _I, _VP]),
     "tts_trace_step": (_I, [_VP, _VP, _I, _VP, _VP]),
     "tts_debug_layer_states": (_I, [_VP, _VP, _VP, _VP, _I]),
+    "tts_gemm_bf16": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_attention_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -119,6 +120,15 @@ def _torch():
 def _to_dev_u16(a: np.ndarray, device):
     torch = _torch()
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device, non_blocking=False)
+
+
+def gemm_bf16(a_dev, b_dev, c_dev, epi: int = 0, splits: int = 1, stream=None):
+    """C = A . B^T on the tensor cores (see tts_gemm_bf16): a_dev [M][K] and
+    b_dev [N][K] (epi 2: [2N][K]) bf16 CUDA tensors; c_dev fp32 [M][N]
+    (epi 0, 1) or bf16 [M][N] (epi 2)."""
+    M, K = a_dev.shape
+    N = c_dev.shape[1]
+    _call("tts_gemm_bf16", a_dev.data_ptr(), b_dev.data_ptr(), c_dev.data_ptr(), M, N, K, epi, splits, stream)
 
 
 def quantize_fp8_weight(w_dev, stream=None):

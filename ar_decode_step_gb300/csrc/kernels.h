@@ -206,6 +206,24 @@ int step_attn_scratch_bytes(int G);
 int step_threads();
 cudaError_t launch_step(const StepParams& p, int prec, int G, int grid, int smem, cudaStream_t s);
 
+// C = A . B^T on the tensor cores (gemm_tc.cu): A [M][K] and B [N][K] bf16,
+// K-major, fp32 accumulation.  Epilogues: store fp32 C[M][ldc]; add into fp32
+// C (residual stream, split-K partials); SwiGLU: B = [gate rows; up rows] of
+// a [2 n_half][K] matrix, out_bf16[M][ldc] = bf16(silu(gate) * up), N = n_half.
+enum GemmEpi { kGemmStore = 0, kGemmAdd = 1, kGemmSwiglu = 2 };
+struct GemmParams {
+    float* C;
+    __nv_bfloat16* out_bf16;
+    int ldc;
+    int M, N, K;
+    int n_half;
+    int kb_per_split;  // filled in by launch_gemm_bf16
+    int* err;          // error word (kErrTimeout on an expired wait), may be NULL
+};
+bool gemm_shape_ok(int M, int N, int K, int epi);
+cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p, int epi, int splits,
+                             cudaStream_t s);
+
 // Per-row E4M3 weight quantisation.
 cudaError_t launch_quantize_weight(const __nv_bfloat16* W, int N, int K, uint8_t* W8, float* s,
                                    cudaStream_t st);

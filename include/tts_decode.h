@@ -208,6 +208,22 @@ int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, 
 int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out, float* host_h,
                            int capacity);
 
+/* Stand-alone op: C = A . B^T on the tensor cores (tcgen05 MMA, TMEM
+ * accumulators, TMA-staged operands), the GEMM of the batched prompt prefill
+ * ("Higgs Audio v3 TTS-4B on FlashRT", Performance "BF16 W16A16" and section
+ * 7: the prompt runs as one M = P pass over the weights).
+ *   A: device bf16 [M][K] row-major (activations), B: device bf16 [N][K]
+ *   (weights, one output feature per row), both borrowed, 16-byte aligned.
+ *   epi 0: C = device fp32 [M][N], overwritten.
+ *   epi 1: C = device fp32 [M][N], C += A . B^T (fp32 atomic adds; with
+ *          splits > 1 the K range is split over that many CTAs per tile).
+ *   epi 2: SwiGLU: B = [gate rows; up rows], a [2N][K] matrix; C = device
+ *          bf16 [M][N] = bf16(silu(A . gate^T) * (A . up^T)).
+ * fp32 accumulation; K % 64 == 0, N % 128 == 0, any M >= 1.  Enqueued on
+ * `stream` (NULL: the default stream); does not synchronise.  Returns
+ * TTS_ERR_ARG for bad sizes, NULL or misaligned pointers. */
+int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, int epi, int splits, void* stream);
+
 /* Per-output-row FP8 weight quantisation on the GPU (FlashRT page,
  * Performance "FP8 W8A8"; section 8, scale amax/448): for each row n,
  * s[n] = max_k |W[n][k]| / 448 (1 if the row is zero) and

@@ -1,0 +1,81 @@
+"""The tensor-core GEMM of the batched prefill (tts_gemm_bf16) against the CPU
+oracle's linear layer (fp64 sums of the same bf16 operands): plain store,
+additive epilogue with split-K, and the fused gate/up + SwiGLU epilogue, on
+shapes with ragged M (rows past M are masked), several N tiles and several
+k-blocks."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import ar_decode_step_gb300.build as b
+    b.build()
+    import ar_decode_step_gb300 as m
+    m.load()
+    return m, torch
+
+
+def bf16_dev(torch, bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def f64(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def ref_rows(Wb, Ab):
+    """Oracle linear layer applied to every row of A: [M][N] fp64."""
+    return np.stack([oracle.linear_bf16(Wb, f64(Ab[i])) for i in range(Ab.shape[0])])
+
+
+@pytest.mark.parametrize("M,N,K", [(37, 128, 64), (200, 256, 512), (300, 384, 2560)])
+def test_gemm_store(env, M, N, K):
+    ads, torch = env
+    Ab = synth.normal_bf16(2, 101, (M, K))
+    Wb = synth.normal_bf16(2, 102, (N, K), std=0.02)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ads.gemm_bf16(bf16_dev(torch, Ab), bf16_dev(torch, Wb), C, epi=0)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy().astype(np.float64)
+    ref = ref_rows(Wb, Ab)
+    assert np.isfinite(got).all()
+    assert np.allclose(got, ref, rtol=1e-4, atol=1e-4 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_gemm_add_split_k(env, splits):
+    ads, torch = env
+    M, N, K = 150, 256, 1024
+    Ab = synth.normal_bf16(2, 103, (M, K))
+    Wb = synth.normal_bf16(2, 104, (N, K), std=0.02)
+    base = synth.normal_f32(2, 105, (M, N))
+    C = torch.from_numpy(base.copy()).cuda()
+    ads.gemm_bf16(bf16_dev(torch, Ab), bf16_dev(torch, Wb), C, epi=1, splits=splits)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy().astype(np.float64)
+    ref = base.astype(np.float64) + ref_rows(Wb, Ab)
+    assert np.allclose(got, ref, rtol=1e-4, atol=2e-4 * np.abs(ref).max())
+
+
+def test_gemm_swiglu(env):
+    ads, torch = env
+    M, N, K = 130, 256, 512
+    Ab = synth.normal_bf16(2, 106, (M, K))
+    Wb = synth.normal_bf16(2, 107, (2 * N, K), std=0.05)
+    out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    ads.gemm_bf16(bf16_dev(torch, Ab), bf16_dev(torch, Wb), out, epi=2)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    gu = ref_rows(Wb, Ab)
+    g, u = gu[:, :N], gu[:, N:]
+    ref = g / (1.0 + np.exp(-g)) * u
+    # one bf16 rounding of an fp32 value: within 2^-8 relative (plus tiny values)
+    assert np.allclose(got, ref, rtol=2 ** -7, atol=1e-3 * np.abs(ref).max())
