@@ -68,6 +68,7 @@ SIGNATURES = {
     "tts_trace_step": (_I, [_VP, _VP, _I, _VP, _VP]),
     "tts_debug_layer_states": (_I, [_VP, _VP, _VP, _VP, _I]),
     "tts_gemm_bf16": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tts_debug_prefill_states": (_I, [_VP, _VP, _I, _VP, ctypes.c_longlong]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_attention_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -327,6 +328,16 @@ class Decoder:
         c = None if codes_in is None else np.ascontiguousarray(codes_in, np.int32)
         _call("tts_debug_layer_states", self._ctx, None if c is None else _ptr(c), _ptr(out), _ptr(buf), n)
         return out, buf.reshape(self.dims.n_layers + 1, self.dims.hidden)
+
+    def prefill_states(self, codes):
+        """prefill(codes) on the batched path, returning the residual stream of
+        every row after the embedding and after each layer: [n_layers + 1][P][hidden]."""
+        c = np.ascontiguousarray(codes, np.int32)
+        P = c.shape[0]
+        n = (self.dims.n_layers + 1) * P * self.dims.hidden
+        buf = np.zeros(n, np.float32)
+        _call("tts_debug_prefill_states", self._ctx, _ptr(c), P, _ptr(buf), n)
+        return buf.reshape(self.dims.n_layers + 1, P, self.dims.hidden)
 
     def last_steps_ms(self) -> float:
         ms = ctypes.c_float()

@@ -6,7 +6,7 @@
 // are dense contractions of P rows against every weight matrix, so they run
 // here rather than on the M = 1 weight-streaming path.
 //
-// One CTA per 128 x BN output tile (BN = 128; 256 for the fused gate/up tile):
+// One CTA per 128 x BN output tile (BN = 64 or 128; 256 for the fused gate/up tile):
 //   warp 0 (one thread)  TMA producer: 128 x 64 A box and BN x 64 B box(es)
 //                        per k-block into a 4-stage ring (128-byte swizzle),
 //                        completion counted on the stage's "full" mbarrier;
@@ -221,9 +221,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
                         *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-                } else {
+                } else if (p.atomic) {  // split-K partials: several CTAs add into the same tile
 #pragma unroll
                     for (int e = 0; e < 16; ++e) atomicAdd(dst + e, v[e]);
+                } else {  // the only writer of these elements: deterministic
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        float4 o = *reinterpret_cast<const float4*>(dst + e);
+                        o.x += v[e];
+                        o.y += v[e + 1];
+                        o.z += v[e + 2];
+                        o.w += v[e + 3];
+                        *reinterpret_cast<float4*>(dst + e) = o;
+                    }
                 }
             }
         }
@@ -287,30 +297,33 @@ cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParam
 
 }  // namespace
 
-bool gemm_shape_ok(int M, int N, int K, int epi) {
-    const int nt = 128;
-    return M > 0 && N > 0 && K > 0 && K % kBK == 0 && N % nt == 0 && (epi != kGemmSwiglu || N % 128 == 0);
+bool gemm_shape_ok(int M, int N, int K, int epi, int bn) {
+    return M > 0 && N > 0 && K > 0 && K % kBK == 0 && (bn == 64 || bn == 128) && N % bn == 0 &&
+           (epi != kGemmSwiglu || bn == 128);
 }
 
 cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p_in, int epi, int splits,
                              cudaStream_t s) {
     GemmParams p = p_in;
-    if (!gemm_shape_ok(p.M, p.N, p.K, epi) || splits < 1) return cudaErrorInvalidValue;
+    if (p.bn == 0) p.bn = 128;
+    if (!gemm_shape_ok(p.M, p.N, p.K, epi, p.bn) || splits < 1) return cudaErrorInvalidValue;
     const int nkb = p.K / kBK;
     if (epi != kGemmAdd) splits = 1;  // only an additive epilogue can take split-K partials
     p.kb_per_split = (nkb + splits - 1) / splits;
     splits = (nkb + p.kb_per_split - 1) / p.kb_per_split;
+    p.atomic = splits > 1 ? 1 : 0;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, p.M, p.K, kBM)) return cudaErrorInvalidValue;
-    const dim3 grid(p.N / 128, (p.M + kBM - 1) / kBM, splits);
+    const dim3 grid(p.N / p.bn, (p.M + kBM - 1) / kBM, splits);
     if (epi == kGemmSwiglu) {
         // B = [gate rows; up rows] of a [2 n_half][K] matrix; N = n_half output columns
         if (!make_map(&mb, B, 2 * p.n_half, p.K, 128)) return cudaErrorInvalidValue;
         return launch_t<kGemmSwiglu, 256>(ma, mb, p, grid, s);
     }
-    if (!make_map(&mb, B, p.N, p.K, 128)) return cudaErrorInvalidValue;
-    if (epi == kGemmStore) return launch_t<kGemmStore, 128>(ma, mb, p, grid, s);
-    return launch_t<kGemmAdd, 128>(ma, mb, p, grid, s);
+    if (!make_map(&mb, B, p.N, p.K, p.bn)) return cudaErrorInvalidValue;
+    if (epi == kGemmStore)
+        return p.bn == 64 ? launch_t<kGemmStore, 64>(ma, mb, p, grid, s) : launch_t<kGemmStore, 128>(ma, mb, p, grid, s);
+    return p.bn == 64 ? launch_t<kGemmAdd, 64>(ma, mb, p, grid, s) : launch_t<kGemmAdd, 128>(ma, mb, p, grid, s);
 }
 
 }  // namespace tts
@@ -322,7 +335,7 @@ extern "C" int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N
     if (!A || !B || !C || epi < kGemmStore || epi > kGemmSwiglu || splits < 1) return TTS_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15)
         return TTS_ERR_ARG;
-    if (!gemm_shape_ok(M, N, K, epi)) return TTS_ERR_ARG;
+    if (!gemm_shape_ok(M, N, K, epi, 128)) return TTS_ERR_ARG;
     GemmParams p{};
     p.M = M;
     p.N = N;

@@ -208,7 +208,7 @@ cudaError_t launch_step(const StepParams& p, int prec, int G, int grid, int smem
 
 // C = A . B^T on the tensor cores (gemm_tc.cu): A [M][K] and B [N][K] bf16,
 // K-major, fp32 accumulation.  Epilogues: store fp32 C[M][ldc]; add into fp32
-// C (residual stream, split-K partials); SwiGLU: B = [gate rows; up rows] of
+// C (residual stream: deterministic with one k-split, atomic with several); SwiGLU: B = [gate rows; up rows] of
 // a [2 n_half][K] matrix, out_bf16[M][ldc] = bf16(silu(gate) * up), N = n_half.
 enum GemmEpi { kGemmStore = 0, kGemmAdd = 1, kGemmSwiglu = 2 };
 struct GemmParams {
@@ -217,12 +217,26 @@ struct GemmParams {
     int ldc;
     int M, N, K;
     int n_half;
+    int bn;            // output columns per tile: 128 (0 = default) or 64 (more tiles for narrow N)
     int kb_per_split;  // filled in by launch_gemm_bf16
+    int atomic;        // filled in: split-K partials are added atomically
     int* err;          // error word (kErrTimeout on an expired wait), may be NULL
 };
-bool gemm_shape_ok(int M, int N, int K, int epi);
+bool gemm_shape_ok(int M, int N, int K, int epi, int bn);
 cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p, int epi, int splits,
                              cudaStream_t s);
+
+// Batched prefill glue (prefill.cu): P rows at positions pos0 .. pos0+P-1.
+cudaError_t launch_prefill_embed(const __nv_bfloat16* E, const int* codes, float* H, int P, int n_cb, int V,
+                                 int hidden, cudaStream_t s);
+cudaError_t launch_prefill_rmsnorm(const float* H, const __nv_bfloat16* gamma, __nv_bfloat16* out, int P,
+                                   int hidden, float eps, cudaStream_t s);
+cudaError_t launch_prefill_qk_rope_kv(const float* QKV, const __nv_bfloat16* qn, const __nv_bfloat16* kn,
+                                      const float2* rope, float* Q, __nv_bfloat16* kc, __nv_bfloat16* vc, int pos0,
+                                      int P, int n_q, int n_kv, int max_pos, float eps, cudaStream_t s);
+cudaError_t launch_prefill_attention(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
+                                     __nv_bfloat16* out, int pos0, int P, int n_q, int n_kv, int max_pos,
+                                     cudaStream_t s);
 
 // Per-row E4M3 weight quantisation.
 cudaError_t launch_quantize_weight(const __nv_bfloat16* W, int N, int K, uint8_t* W8, float* s,

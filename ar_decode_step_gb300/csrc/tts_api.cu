@@ -68,6 +68,11 @@ struct tts_ctx {
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     float last_ms = 0.f;
     int pos = 0;  // host shadow of st->pos
+
+    // batched prefill scratch (allocated on first use, kPrefillChunk rows)
+    float *pf_h = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
+    __nv_bfloat16 *pf_a = nullptr, *pf_attn = nullptr, *pf_m = nullptr;
+    bool batched_prefill = true;
 };
 
 namespace {
@@ -443,6 +448,9 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     {
         const char* mode = std::getenv("TTS_STEP_MODE");
         c->persistent = !(mode && std::strcmp(mode, "kernels") == 0);
+        // TTS_PREFILL=steps runs a prompt position by position through the decode step instead
+        const char* pf = std::getenv("TTS_PREFILL");
+        c->batched_prefill = !(pf && std::strcmp(pf, "steps") == 0);
     }
     // the persistent kernel keeps a normalised activation in registers while
     // its statistics arrive: longer hidden sizes take the graph of kernels
@@ -452,6 +460,68 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     TTS_TRY(capture(c, true, &c->step_exec));
     TTS_TRY(capture(c, false, &c->prefill_exec));
     TTS_CK(cudaStreamSynchronize(c->stream));
+    return TTS_OK;
+}
+
+constexpr int kPrefillChunk = 512;  // rows per batched pass (the prompt is split into chunks)
+
+// Whether tts_prefill runs the batched tensor-core path: BF16 weights (the
+// tensor-core GEMM takes bf16 operands), K and N multiples of the GEMM tiles.
+bool batched_prefill_ok(const tts_ctx* c) {
+    const tts_config& k = c->cfg;
+    const int G = k.n_q_heads / k.n_kv_heads;
+    return c->batched_prefill && k.precision == TTS_BF16 && k.head_dim == kHeadDim &&
+           gemm_shape_ok(1, c->qkv_rows, k.hidden, kGemmStore, 128) &&
+           gemm_shape_ok(1, k.hidden, c->attn_dim, kGemmAdd, 64) &&
+           gemm_shape_ok(1, k.inter, k.hidden, kGemmSwiglu, 128) && gemm_shape_ok(1, k.hidden, k.inter, kGemmAdd, 64) &&
+           (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+// P rows (codes already on the device at c->prompt) through every layer at
+// positions pos0 .. pos0+P-1: W16A16 tensor-core GEMMs, fp32 residual stream,
+// bf16 K/V written to the cache.  P <= kPrefillChunk.
+int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap = nullptr) {
+    const tts_config& k = c->cfg;
+    const int H = k.hidden, I = k.inter, A = c->attn_dim, QD = c->qkv_rows;
+    cudaStream_t s = c->stream;
+    if (!c->pf_h) {
+        const size_t R = kPrefillChunk;
+        TTS_TRY(dalloc(c, &c->pf_h, R * H));
+        TTS_TRY(dalloc(c, &c->pf_qkv, R * QD));
+        TTS_TRY(dalloc(c, &c->pf_q, R * A));
+        TTS_TRY(dalloc(c, &c->pf_a, R * H));
+        TTS_TRY(dalloc(c, &c->pf_attn, R * A));
+        TTS_TRY(dalloc(c, &c->pf_m, R * I));
+    }
+    int* err = &c->st->err;
+    TTS_CK(launch_prefill_embed(c->embed, d_codes, c->pf_h, P, k.n_codebooks, k.cb_vocab, H, s));
+    const size_t rows_bytes = sizeof(float) * (size_t)P * H;
+    if (snap) TTS_CK(cudaMemcpyAsync(snap, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
+    // the residual GEMMs (N = hidden) take 64-column tiles: twice the tiles of
+    // the 128-wide ones, one writer per element (deterministic, no split-K)
+    for (int l = 0; l < k.n_layers; ++l) {
+        const LayerW& w = c->L[l];
+        const size_t coff = (size_t)l * k.n_kv_heads * k.max_pos * kHeadDim;
+        TTS_CK(launch_prefill_rmsnorm(c->pf_h, w.ln_in, c->pf_a, P, H, k.rms_eps, s));
+        GemmParams g{};
+        g.M = P; g.err = err;
+        g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H;
+        TTS_CK(launch_gemm_bf16(c->pf_a, w.wqkv, g, kGemmStore, 1, s));
+        TTS_CK(launch_prefill_qk_rope_kv(c->pf_qkv, w.qn, w.kn, c->rope, c->pf_q, c->kc + coff, c->vc + coff, pos0,
+                                         P, k.n_q_heads, k.n_kv_heads, k.max_pos, k.rms_eps, s));
+        TTS_CK(launch_prefill_attention(c->pf_q, c->kc + coff, c->vc + coff, c->pf_attn, pos0, P, k.n_q_heads,
+                                        k.n_kv_heads, k.max_pos, s));
+        g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A; g.bn = 64;
+        TTS_CK(launch_gemm_bf16(c->pf_attn, w.wo, g, kGemmAdd, 1, s));
+        g.bn = 0;
+        TTS_CK(launch_prefill_rmsnorm(c->pf_h, w.ln_post, c->pf_a, P, H, k.rms_eps, s));
+        g.C = nullptr; g.out_bf16 = c->pf_m; g.ldc = I; g.N = I; g.n_half = I; g.K = H;
+        TTS_CK(launch_gemm_bf16(c->pf_a, w.wgu, g, kGemmSwiglu, 1, s));
+        g.out_bf16 = nullptr; g.C = c->pf_h; g.ldc = H; g.N = H; g.n_half = 0; g.K = I; g.bn = 64;
+        TTS_CK(launch_gemm_bf16(c->pf_m, w.wd, g, kGemmAdd, 1, s));
+        if (snap)
+            TTS_CK(cudaMemcpyAsync(snap + (size_t)(l + 1) * P * H, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
+    }
     return TTS_OK;
 }
 
@@ -552,6 +622,20 @@ int tts_prefill(tts_ctx* ctx, const int32_t* codes, int P) {
                            cudaMemcpyHostToDevice, ctx->stream));
     TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
     TTS_CK(cudaStreamSynchronize(ctx->stream));
+    if (batched_prefill_ok(ctx)) {
+        // the whole prompt as M = P tensor-core passes, kPrefillChunk rows at a time
+        DevState s = *ctx->h_out;
+        for (int r = 0; r < P; r += kPrefillChunk)
+            TTS_TRY(prefill_chunk(ctx, ctx->prompt + (size_t)r * k.n_codebooks, s.pos + r,
+                                  std::min(kPrefillChunk, P - r)));
+        TTS_CK(cudaStreamSynchronize(ctx->stream));
+        int rc = pull_state(ctx);  // reports a GEMM wait that expired (device error word)
+        if (rc != TTS_OK) return rc;
+        s.pos += P;
+        s.prefill_row = 0;
+        for (int i = 0; i < kMaxCodebooks; ++i) s.codes[i] = k.cb_vocab - 2;  // next input: all-BOS frame
+        return push_state(ctx, s);
+    }
     DevState s = *ctx->h_out;
     s.prefill_row = 0;
     TTS_TRY(push_state(ctx, s));
@@ -742,6 +826,38 @@ int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes
     const int rc = pull_state(ctx);
     if (rc == TTS_OK && codes_out) std::memcpy(codes_out, ctx->h_out->codes, sizeof(int32_t) * k.n_codebooks);
     return rc;
+}
+
+int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* host_h, long long capacity) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (!codes || P < 1 || P > kPrefillChunk || !host_h) return TTS_ERR_ARG;
+    if (!batched_prefill_ok(ctx)) return TTS_ERR_UNSUPPORTED;
+    const size_t n = (size_t)(k.n_layers + 1) * P * k.hidden;
+    if (capacity < (long long)n) return TTS_ERR_ARG;
+    if ((long long)ctx->pos + P > k.max_pos) return TTS_ERR_FULL;
+    for (long long i = 0; i < (long long)P * k.n_codebooks; ++i)
+        if (codes[i] < 0 || codes[i] >= k.cb_vocab) return TTS_ERR_CODE;
+    TTS_CK(cudaMemcpyAsync(ctx->prompt, codes, sizeof(int32_t) * (size_t)P * k.n_codebooks,
+                           cudaMemcpyHostToDevice, ctx->stream));
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    DevState s = *ctx->h_out;
+    float* snap = nullptr;
+    TTS_CK(cudaMalloc(&snap, n * sizeof(float)));
+    int rc = prefill_chunk(ctx, ctx->prompt, s.pos, P, snap);
+    cudaError_t e = cudaSuccess;
+    if (rc == TTS_OK) e = cudaMemcpyAsync(host_h, snap, n * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    cudaFree(snap);
+    if (rc != TTS_OK) return rc;
+    if (e != cudaSuccess) return report(e, "tts_debug_prefill_states");
+    rc = pull_state(ctx);
+    if (rc != TTS_OK) return rc;
+    s.pos += P;
+    s.prefill_row = 0;
+    for (int i = 0; i < kMaxCodebooks; ++i) s.codes[i] = k.cb_vocab - 2;
+    return push_state(ctx, s);
 }
 
 int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream) {

@@ -208,6 +208,15 @@ int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, 
 int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out, float* host_h,
                            int capacity);
 
+/* Test hook (not part of the product path): tts_prefill of P <= 512
+ * positions on the batched path that also records the fp32 residual stream
+ * of every prompt row after the embedding and after every layer into
+ * `host_h` ([n_layers + 1][P][hidden], caller-owned, `capacity` floats), so a
+ * check can start the CPU oracle's layer l from the GPU's input to it.
+ * TTS_ERR_UNSUPPORTED when the context does not prefill on the batched path
+ * (FP8 weights); otherwise as tts_prefill.  Synchronises. */
+int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* host_h, long long capacity);
+
 /* Stand-alone op: C = A . B^T on the tensor cores (tcgen05 MMA, TMEM
  * accumulators, TMA-staged operands), the GEMM of the batched prompt prefill
  * ("Higgs Audio v3 TTS-4B on FlashRT", Performance "BF16 W16A16" and section

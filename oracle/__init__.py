@@ -83,7 +83,7 @@ def lib():
                 "or_prefill": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
                                      ctypes.POINTER(_State), vp, i32, i32]),
                 "or_layer": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
-                                   ctypes.POINTER(_State), i32, i32, vp]),
+                                   ctypes.POINTER(_State), i32, i32, vp, i32]),
                 "or_head": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
                                   ctypes.POINTER(_State), vp, vp, vp, vp]),
             }
@@ -277,12 +277,13 @@ class Oracle:
         """The step's input residual stream for these codes."""
         return embed(self.w.embed, codes_in)
 
-    def layer(self, layer: int, pos: int, h) -> np.ndarray:
+    def layer(self, layer: int, pos: int, h, a16: bool = False) -> np.ndarray:
         """Layer `layer` at position pos applied to the residual stream h
-        (returns the layer's output; writes that layer's K/V at pos)."""
+        (returns the layer's output; writes that layer's K/V at pos).  a16 as
+        in prefill."""
         x = np.ascontiguousarray(h, np.float64).copy()
         rc = lib().or_layer(ctypes.byref(self.cdims), ctypes.byref(self.cw), ctypes.byref(self.st),
-                            int(layer), int(pos), _p(x))
+                            int(layer), int(pos), _p(x), int(a16))
         if rc:
             raise ValueError(f"or_layer failed ({rc})")
         return x

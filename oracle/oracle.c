@@ -398,10 +398,10 @@ static void head_codes(const or_dims* d, const or_weights* w, const or_state* st
     free(lg);
 }
 
-int or_layer(const or_dims* d, const or_weights* w, or_state* st, int layer, int pos, double* h) {
+int or_layer(const or_dims* d, const or_weights* w, or_state* st, int layer, int pos, double* h, int a16) {
     if (check_dims(d) || !w || !st || !h || layer < 0 || layer >= d->n_layers || pos < 0 || pos >= d->max_pos)
         return -1;
-    stack_layers(d, w, st, pos, h, 0, layer, layer + 1);
+    stack_layers(d, w, st, pos, h, a16, layer, layer + 1);
     return 0;
 }
 

@@ -96,8 +96,9 @@ int or_decode_step(const or_dims* d, const or_weights* w, or_state* st,
 
 /* One layer `layer` at position pos (layer-level checks): h holds the
  * layer's input residual stream on entry and its output on exit; writes that
- * layer's K/V at pos.  Changes neither pos nor t.  Returns 0 or -1. */
-int or_layer(const or_dims* d, const or_weights* w, or_state* st, int layer, int pos, double* h);
+ * layer's K/V at pos.  a16 as in or_prefill.  Changes neither pos nor t.
+ * Returns 0 or -1. */
+int or_layer(const or_dims* d, const or_weights* w, or_state* st, int layer, int pos, double* h, int a16);
 
 /* The head of the step on a given final residual stream h: final RMSNorm,
  * codebook logits, argmax under the delay mask at frame st->t (codes_out,

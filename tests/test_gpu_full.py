@@ -25,7 +25,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import check_frame, cosine, to_binding_dims, upload_kv
+from helpers import adopt_gpu_cache, check_frame, check_kv_rows, cosine, to_binding_dims, upload_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -65,8 +65,12 @@ def test_full36_bf16_prompt13(ads, full_weights):
     orc = oracle.Oracle(w, max_pos, precision=0)
     prompt = synth.delayed_prompt_codes(13)
     dec.prefill(prompt)
-    orc.prefill(prompt)
+    orc.prefill(prompt, a16=True)  # the batched prefill is W16A16
     assert dec.state()[0] == orc.pos == 13
+    gk, gv = dec.get_kv(0, 13)
+    check_kv_rows(gk, orc.k[:, :, :13], "prefill K")
+    check_kv_rows(gv, orc.v[:, :, :13], "prefill V")
+    adopt_gpu_cache(dec, orc, 13)  # decode frames compared from the same cache
     bos = np.full(8, 1024, np.int32)
     stats = teacher_forced(dec, orc, [bos, synth.random_codes(1, seed=2, stream=7)[0]], False, "bf16-36L")
     print("bf16 36L", stats)

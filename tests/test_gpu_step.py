@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import check_frame, reduced_dims, to_binding_dims, upload_kv
+from helpers import adopt_gpu_cache, check_frame, check_kv_rows, reduced_dims, to_binding_dims, upload_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -118,13 +118,13 @@ def test_prefill_matches_oracle(ads):
     prompt = synth.delayed_prompt_codes(9, stream=1)
     dec.prefill(prompt[:4])
     dec.prefill(prompt[4:])
-    orc.prefill(prompt)
+    orc.prefill(prompt, a16=True)  # the batched prefill is W16A16
     assert dec.state()[0] == orc.pos == 9
     gk, gv = dec.get_kv(0, 9)
-    f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    assert np.allclose(f(gk), f(orc.k[:, :, :9]), rtol=2 ** -6, atol=1e-3)
-    assert np.allclose(f(gv), f(orc.v[:, :, :9]), rtol=2 ** -6, atol=1e-3)
-    # the frame after a prefill is the all-BOS frame at t = 0
+    check_kv_rows(gk, orc.k[:, :, :9], "prefill K")
+    check_kv_rows(gv, orc.v[:, :, :9], "prefill V")
+    # the frame after a prefill is the all-BOS frame at t = 0 (from the GPU's cache)
+    adopt_gpu_cache(dec, orc, 9)
     g = dec.decode_step()
     o, ol, og = orc.decode_step(np.full(8, 1024, np.int32))
     check_frame(g, dec.get_logits(), o, ol, og, False, 0, -1, "after prefill")
