@@ -55,7 +55,10 @@ __device__ __forceinline__ void dot_bf16(const uint4 w, const float4 a, const fl
     ffma2(e, o, bf16lo(w.w), bf16hi(w.w), b.z, b.w);
 }
 
-// Two E4M3 weights (low 16 bits of w) times two f16 activations, f32 accumulate.
+// Two E4M3 weights (low 16 bits of w16) times two activations (exact E4M3
+// values held in fp32), f32 accumulate: the weights go through f16 and the
+// products are taken by the mixed-precision f16 x f16 + f32 FMA (the
+// activations are exact in f16).
 __device__ __forceinline__ float fma2_e4m3_f16(uint32_t w16, uint32_t x2, float acc) {
     const __half2_raw wh = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w16 & 0xffffu), __NV_E4M3);
     const uint32_t w2 = (uint32_t)wh.x | ((uint32_t)wh.y << 16);
@@ -314,8 +317,13 @@ __device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* ga
 // (bf16 weights) or f16 (FP8 weights).
 template <bool FP8>
 struct XSeg {
-    using V = typename std::conditional<FP8, uint4, float4>::type;
-    V a[kMaxLaneChunks], b[kMaxLaneChunks];
+    static constexpr int kChunks = lane_chunk_limit(0);
+    float4 a[kChunks], b[kChunks];  // elements 0-3 and 4-7 of each 8-weight chunk
+};
+template <>
+struct XSeg<true> {
+    static constexpr int kChunks = lane_chunk_limit(1);
+    uint4 a[kChunks], b[kChunks];   // f16 activations (exact E4M3 values) 0-7 and 8-15 of each chunk
 };
 
 // This warp's segment of projection j.
@@ -327,16 +335,21 @@ __device__ __forceinline__ void proj_segment(const Proj& j, int warp, int& rslot
     c1 = (int)((long long)(sg + 1) * CPR / WPR);
 }
 
-// Segment from the shared-memory planes written by stage_x.
+// Segment from the shared-memory planes written by stage_x: fp32 planes for
+// bf16 weights, f16 planes (exact E4M3 values) for FP8.
 template <bool FP8>
 __device__ __forceinline__ void load_xseg_smem(const unsigned char* xs, int CPR, int c0, int c1, XSeg<FP8>& x) {
-    using V = typename XSeg<FP8>::V;
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < kMaxLaneChunks; ++i) {
+    for (int i = 0; i < XSeg<FP8>::kChunks; ++i) {
         const int c = c0 + lane + 32 * i;
-        x.a[i] = c < c1 ? reinterpret_cast<const V*>(xs)[c] : V{};
-        x.b[i] = c < c1 ? reinterpret_cast<const V*>(xs)[CPR + c] : V{};
+        if constexpr (!FP8) {
+            x.a[i] = c < c1 ? reinterpret_cast<const float4*>(xs)[c] : float4{};
+            x.b[i] = c < c1 ? reinterpret_cast<const float4*>(xs)[CPR + c] : float4{};
+        } else {
+            x.a[i] = c < c1 ? reinterpret_cast<const uint4*>(xs)[c] : uint4{};
+            x.b[i] = c < c1 ? reinterpret_cast<const uint4*>(xs)[CPR + c] : uint4{};
+        }
     }
 }
 
@@ -518,7 +531,7 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
                 const uint4* wrow = reinterpret_cast<const uint4*>(sbuf + r * rowb);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < kMaxLaneChunks; ++i) {
+                for (int i = 0; i < XSeg<FP8>::kChunks; ++i) {
                     const int c = c0 + lane + 32 * i;
                     if (c < c1) {
                         const uint4 w = wrow[c];

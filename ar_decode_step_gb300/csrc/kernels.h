@@ -23,6 +23,10 @@ enum Epi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiLogits = 3 };
 #endif
 constexpr int kConsumerWarps = TTS_CONSUMER_WARPS;
 constexpr int kMaxLaneChunks = TTS_MAX_LANE_CHUNKS;
+// FP8 chunks carry 16 weights (twice the FMAs per chunk): half as many per
+// lane keep the FP8 stage loop's registers (activations as f16 pairs plus the
+// conversion temporaries) within the budget.
+constexpr int lane_chunk_limit(int prec) { return prec == 1 ? kMaxLaneChunks / 2 : kMaxLaneChunks; }
 constexpr int kStageTarget = 40 * 1024;  // bytes per ring stage, at most (unless one row is longer)
 constexpr int kMaxRmsK = 4096;            // persistent step: longest normalised activation (hidden)
 constexpr int kMaxPlainK = 12288;         // longest plain activation (attention output, MLP activation)
@@ -42,13 +46,14 @@ inline __host__ __device__ StageGeom stage_geom(int prec, int epi, int K) {
     const long long rowb = (long long)cpr * 16;
     auto lane_chunks = [&](int w) { return ((cpr + w - 1) / w + 31) / 32; };
     int wpr = 1;
-    while (wpr < kConsumerWarps && lane_chunks(wpr) > kMaxLaneChunks) wpr *= 2;
+    const int limit = lane_chunk_limit(prec);
+    while (wpr < kConsumerWarps && lane_chunks(wpr) > limit) wpr *= 2;
     while (wpr < kConsumerWarps && (long long)(kConsumerWarps / wpr) * rowb > kStageTarget) wpr *= 2;
     const int slots = kConsumerWarps / wpr;
     int rs = slots;
     while (rs < 4 * slots && 2LL * rs * rowb <= kStageTarget) rs *= 2;  // up to four rows per warp and stage
     if (epi == kEpiSwiglu && rs < 2) rs = 2;
-    return StageGeom{rs, wpr, K % 256 == 0 && cpr >= wpr && lane_chunks(wpr) <= kMaxLaneChunks};
+    return StageGeom{rs, wpr, K % 256 == 0 && cpr >= wpr && lane_chunks(wpr) <= limit};
 }
 
 // y = epilogue(W . prologue(x)) for one activation vector (M = 1).

@@ -34,7 +34,7 @@ namespace {
 using namespace core;
 
 constexpr int kMaxHRows = 256;     // rows of h one CTA owns, at most
-constexpr int kAttnMinChunk = 128;  // positions per attention split, at least (no merge below)
+constexpr int kAttnMinChunk = 32;   // positions per attention split, at least (no merge below)
 
 // Grid barrier among the consumer warps of all CTAs.  `gbar` counts arrivals
 // over the launch (zeroed before it); barrier k (1-based) waits for
