@@ -92,13 +92,23 @@ __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const floa
 }
 
 // Causal GQA attention over the cache for rows [rb*16, rb*16+16) of the
-// prompt and the G query heads of kv head g: 64 (row, head) pairs per CTA, 8
-// per warp.  Keys go through shared memory 64 at a time (fp32, K rows padded
-// against bank conflicts); each lane scores two keys of a pair, then
-// accumulates 4 output dims with the online softmax (fp32).
+// prompt and the G query heads of kv head g: G*16 (row, head) pairs per CTA,
+// 2G per warp (one head, consecutive rows).  Keys go through shared memory 64
+// at a time (fp32, K rows padded against bank conflicts).  Register tiling:
+// a lane scores its two keys against every pair of its warp (each K value
+// loaded once for all pairs, the queries broadcast); the probabilities go
+// through a per-warp shared tile, and for the output each lane keeps 4 dims
+// of every pair (each V value loaded once for all pairs).  Online softmax in
+// fp32.
 constexpr int kAttRows = 16;
 constexpr int kAttKeys = 64;
 constexpr int kKPad = kHeadDim + 4;
+
+template <int G>
+constexpr int attention_rows_smem() {
+    return (G * kAttRows * kHeadDim + kAttKeys * kKPad + kAttKeys * kHeadDim + G * kAttRows * kAttKeys) *
+           (int)sizeof(float);
+}
 
 template <int G>
 __global__ void __launch_bounds__(kRowThreads) attention_rows_kernel(const float* Q, const __nv_bfloat16* kc,
@@ -106,18 +116,19 @@ __global__ void __launch_bounds__(kRowThreads) attention_rows_kernel(const float
                                                                      __nv_bfloat16* out, int pos0, int P, int n_q,
                                                                      int max_pos) {
     extern __shared__ __align__(16) float sm[];
-    float* Qs = sm;                                    // [G * 16][128]
-    float* Ks = Qs + G * kAttRows * kHeadDim;          // [64][132]
-    float* Vs = Ks + kAttKeys * kKPad;                 // [64][128]
     constexpr int kPairs = G * kAttRows;
     constexpr int kPerWarp = kPairs / (kRowThreads / 32);
+    float* Qs = sm;                                    // [pairs][128]
+    float* Ks = Qs + kPairs * kHeadDim;                // [64][132]
+    float* Vs = Ks + kAttKeys * kKPad;                 // [64][128]
+    float* Ps = Vs + kAttKeys * kHeadDim;              // [pairs][64] probabilities
     const int rb = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = rb * kAttRows;
     const int nrows = min(kAttRows, P - row0);
     const size_t cache0 = (size_t)g * max_pos * kHeadDim;
 
-    // pair = head_local * 16 + row_local
+    // pair = head_local * 16 + row_local; warp w owns pairs [w * kPerWarp, (w+1) * kPerWarp)
     for (int i = threadIdx.x; i < kPairs * kHeadDim / 4; i += kRowThreads) {
         const int pair = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
         const int hl = pair / kAttRows, rl = pair % kAttRows;
@@ -125,7 +136,15 @@ __global__ void __launch_bounds__(kRowThreads) attention_rows_kernel(const float
         if (rl < nrows) v = reinterpret_cast<const float4*>(Q + ((size_t)(row0 + rl) * n_q + g * G + hl) * kHeadDim)[d4];
         reinterpret_cast<float4*>(Qs)[i] = v;
     }
-
+    const int pair0 = warp * kPerWarp;
+    int qpos[kPerWarp];
+    int qpos_max = -1;
+#pragma unroll
+    for (int i = 0; i < kPerWarp; ++i) {
+        const int rl = (pair0 + i) % kAttRows;
+        qpos[i] = rl < nrows ? pos0 + row0 + rl : -1;  // -1: no such row (never attends)
+        qpos_max = max(qpos_max, qpos[i]);
+    }
     float m[kPerWarp], l[kPerWarp], o[kPerWarp][4];
 #pragma unroll
     for (int i = 0; i < kPerWarp; ++i) {
@@ -133,6 +152,7 @@ __global__ void __launch_bounds__(kRowThreads) attention_rows_kernel(const float
         l[i] = 0.f;
         o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
+    float* pw = Ps + pair0 * kAttKeys;
     const int kmax = pos0 + row0 + nrows - 1;  // last key any row of this block sees
     for (int k0 = 0; k0 <= kmax; k0 += kAttKeys) {
         __syncthreads();  // previous tile consumed (and Qs written, first time)
@@ -150,48 +170,62 @@ __global__ void __launch_bounds__(kRowThreads) attention_rows_kernel(const float
             *reinterpret_cast<float4*>(Vs + kr * kHeadDim + 4 * d4) = vv;
         }
         __syncthreads();
+        if (k0 > qpos_max) continue;  // warp-uniform: no row of this warp reaches the tile
+
+        // scores of keys k0 + lane and k0 + lane + 32 against every pair of the warp
+        float s0[kPerWarp], s1[kPerWarp];
+#pragma unroll
+        for (int i = 0; i < kPerWarp; ++i) s0[i] = s1[i] = 0.f;
+        const float* ka = Ks + lane * kKPad;
+        const float* kb = Ks + (lane + 32) * kKPad;
+        const float* qw = Qs + pair0 * kHeadDim;
+#pragma unroll 2
+        for (int d = 0; d < kHeadDim; d += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(ka + d);
+            const float4 b = *reinterpret_cast<const float4*>(kb + d);
+#pragma unroll
+            for (int i = 0; i < kPerWarp; ++i) {
+                const float4 qq = *reinterpret_cast<const float4*>(qw + i * kHeadDim + d);
+                s0[i] = fmaf(qq.x, a.x, fmaf(qq.y, a.y, fmaf(qq.z, a.z, fmaf(qq.w, a.w, s0[i]))));
+                s1[i] = fmaf(qq.x, b.x, fmaf(qq.y, b.y, fmaf(qq.z, b.z, fmaf(qq.w, b.w, s1[i]))));
+            }
+        }
+        // online softmax per pair; probabilities to the warp's shared tile
 #pragma unroll
         for (int i = 0; i < kPerWarp; ++i) {
-            const int pair = warp * kPerWarp + i;
-            const int rl = pair % kAttRows;
-            if (rl >= nrows) continue;
-            const int qpos = pos0 + row0 + rl;
-            if (k0 > qpos) continue;
-            const float* q = Qs + pair * kHeadDim;
-            const float* ka = Ks + lane * kKPad;
-            const float* kb = Ks + (lane + 32) * kKPad;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-            for (int d = 0; d < kHeadDim; d += 4) {
-                const float4 qq = *reinterpret_cast<const float4*>(q + d);
-                const float4 a = *reinterpret_cast<const float4*>(ka + d);
-                const float4 b = *reinterpret_cast<const float4*>(kb + d);
-                s0 = fmaf(qq.x, a.x, fmaf(qq.y, a.y, fmaf(qq.z, a.z, fmaf(qq.w, a.w, s0))));
-                s1 = fmaf(qq.x, b.x, fmaf(qq.y, b.y, fmaf(qq.z, b.z, fmaf(qq.w, b.w, s1))));
-            }
-            if (k0 + lane > qpos) s0 = -INFINITY;
-            if (k0 + lane + 32 > qpos) s1 = -INFINITY;
-            const float mn = fmaxf(m[i], warp_max(fmaxf(s0, s1)));
-            const float corr = __expf(m[i] - mn);
-            const float p0 = __expf(s0 - mn), p1 = __expf(s1 - mn);
+            if (k0 + lane > qpos[i]) s0[i] = -INFINITY;
+            if (k0 + lane + 32 > qpos[i]) s1[i] = -INFINITY;
+            const float mx = warp_max(fmaxf(s0[i], s1[i]));
+            const float mn = fmaxf(m[i], mx);
+            // a pair with no key in this tile (mn = -inf) keeps its state
+            const float corr = mn == -INFINITY ? 1.f : __expf(m[i] - mn);
+            const float p0 = mn == -INFINITY ? 0.f : __expf(s0[i] - mn);
+            const float p1 = mn == -INFINITY ? 0.f : __expf(s1[i] - mn);
             l[i] = l[i] * corr + warp_sum(p0 + p1);
             m[i] = mn;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) o[i][jj] *= corr;
-            const int nk = min(kAttKeys, qpos - k0 + 1);
-            for (int kk = 0; kk < nk; ++kk) {
-                const float pk = __shfl_sync(0xffffffffu, kk < 32 ? p0 : p1, kk & 31);
-                const float4 vv = *reinterpret_cast<const float4*>(Vs + kk * kHeadDim + 4 * lane);
+            pw[i * kAttKeys + lane] = p0;
+            pw[i * kAttKeys + lane + 32] = p1;
+        }
+        __syncwarp();
+        const int nk = min(kAttKeys, qpos_max - k0 + 1);
+        for (int kk = 0; kk < nk; ++kk) {
+            const float4 vv = *reinterpret_cast<const float4*>(Vs + kk * kHeadDim + 4 * lane);
+#pragma unroll
+            for (int i = 0; i < kPerWarp; ++i) {
+                const float pk = pw[i * kAttKeys + kk];
                 o[i][0] = fmaf(pk, vv.x, o[i][0]);
                 o[i][1] = fmaf(pk, vv.y, o[i][1]);
                 o[i][2] = fmaf(pk, vv.z, o[i][2]);
                 o[i][3] = fmaf(pk, vv.w, o[i][3]);
             }
         }
+        __syncwarp();
     }
 #pragma unroll
     for (int i = 0; i < kPerWarp; ++i) {
-        const int pair = warp * kPerWarp + i;
+        const int pair = pair0 + i;
         const int hl = pair / kAttRows, rl = pair % kAttRows;
         if (rl >= nrows) continue;
         const float inv = 1.0f / l[i];
@@ -207,7 +241,7 @@ template <int G>
 cudaError_t launch_attention_rows_t(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                                     __nv_bfloat16* out, int pos0, int P, int n_q, int n_kv, int max_pos,
                                     cudaStream_t s) {
-    constexpr int smem = (G * kAttRows * kHeadDim + kAttKeys * kKPad + kAttKeys * kHeadDim) * (int)sizeof(float);
+    constexpr int smem = attention_rows_smem<G>();
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(attention_rows_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
