@@ -118,7 +118,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __shared__ int s_never;  // abort flag of the epilogue wait: only the time limit ends it
     constexpr uint32_t kBTileBytes = MMA_N * kBK * 2;
     constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
-    constexpr uint32_t kTmemCols = MMA_N;  // fp32 accumulator columns (power of two >= 32)
+    // fp32 accumulator columns: the allocation is a power of two >= 32
+    constexpr uint32_t kTmemCols = MMA_N <= 32 ? 32 : MMA_N <= 64 ? 64 : MMA_N <= 128 ? 128 : 256;
     // stage tiles 1024-byte aligned (swizzle atoms)
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -298,8 +299,27 @@ cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParam
 }  // namespace
 
 bool gemm_shape_ok(int M, int N, int K, int epi, int bn) {
-    return M > 0 && N > 0 && K > 0 && K % kBK == 0 && (bn == 64 || bn == 128) && N % bn == 0 &&
-           (epi != kGemmSwiglu || bn == 128);
+    const bool bn_ok = bn == 64 || bn == 80 || bn == 128 || bn == 192;
+    return M > 0 && N > 0 && K > 0 && K % kBK == 0 && bn_ok && N % bn == 0 && (epi != kGemmSwiglu || bn == 128);
+}
+
+int gemm_pick_bn(int M, int N, int epi, int num_sms) {
+    // the widest tile whose grid still fits one wave of CTAs (fewest idle SMs)
+    if (epi == kGemmSwiglu) return 128;
+    const int mt = (M + kBM - 1) / kBM;
+    int best = 0;
+    double best_eff = -1.0;
+    for (int bn : {192, 128, 80, 64}) {
+        if (N % bn) continue;
+        const long long ctas = (long long)(N / bn) * mt;
+        const long long waves = (ctas + num_sms - 1) / num_sms;
+        const double eff = (double)ctas / (double)(waves * num_sms);  // busy fraction of the SM-waves
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = bn;
+        }
+    }
+    return best ? best : 128;
 }
 
 cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p_in, int epi, int splits,
@@ -321,9 +341,16 @@ cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p_i
         return launch_t<kGemmSwiglu, 256>(ma, mb, p, grid, s);
     }
     if (!make_map(&mb, B, p.N, p.K, p.bn)) return cudaErrorInvalidValue;
-    if (epi == kGemmStore)
-        return p.bn == 64 ? launch_t<kGemmStore, 64>(ma, mb, p, grid, s) : launch_t<kGemmStore, 128>(ma, mb, p, grid, s);
-    return p.bn == 64 ? launch_t<kGemmAdd, 64>(ma, mb, p, grid, s) : launch_t<kGemmAdd, 128>(ma, mb, p, grid, s);
+#define TTS_GEMM_BN(EP)                                                      \
+    switch (p.bn) {                                                          \
+        case 64: return launch_t<EP, 64>(ma, mb, p, grid, s);                \
+        case 80: return launch_t<EP, 80>(ma, mb, p, grid, s);                \
+        case 192: return launch_t<EP, 192>(ma, mb, p, grid, s);              \
+        default: return launch_t<EP, 128>(ma, mb, p, grid, s);               \
+    }
+    if (epi == kGemmStore) TTS_GEMM_BN(kGemmStore)
+    TTS_GEMM_BN(kGemmAdd)
+#undef TTS_GEMM_BN
 }
 
 }  // namespace tts
@@ -335,8 +362,13 @@ extern "C" int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N
     if (!A || !B || !C || epi < kGemmStore || epi > kGemmSwiglu || splits < 1) return TTS_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15)
         return TTS_ERR_ARG;
-    if (!gemm_shape_ok(M, N, K, epi, 128)) return TTS_ERR_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TTS_ERR_CUDA;
+    const int bn = gemm_pick_bn(M, N, epi, sms);
+    if (!gemm_shape_ok(M, N, K, epi, bn)) return TTS_ERR_ARG;
     GemmParams p{};
+    p.bn = bn;
     p.M = M;
     p.N = N;
     p.K = K;

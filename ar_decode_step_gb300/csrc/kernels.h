@@ -222,12 +222,13 @@ struct GemmParams {
     int ldc;
     int M, N, K;
     int n_half;
-    int bn;            // output columns per tile: 128 (0 = default) or 64 (more tiles for narrow N)
+    int bn;            // output columns per tile: 64, 80, 128 (0 = default) or 192; SwiGLU: 128
     int kb_per_split;  // filled in by launch_gemm_bf16
     int atomic;        // filled in: split-K partials are added atomically
     int* err;          // error word (kErrTimeout on an expired wait), may be NULL
 };
 bool gemm_shape_ok(int M, int N, int K, int epi, int bn);
+int gemm_pick_bn(int M, int N, int epi, int num_sms);  // tile width that fills the SMs best
 cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p, int epi, int splits,
                              cudaStream_t s);
 

@@ -471,7 +471,7 @@ bool batched_prefill_ok(const tts_ctx* c) {
     const tts_config& k = c->cfg;
     const int G = k.n_q_heads / k.n_kv_heads;
     return c->batched_prefill && k.precision == TTS_BF16 && k.head_dim == kHeadDim &&
-           gemm_shape_ok(1, c->qkv_rows, k.hidden, kGemmStore, 128) &&
+           gemm_shape_ok(1, c->qkv_rows, k.hidden, kGemmStore, 64) &&
            gemm_shape_ok(1, k.hidden, c->attn_dim, kGemmAdd, 64) &&
            gemm_shape_ok(1, k.inter, k.hidden, kGemmSwiglu, 128) && gemm_shape_ok(1, k.hidden, k.inter, kGemmAdd, 64) &&
            (G == 1 || G == 2 || G == 4 || G == 8);
@@ -497,27 +497,28 @@ int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap =
     TTS_CK(launch_prefill_embed(c->embed, d_codes, c->pf_h, P, k.n_codebooks, k.cb_vocab, H, s));
     const size_t rows_bytes = sizeof(float) * (size_t)P * H;
     if (snap) TTS_CK(cudaMemcpyAsync(snap, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
-    // the residual GEMMs (N = hidden) take 64-column tiles: twice the tiles of
-    // the 128-wide ones, one writer per element (deterministic, no split-K)
+    // tile widths chosen per GEMM so that the grid fills the SMs in whole
+    // waves; the residual GEMMs keep one writer per element (deterministic, no split-K)
     for (int l = 0; l < k.n_layers; ++l) {
         const LayerW& w = c->L[l];
         const size_t coff = (size_t)l * k.n_kv_heads * k.max_pos * kHeadDim;
         TTS_CK(launch_prefill_rmsnorm(c->pf_h, w.ln_in, c->pf_a, P, H, k.rms_eps, s));
         GemmParams g{};
         g.M = P; g.err = err;
-        g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H;
+        g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H; g.bn = gemm_pick_bn(P, QD, kGemmStore, c->num_sms);
         TTS_CK(launch_gemm_bf16(c->pf_a, w.wqkv, g, kGemmStore, 1, s));
         TTS_CK(launch_prefill_qk_rope_kv(c->pf_qkv, w.qn, w.kn, c->rope, c->pf_q, c->kc + coff, c->vc + coff, pos0,
                                          P, k.n_q_heads, k.n_kv_heads, k.max_pos, k.rms_eps, s));
         TTS_CK(launch_prefill_attention(c->pf_q, c->kc + coff, c->vc + coff, c->pf_attn, pos0, P, k.n_q_heads,
                                         k.n_kv_heads, k.max_pos, s));
-        g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A; g.bn = 64;
+        g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A; g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
         TTS_CK(launch_gemm_bf16(c->pf_attn, w.wo, g, kGemmAdd, 1, s));
         g.bn = 0;
         TTS_CK(launch_prefill_rmsnorm(c->pf_h, w.ln_post, c->pf_a, P, H, k.rms_eps, s));
         g.C = nullptr; g.out_bf16 = c->pf_m; g.ldc = I; g.N = I; g.n_half = I; g.K = H;
         TTS_CK(launch_gemm_bf16(c->pf_a, w.wgu, g, kGemmSwiglu, 1, s));
-        g.out_bf16 = nullptr; g.C = c->pf_h; g.ldc = H; g.N = H; g.n_half = 0; g.K = I; g.bn = 64;
+        g.out_bf16 = nullptr; g.C = c->pf_h; g.ldc = H; g.N = H; g.n_half = 0; g.K = I;
+        g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
         TTS_CK(launch_gemm_bf16(c->pf_m, w.wd, g, kGemmAdd, 1, s));
         if (snap)
             TTS_CK(cudaMemcpyAsync(snap + (size_t)(l + 1) * P * H, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));

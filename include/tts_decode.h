@@ -228,7 +228,9 @@ int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* h
  *          splits > 1 the K range is split over that many CTAs per tile).
  *   epi 2: SwiGLU: B = [gate rows; up rows], a [2N][K] matrix; C = device
  *          bf16 [M][N] = bf16(silu(A . gate^T) * (A . up^T)).
- * fp32 accumulation; K % 64 == 0, N % 128 == 0, any M >= 1.  Enqueued on
+ * fp32 accumulation; K % 64 == 0, N a multiple of 64 or 80 (epi 2: of
+ * 128), any M >= 1; the tile width (64, 80, 128 or 192 columns) is chosen to
+ * fill the SMs.  Enqueued on
  * `stream` (NULL: the default stream); does not synchronise.  Returns
  * TTS_ERR_ARG for bad sizes, NULL or misaligned pointers. */
 int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, int epi, int splits, void* stream);

@@ -2,7 +2,7 @@
 oracle's linear layer (fp64 sums of the same bf16 operands): plain store,
 additive epilogue with split-K, and the fused gate/up + SwiGLU epilogue, on
 shapes with ragged M (rows past M are masked), several N tiles and several
-k-blocks."""
+k-blocks, covering the 64-, 80-, 128- and 192-column tile widths."""
 import numpy as np
 import pytest
 
@@ -36,7 +36,8 @@ def ref_rows(Wb, Ab):
     return np.stack([oracle.linear_bf16(Wb, f64(Ab[i])) for i in range(Ab.shape[0])])
 
 
-@pytest.mark.parametrize("M,N,K", [(37, 128, 64), (200, 256, 512), (300, 384, 2560)])
+@pytest.mark.parametrize("M,N,K", [(37, 128, 64), (200, 256, 512), (300, 384, 2560), (260, 640, 512),
+                                   (512, 2560, 256)])
 def test_gemm_store(env, M, N, K):
     ads, torch = env
     Ab = synth.normal_bf16(2, 101, (M, K))
