@@ -68,6 +68,14 @@ def step_bytes(d, precision: int, ctx_len: int) -> float:
     return d.n_layers * (per_layer + kv_read + kv_write) + head + embed
 
 
+def read_bf16_peak() -> float:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 def source_digest() -> str:
     """Hash of the step kernel's sources: a stored ncu traffic figure is only
     used while the kernel it was taken from is unchanged."""
@@ -362,6 +370,37 @@ def run_gpu(args, wl_name, wl):
     te1 = time.perf_counter()
     e2e_fps = world * n_e2e / (te1 - te0)
 
+    # batched prompt prefill (tensor-core path) at P = 512, same weights: the
+    # median of timed prefills after warm-up, with CUDA events
+    prefill_512 = None
+    if wl["precision"] == 0 and not args.no_prefill:
+        Pp = 512
+        pdec = ads.Decoder(ads.Dims(**{f: getattr(d, f) for f in ("n_layers", "hidden", "n_q", "n_kv", "head_dim",
+                                                                   "inter", "n_cb", "cb_vocab")}),
+                           dw, Pp + 8, stream=torch.cuda.current_stream().cuda_stream)
+        pprompt = synth.delayed_prompt_codes(Pp)
+        pts = []
+        for i in range(3 + 10):
+            pdec.reset()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pdec.prefill(pprompt)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                pts.append(e0.elapsed_time(e1))
+        pms = float(np.median(pts))
+        H, I, D = d.hidden, d.inter, d.head_dim
+        proj = (d.n_q + 2 * d.n_kv) * D * H + H * d.n_q * D + 2 * I * H + H * I
+        gemm_flop = 2.0 * Pp * d.n_layers * proj
+        attn_flop = 2.0 * 2 * d.n_layers * d.n_q * D * (Pp * (Pp + 1) / 2)
+        prefill_512 = {"positions": Pp, "ms": pms, "tokens_per_s": Pp / (pms * 1e-3),
+                       "gemm_tflops": gemm_flop / (pms * 1e-3) / 1e12,
+                       "flop": gemm_flop + attn_flop, "bf16_peak_tflops": read_bf16_peak(),
+                       "frac_of_bf16_peak": gemm_flop / (pms * 1e-3) / 1e12 / read_bf16_peak()}
+        pdec.close()
+
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
         s_per_frame, nfr = oracle_frame_seconds(host_w, wl, frames=20, budget_s=args.cpu_budget)
@@ -388,6 +427,7 @@ def run_gpu(args, wl_name, wl):
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu_baseline,
         "prefill_ms": prefill_ms,
+        "prefill_512": prefill_512,
         "setup_s": gen_s,
     }
     if rank == 0:
@@ -406,6 +446,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-prefill", action="store_true", help="skip the P = 512 batched-prefill measurement")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the workload's depth (small profiling cases only; not a bench line)")
     args = ap.parse_args()
