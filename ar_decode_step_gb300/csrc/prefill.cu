@@ -9,8 +9,9 @@
 //   qk_rope_kv_rows   per-head q/k RMSNorm + RoPE at position pos0 + p, q kept
 //                     in fp32 (pre-scaled by 1/sqrt(128)), k and v written to
 //                     the bf16 cache
-//   attention_rows    causal GQA: row p attends positions [0, pos0 + p];
-//                     output rounded to bf16 (the O-proj GEMM's A operand)
+//   attention_mma     causal GQA on the tensor cores: row p attends positions
+//                     [0, pos0 + p]; output rounded to bf16 (the O-proj
+//                     GEMM's A operand)
 #include "kernels.h"
 
 namespace tts {
@@ -91,149 +92,221 @@ __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const floa
     }
 }
 
-// Causal GQA attention over the cache for rows [rb*16, rb*16+16) of the
-// prompt and the G query heads of kv head g: G*16 (row, head) pairs per CTA,
-// 2G per warp (one head, consecutive rows).  Keys go through shared memory 64
-// at a time (fp32, K rows padded against bank conflicts).  Register tiling:
-// a lane scores its two keys against every pair of its warp (each K value
-// loaded once for all pairs, the queries broadcast); the probabilities go
-// through a per-warp shared tile, and for the output each lane keeps 4 dims
-// of every pair (each V value loaded once for all pairs).  Online softmax in
-// fp32.
-constexpr int kAttRows = 16;
-constexpr int kAttKeys = 64;
-constexpr int kKPad = kHeadDim + 4;
+// ---- causal GQA attention on the tensor cores --------------------------------
+// Rows [row0, row0 + 16) of the prompt against the G query heads of kv head g:
+// warp w takes query head g*G + w for the 16 rows.  Per 64-key tile,
+//   S = Q K^T      mma.sync m16n8k16, bf16 operands, fp32 accumulation
+//                  (Q rounded to bf16 once; K straight from the bf16 cache)
+//   online softmax in fp32 on the accumulator fragments (row max and the
+//                  rescale of O); P rounded to bf16 and reused in registers as
+//                  the A operand of
+//   O += P V       mma.sync, V read transposed from shared memory.
+// Row p attends positions [0, pos0 + p].  K/V tiles are double-buffered in
+// shared memory (cp.async); the row sums are taken over the rounded P, the
+// weights O is built from.
+constexpr int kMmaRows = 16;
+constexpr int kMmaKeys = 64;
+constexpr int kMmaPad = kHeadDim + 8;  // bf16 per shared row: 272 B, the 8 rows of an ldmatrix on distinct banks
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int G>
-constexpr int attention_rows_smem() {
-    return (G * kAttRows * kHeadDim + kAttKeys * kKPad + kAttKeys * kHeadDim + G * kAttRows * kAttKeys) *
-           (int)sizeof(float);
+constexpr int attention_mma_smem() {
+    return 2 * 2 * kMmaKeys * kMmaPad * (int)sizeof(__nv_bfloat16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t* r, const void* smem_row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(smem_row)));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* smem_row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(smem_row)));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int G>
-__global__ void __launch_bounds__(kRowThreads) attention_rows_kernel(const float* Q, const __nv_bfloat16* kc,
-                                                                     const __nv_bfloat16* vc,
-                                                                     __nv_bfloat16* out, int pos0, int P, int n_q,
-                                                                     int max_pos) {
-    extern __shared__ __align__(16) float sm[];
-    constexpr int kPairs = G * kAttRows;
-    constexpr int kPerWarp = kPairs / (kRowThreads / 32);
-    float* Qs = sm;                                    // [pairs][128]
-    float* Ks = Qs + kPairs * kHeadDim;                // [64][132]
-    float* Vs = Ks + kAttKeys * kKPad;                 // [64][128]
-    float* Ps = Vs + kAttKeys * kHeadDim;              // [pairs][64] probabilities
-    const int rb = blockIdx.x, g = blockIdx.y;
+__global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, const __nv_bfloat16* kc,
+                                                               const __nv_bfloat16* vc, __nv_bfloat16* out,
+                                                               int pos0, int P, int n_q, int max_pos) {
+    extern __shared__ __align__(16) __nv_bfloat16 kvs[];  // [2 buffers][K, V][64 keys][kMmaPad]
+    const int rb = gridDim.x - 1 - blockIdx.x;             // the longest rows first
+    const int g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = rb * kAttRows;
-    const int nrows = min(kAttRows, P - row0);
+    const int gi = lane >> 2, ti = lane & 3;                // fragment row group, thread in group
+    const int row0 = rb * kMmaRows;
+    const int nrows = min(kMmaRows, P - row0);
+    const int key_end = pos0 + row0 + nrows;                // keys [0, key_end) are read
+    const int ntiles = (key_end + kMmaKeys - 1) / kMmaKeys;
     const size_t cache0 = (size_t)g * max_pos * kHeadDim;
+    const int h = g * G + warp;
 
-    // pair = head_local * 16 + row_local; warp w owns pairs [w * kPerWarp, (w+1) * kPerWarp)
-    for (int i = threadIdx.x; i < kPairs * kHeadDim / 4; i += kRowThreads) {
-        const int pair = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
-        const int hl = pair / kAttRows, rl = pair % kAttRows;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (rl < nrows) v = reinterpret_cast<const float4*>(Q + ((size_t)(row0 + rl) * n_q + g * G + hl) * kHeadDim)[d4];
-        reinterpret_cast<float4*>(Qs)[i] = v;
-    }
-    const int pair0 = warp * kPerWarp;
-    int qpos[kPerWarp];
-    int qpos_max = -1;
-#pragma unroll
-    for (int i = 0; i < kPerWarp; ++i) {
-        const int rl = (pair0 + i) % kAttRows;
-        qpos[i] = rl < nrows ? pos0 + row0 + rl : -1;  // -1: no such row (never attends)
-        qpos_max = max(qpos_max, qpos[i]);
-    }
-    float m[kPerWarp], l[kPerWarp], o[kPerWarp][4];
-#pragma unroll
-    for (int i = 0; i < kPerWarp; ++i) {
-        m[i] = -INFINITY;
-        l[i] = 0.f;
-        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    }
-    float* pw = Ps + pair0 * kAttKeys;
-    const int kmax = pos0 + row0 + nrows - 1;  // last key any row of this block sees
-    for (int k0 = 0; k0 <= kmax; k0 += kAttKeys) {
-        __syncthreads();  // previous tile consumed (and Qs written, first time)
-        for (int i = threadIdx.x; i < kAttKeys * kHeadDim / 4; i += kRowThreads) {
-            const int kr = i / (kHeadDim / 4), d4 = i % (kHeadDim / 4);
-            const int key = k0 + kr;
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (key <= kmax) {
-                const uint2 kb = *reinterpret_cast<const uint2*>(kc + cache0 + (size_t)key * kHeadDim + 4 * d4);
-                const uint2 vb = *reinterpret_cast<const uint2*>(vc + cache0 + (size_t)key * kHeadDim + 4 * d4);
-                kv = make_float4(bf16lo(kb.x), bf16hi(kb.x), bf16lo(kb.y), bf16hi(kb.y));
-                vv = make_float4(bf16lo(vb.x), bf16hi(vb.x), bf16lo(vb.y), bf16hi(vb.y));
+    auto load_tile = [&](int t, int buf) {
+        __nv_bfloat16* Ks = kvs + (size_t)buf * 2 * kMmaKeys * kMmaPad;
+        __nv_bfloat16* Vs = Ks + kMmaKeys * kMmaPad;
+        for (int i = threadIdx.x; i < kMmaKeys * (kHeadDim / 8); i += 32 * G) {
+            const int kr = i / (kHeadDim / 8), c8 = i % (kHeadDim / 8);
+            const int key = t * kMmaKeys + kr;
+            __nv_bfloat16* kd = Ks + kr * kMmaPad + 8 * c8;
+            __nv_bfloat16* vd = Vs + kr * kMmaPad + 8 * c8;
+            if (key < key_end) {
+                cp_async16(kd, kc + cache0 + (size_t)key * kHeadDim + 8 * c8);
+                cp_async16(vd, vc + cache0 + (size_t)key * kHeadDim + 8 * c8);
+            } else {  // past the last key read: zeros (masked scores, zero weights)
+                *reinterpret_cast<uint4*>(kd) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(vd) = make_uint4(0u, 0u, 0u, 0u);
             }
-            *reinterpret_cast<float4*>(Ks + kr * kKPad + 4 * d4) = kv;
-            *reinterpret_cast<float4*>(Vs + kr * kHeadDim + 4 * d4) = vv;
+        }
+        cp_async_commit();
+    };
+    load_tile(0, 0);
+
+    // this warp's Q (16 rows x 128 dims) as A fragments, one per 16-dim k-step
+    uint32_t qa[kHeadDim / 16][4];
+    {
+        const bool v0 = gi < nrows, v1 = gi + 8 < nrows;
+        const float* q0 = Q + ((size_t)(row0 + gi) * n_q + h) * kHeadDim;
+        const float* q1 = Q + ((size_t)(row0 + gi + 8) * n_q + h) * kHeadDim;
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+            const int d = ks * 16 + 2 * ti;
+            const float2 z = make_float2(0.f, 0.f);
+            const float2 a00 = v0 ? *reinterpret_cast<const float2*>(q0 + d) : z;
+            const float2 a01 = v0 ? *reinterpret_cast<const float2*>(q0 + d + 8) : z;
+            const float2 a10 = v1 ? *reinterpret_cast<const float2*>(q1 + d) : z;
+            const float2 a11 = v1 ? *reinterpret_cast<const float2*>(q1 + d + 8) : z;
+            qa[ks][0] = pack_bf16x2(a00.x, a00.y);
+            qa[ks][1] = pack_bf16x2(a10.x, a10.y);
+            qa[ks][2] = pack_bf16x2(a01.x, a01.y);
+            qa[ks][3] = pack_bf16x2(a11.x, a11.y);
+        }
+    }
+    float o[kHeadDim / 8][4];
+#pragma unroll
+    for (int d = 0; d < kHeadDim / 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gi and gi + 8 (lane partial sums)
+    const int qpos0 = pos0 + row0 + gi, qpos1 = qpos0 + 8;
+    const int mat = lane >> 3, mrow = lane & 7;  // ldmatrix: this lane addresses row mrow of matrix mat
+
+    for (int t = 0; t < ntiles; ++t) {
+        if (t + 1 < ntiles) {
+            load_tile(t + 1, (t + 1) & 1);
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
         }
         __syncthreads();
-        if (k0 > qpos_max) continue;  // warp-uniform: no row of this warp reaches the tile
+        const __nv_bfloat16* Ks = kvs + (size_t)(t & 1) * 2 * kMmaKeys * kMmaPad;
+        const __nv_bfloat16* Vs = Ks + kMmaKeys * kMmaPad;
 
-        // scores of keys k0 + lane and k0 + lane + 32 against every pair of the warp
-        float s0[kPerWarp], s1[kPerWarp];
+        // S = Q K^T over the tile: 8 n-tiles of 8 keys
+        float s[kMmaKeys / 8][4];
 #pragma unroll
-        for (int i = 0; i < kPerWarp; ++i) s0[i] = s1[i] = 0.f;
-        const float* ka = Ks + lane * kKPad;
-        const float* kb = Ks + (lane + 32) * kKPad;
-        const float* qw = Qs + pair0 * kHeadDim;
-#pragma unroll 2
-        for (int d = 0; d < kHeadDim; d += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(ka + d);
-            const float4 b = *reinterpret_cast<const float4*>(kb + d);
+        for (int j = 0; j < kMmaKeys / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
-            for (int i = 0; i < kPerWarp; ++i) {
-                const float4 qq = *reinterpret_cast<const float4*>(qw + i * kHeadDim + d);
-                s0[i] = fmaf(qq.x, a.x, fmaf(qq.y, a.y, fmaf(qq.z, a.z, fmaf(qq.w, a.w, s0[i]))));
-                s1[i] = fmaf(qq.x, b.x, fmaf(qq.y, b.y, fmaf(qq.z, b.z, fmaf(qq.w, b.w, s1[i]))));
+        for (int np = 0; np < kMmaKeys / 16; ++np) {
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                uint32_t b[4];  // keys np*16 + {0..7 | 8..15} x dims ks*16 + {0..7 | 8..15}
+                ldmatrix_x4(b, Ks + (np * 16 + (mat >> 1) * 8 + mrow) * kMmaPad + ks * 16 + (mat & 1) * 8);
+                mma_bf16_16816(s[2 * np], qa[ks], b[0], b[1]);
+                mma_bf16_16816(s[2 * np + 1], qa[ks], b[2], b[3]);
             }
         }
-        // online softmax per pair; probabilities to the warp's shared tile
+        // causal mask: key > position of the row
+        const int kbase = t * kMmaKeys;
+        if (kbase + kMmaKeys - 1 > qpos0) {
 #pragma unroll
-        for (int i = 0; i < kPerWarp; ++i) {
-            if (k0 + lane > qpos[i]) s0[i] = -INFINITY;
-            if (k0 + lane + 32 > qpos[i]) s1[i] = -INFINITY;
-            const float mx = warp_max(fmaxf(s0[i], s1[i]));
-            const float mn = fmaxf(m[i], mx);
-            // a pair with no key in this tile (mn = -inf) keeps its state
-            const float corr = mn == -INFINITY ? 1.f : __expf(m[i] - mn);
-            const float p0 = mn == -INFINITY ? 0.f : __expf(s0[i] - mn);
-            const float p1 = mn == -INFINITY ? 0.f : __expf(s1[i] - mn);
-            l[i] = l[i] * corr + warp_sum(p0 + p1);
-            m[i] = mn;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) o[i][jj] *= corr;
-            pw[i * kAttKeys + lane] = p0;
-            pw[i * kAttKeys + lane + 32] = p1;
-        }
-        __syncwarp();
-        const int nk = min(kAttKeys, qpos_max - k0 + 1);
-        for (int kk = 0; kk < nk; ++kk) {
-            const float4 vv = *reinterpret_cast<const float4*>(Vs + kk * kHeadDim + 4 * lane);
-#pragma unroll
-            for (int i = 0; i < kPerWarp; ++i) {
-                const float pk = pw[i * kAttKeys + kk];
-                o[i][0] = fmaf(pk, vv.x, o[i][0]);
-                o[i][1] = fmaf(pk, vv.y, o[i][1]);
-                o[i][2] = fmaf(pk, vv.z, o[i][2]);
-                o[i][3] = fmaf(pk, vv.w, o[i][3]);
+            for (int j = 0; j < kMmaKeys / 8; ++j) {
+                const int key = kbase + j * 8 + 2 * ti;
+                if (key > qpos0) s[j][0] = -INFINITY;
+                if (key + 1 > qpos0) s[j][1] = -INFINITY;
+                if (key > qpos1) s[j][2] = -INFINITY;
+                if (key + 1 > qpos1) s[j][3] = -INFINITY;
             }
         }
-        __syncwarp();
+        // online softmax: the four lanes of a row group share rows gi and gi + 8
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kMmaKeys / 8; ++j) {
+            mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        // a row with no key yet (only rows past the prompt) keeps zero weights
+        const float e0 = mn0 == -INFINITY ? 0.f : mn0 * kLog2e;
+        const float e1 = mn1 == -INFINITY ? 0.f : mn1 * kLog2e;
+        const float c0 = exp2f(m0 * kLog2e - e0), c1 = exp2f(m1 * kLog2e - e1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 *= c0;
+        l1 *= c1;
+#pragma unroll
+        for (int d = 0; d < kHeadDim / 8; ++d) {
+            o[d][0] *= c0;
+            o[d][1] *= c0;
+            o[d][2] *= c1;
+            o[d][3] *= c1;
+        }
+        uint32_t pa[kMmaKeys / 16][4];  // P as A fragments, one per 16-key k-step
+#pragma unroll
+        for (int j = 0; j < kMmaKeys / 8; ++j) {
+            const __nv_bfloat162 p01 =
+                __floats2bfloat162_rn(exp2f(s[j][0] * kLog2e - e0), exp2f(s[j][1] * kLog2e - e0));
+            const __nv_bfloat162 p23 =
+                __floats2bfloat162_rn(exp2f(s[j][2] * kLog2e - e1), exp2f(s[j][3] * kLog2e - e1));
+            l0 += __low2float(p01) + __high2float(p01);
+            l1 += __low2float(p23) + __high2float(p23);
+            pa[j >> 1][(j & 1) * 2] = *reinterpret_cast<const uint32_t*>(&p01);
+            pa[j >> 1][(j & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&p23);
+        }
+        // O += P V: 16 n-tiles of 8 dims, 4 k-steps of 16 keys
+#pragma unroll
+        for (int dp = 0; dp < kHeadDim / 16; ++dp) {
+#pragma unroll
+            for (int kk = 0; kk < kMmaKeys / 16; ++kk) {
+                uint32_t b[4];  // keys kk*16 + {0..7 | 8..15} x dims dp*16 + {0..7 | 8..15}, transposed
+                ldmatrix_x4_trans(b, Vs + (kk * 16 + (mat & 1) * 8 + mrow) * kMmaPad + dp * 16 + (mat >> 1) * 8);
+                mma_bf16_16816(o[2 * dp], pa[kk], b[0], b[1]);
+                mma_bf16_16816(o[2 * dp + 1], pa[kk], b[2], b[3]);
+            }
+        }
+        __syncthreads();  // this buffer is refilled two tiles on
     }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
 #pragma unroll
-    for (int i = 0; i < kPerWarp; ++i) {
-        const int pair = pair0 + i;
-        const int hl = pair / kAttRows, rl = pair % kAttRows;
-        if (rl >= nrows) continue;
-        const float inv = 1.0f / l[i];
-        __nv_bfloat16* dst = out + ((size_t)(row0 + rl) * n_q + g * G + hl) * kHeadDim + 4 * lane;
-        dst[0] = __float2bfloat16_rn(o[i][0] * inv);
-        dst[1] = __float2bfloat16_rn(o[i][1] * inv);
-        dst[2] = __float2bfloat16_rn(o[i][2] * inv);
-        dst[3] = __float2bfloat16_rn(o[i][3] * inv);
+    for (int d = 0; d < kHeadDim / 8; ++d) {
+        const int col = d * 8 + 2 * ti;
+        if (gi < nrows)
+            *reinterpret_cast<__nv_bfloat162*>(out + ((size_t)(row0 + gi) * n_q + h) * kHeadDim + col) =
+                __floats2bfloat162_rn(o[d][0] * inv0, o[d][1] * inv0);
+        if (gi + 8 < nrows)
+            *reinterpret_cast<__nv_bfloat162*>(out + ((size_t)(row0 + gi + 8) * n_q + h) * kHeadDim + col) =
+                __floats2bfloat162_rn(o[d][2] * inv1, o[d][3] * inv1);
     }
 }
 
@@ -241,16 +314,16 @@ template <int G>
 cudaError_t launch_attention_rows_t(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                                     __nv_bfloat16* out, int pos0, int P, int n_q, int n_kv, int max_pos,
                                     cudaStream_t s) {
-    constexpr int smem = attention_rows_smem<G>();
+    constexpr int smem = attention_mma_smem<G>();
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_rows_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attention_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const dim3 grid((P + kAttRows - 1) / kAttRows, n_kv);
-    attention_rows_kernel<G><<<grid, kRowThreads, smem, s>>>(Q, kc, vc, out, pos0, P, n_q, max_pos);
+    const dim3 grid((P + kMmaRows - 1) / kMmaRows, n_kv);
+    attention_mma_kernel<G><<<grid, 32 * G, smem, s>>>(Q, kc, vc, out, pos0, P, n_q, max_pos);
     return cudaGetLastError();
 }
 
