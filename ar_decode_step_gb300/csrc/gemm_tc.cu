@@ -124,9 +124,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * kBM;
+    // the M tiles of one N tile are adjacent in the grid: they run together
+    // and share the weight tile through L2 (one DRAM read per weight)
+    const int m0 = blockIdx.x * kBM;
     const int nt = EPI == kGemmSwiglu ? MMA_N / 2 : MMA_N;  // output columns of this tile
-    const int n0 = blockIdx.x * nt;
+    const int n0 = blockIdx.y * nt;
     const int kb0 = blockIdx.z * p.kb_per_split;
     const int kb1 = min(p.K / kBK, kb0 + p.kb_per_split);
     const int nkb = kb1 - kb0;
@@ -334,7 +336,7 @@ cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p_i
     p.atomic = splits > 1 ? 1 : 0;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, p.M, p.K, kBM)) return cudaErrorInvalidValue;
-    const dim3 grid(p.N / p.bn, (p.M + kBM - 1) / kBM, splits);
+    const dim3 grid((p.M + kBM - 1) / kBM, p.N / p.bn, splits);
     if (epi == kGemmSwiglu) {
         // B = [gate rows; up rows] of a [2 n_half][K] matrix; N = n_half output columns
         if (!make_map(&mb, B, 2 * p.n_half, p.K, 128)) return cudaErrorInvalidValue;
