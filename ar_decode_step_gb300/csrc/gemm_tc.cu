@@ -8,7 +8,7 @@
 //
 // One CTA per 128 x BN output tile (BN = 64 or 128; 256 for the fused gate/up tile):
 //   warp 0 (one thread)  TMA producer: 128 x 64 A box and BN x 64 B box(es)
-//                        per k-block into a 4-stage ring (128-byte swizzle),
+//                        per k-block into a ring of 4-8 stages (128-byte swizzle),
 //                        completion counted on the stage's "full" mbarrier;
 //   warp 1 (one thread)  MMA issuer: four tcgen05.mma (K = 16 each) per
 //                        k-block into the TMEM accumulator, then
@@ -33,7 +33,14 @@ namespace {
 
 constexpr int kBM = 128;          // rows of A per tile (MMA M)
 constexpr int kBK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
+// ring depth: as many stages as fit in shared memory (at most 8), so narrow
+// tiles keep as many bytes in flight from L2 as wide ones
+constexpr int kSmemRing = 225 * 1024;
+template <int MMA_N>
+constexpr int gemm_stages() {
+    return kSmemRing / (int)(kBM * kBK * 2 + MMA_N * kBK * 2) < 8 ? kSmemRing / (int)(kBM * kBK * 2 + MMA_N * kBK * 2)
+                                                                   : 8;
+}
 constexpr int kGemmThreads = 128;
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KB
 
@@ -112,6 +119,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams p) {
     extern __shared__ unsigned char smem_raw[];
+    constexpr int kStages = gemm_stages<MMA_N>();
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
     __shared__ uint32_t s_tmem;
     __shared__ int s_fail;
@@ -281,7 +289,7 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
 
 template <int EPI, int MMA_N>
 constexpr int gemm_smem_bytes() {
-    return kStages * (int)(kATileBytes + MMA_N * kBK * 2) + 1024;
+    return gemm_stages<MMA_N>() * (int)(kATileBytes + MMA_N * kBK * 2) + 1024;
 }
 
 template <int EPI, int MMA_N>
