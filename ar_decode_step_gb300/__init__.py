@@ -57,6 +57,7 @@ SIGNATURES = {
     "tts_decode_step": (_I, [_VP, _VP, _VP]),
     "tts_decode_steps": (_I, [_VP, _I, _VP]),
     "tts_rewind": (_I, [_VP, _I, _I]),
+    "tts_set_sampling": (_I, [_VP, ctypes.c_float, ctypes.c_ulonglong]),
     "tts_set_kv": (_I, [_VP, _VP, _VP, _I, _I]),
     "tts_get_kv": (_I, [_VP, _VP, _VP, _I, _I]),
     "tts_get_logits": (_I, [_VP, _VP]),
@@ -267,6 +268,11 @@ class Decoder:
         out = np.empty((n, self.dims.n_cb), np.int32)
         _call("tts_decode_steps", self._ctx, n, _ptr(out))
         return out
+
+    def set_sampling(self, temperature: float, seed: int = 0):
+        """tts_set_sampling: 0 = greedy argmax; > 0 = seeded categorical draws
+        from softmax(logits / temperature)."""
+        _call("tts_set_sampling", self._ctx, float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF)
 
     def rewind(self, pos: int, t: int = 0):
         _call("tts_rewind", self._ctx, pos, t)

@@ -29,8 +29,10 @@ struct alignas(64) DevState {
     int err;          // error bits
     int hist_idx;     // next slot of the code history ring
     int prefill_row;  // next prompt row the prefill embeds
-    int pad[2];
+    float temperature;        // <= 0: greedy argmax; > 0: categorical draw from softmax(logits / T)
+    int pad;
     int codes[kMaxCodebooks];  // codes produced by the last step = next input
+    unsigned long long seed;   // key of the draws (temperature > 0)
 };
 
 // ---- programmatic dependent launch ------------------------------------

@@ -632,8 +632,79 @@ __device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, 
                                                                                                              : -1;
 }
 
+// Philox4x32-10 counter-based generator (Salmon, Moraes, Dror and Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3", SC'11): ten rounds of the
+// 4 x 32-bit Philox S-box, the key bumped by the Weyl increments each round.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Temperature sampling for codebook k at frame t, one warp ("Higgs Audio v3
+// TTS-4B on FlashRT", section 4 sampling policy: stable softmax and a
+// stateless categorical draw keyed by the request seed).  u in [0, 1) is the
+// top 24 bits of the first Philox word for counter (t, k, 0, 0) and key seed;
+// the code is the first v whose running sum of exp((x_v - max) / T) exceeds
+// u times the total.  Lane l sums the contiguous chunk [l c, (l+1) c) of the
+// V logits (c = ceil(V / 32)), a warp scan orders the chunks, and the lane
+// holding the crossing walks its chunk.  Returns the code in every lane.
+__device__ __forceinline__ int sample_codebook(const float* row, int V, float T, unsigned long long seed, int t,
+                                               int k) {
+    const int lane = threadIdx.x & 31;
+    const int c = (V + 31) / 32;
+    const int v0 = min(V, lane * c), v1 = min(V, v0 + c);
+    float mx = -INFINITY;
+    for (int v = v0; v < v1; ++v) mx = fmaxf(mx, __ldcg(row + v));
+    mx = warp_max(mx);
+    const float invT = 1.0f / T;
+    float sum = 0.f;
+    for (int v = v0; v < v1; ++v) sum += expf((__ldcg(row + v) - mx) * invT);
+    float incl = sum;  // inclusive scan over lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const float total = __shfl_sync(0xffffffffu, incl, 31);
+    const uint4 r = philox4x32_10(make_uint4((uint32_t)t, (uint32_t)k, 0u, 0u), (uint32_t)seed,
+                                  (uint32_t)(seed >> 32));
+    const float u = (float)(r.x >> 8) * (1.0f / 16777216.0f);
+    const float target = u * total;
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > target);
+    int code = -1;
+    if (hit) {
+        const int owner = __ffs(hit) - 1;
+        if (lane == owner) {
+            float run = incl - sum;
+            for (int v = v0; v < v1; ++v) {
+                const float e = expf((__ldcg(row + v) - mx) * invT);
+                run += e;
+                if (run > target) { code = v; break; }
+                if (e > 0.f) code = v;  // rounding: the crossing is at the chunk's last weight
+            }
+        }
+        code = __shfl_sync(0xffffffffu, code, owner);
+    } else {
+        // u * total rounded up to the total: the last code with a non-zero weight
+        int last = -1;
+        for (int v = v0; v < v1; ++v)
+            if (expf((__ldcg(row + v) - mx) * invT) > 0.f) last = v;
+        const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
+        code = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
+    }
+    return code < 0 ? 0 : code;
+}
+
 // Codebook head, after every CTA stored its logits: the last CTA to arrive
-// takes the per-codebook greedy argmax (ties: lowest code) under the delay
+// takes the per-codebook greedy argmax (ties: lowest code; or, with a positive
+// temperature in the state, a sampled code: sample_codebook) under the delay
 // mask (codebook k is BOS-pad before frame k and EOC from frame eoc + k on;
 // "Higgs Audio v3 TTS-4B on FlashRT", section 4 sampling policy and section 5),
 // records the codes (next step's input and the history ring) and advances the
@@ -648,7 +719,13 @@ __device__ __forceinline__ void head_tail(const float* logits, int n_cb, int V, 
     if (!*s_last) return;
     __threadfence();
     const int t = st->t, eoc = st->eoc;
+    const float T = st->temperature;
     for (int k = warp; k < n_cb; k += kConsumerWarps) {
+        if (T > 0.f) {
+            const int c = sample_codebook(logits + (size_t)k * V, V, T, st->seed, t, k);
+            if (lane == 0) s_codes[k] = t < k ? V - 2 : (eoc >= 0 && t >= eoc + k) ? V - 1 : c;
+            continue;
+        }
         float best = -INFINITY;
         int bi = 0x7fffffff;
         for (int v = lane; v < V; v += 32) {

@@ -39,6 +39,8 @@ struct tts_ctx {
     int device = 0, num_sms = 0;
     int qkv_rows = 0, attn_dim = 0, G = 1, S = 1;
     bool pdl = true;
+    float temperature = 0.f;     // sampling head: <= 0 greedy
+    unsigned long long seed = 0;
 
     const __nv_bfloat16 *embed = nullptr, *head = nullptr, *final_norm = nullptr;
     std::vector<LayerW> L;
@@ -273,6 +275,8 @@ int pull_state(tts_ctx* c) {
 
 int push_state(tts_ctx* c, const DevState& s) {
     *c->h_in = s;
+    c->h_in->temperature = c->temperature;  // the sampling settings outlive resets and rewinds
+    c->h_in->seed = c->seed;
     TTS_CK(cudaMemcpyAsync(c->st, c->h_in, sizeof(DevState), cudaMemcpyHostToDevice, c->stream));
     TTS_CK(cudaStreamSynchronize(c->stream));
     c->pos = s.pos;
@@ -714,6 +718,16 @@ int tts_set_frame(tts_ctx* ctx, int t, int eoc_frame) {
     s.t = t;
     s.eoc = eoc_frame;
     return push_state(ctx, s);
+}
+
+int tts_set_sampling(tts_ctx* ctx, float temperature, unsigned long long seed) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!(temperature >= 0.f) || !std::isfinite(temperature)) return TTS_ERR_ARG;
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    ctx->temperature = temperature;
+    ctx->seed = seed;
+    return push_state(ctx, *ctx->h_out);
 }
 
 int tts_get_state(tts_ctx* ctx, int* pos, int* t, int* eoc) {

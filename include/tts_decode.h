@@ -167,6 +167,19 @@ int tts_get_hidden(tts_ctx* ctx, float* hidden_host);
 /* Set the frame index and the EOC frame (-1 = none) used by the delay mask. */
 int tts_set_frame(tts_ctx* ctx, int t, int eoc_frame);
 
+/* Sampling head ("Higgs Audio v3 TTS-4B on FlashRT", section 4 sampling
+ * policy).  temperature == 0 (the default) keeps the greedy argmax; a positive
+ * temperature T replaces it, per codebook k at frame t, by a categorical draw
+ * from softmax(logits_k / T) over all cb_vocab entries: with u the top 24 bits
+ * of the first Philox4x32-10 word for counter (t, k, 0, 0) and key `seed`
+ * (low word first), scaled to [0, 1), the code is the first v whose running
+ * sum of exp((logit_v - max) / T) exceeds u times the total.  The delay mask
+ * applies afterwards as in greedy decoding.  The same seed and frames give the
+ * same draws.  The setting stays until changed (also across tts_reset and
+ * tts_rewind) and applies to every later step, including tts_decode_steps.
+ * Returns TTS_ERR_ARG for a negative or non-finite temperature. */
+int tts_set_sampling(tts_ctx* ctx, float temperature, unsigned long long seed);
+
 /* Read position, frame index and EOC frame (any pointer may be NULL). */
 int tts_get_state(tts_ctx* ctx, int* pos, int* t, int* eoc_frame);
 

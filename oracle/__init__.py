@@ -78,6 +78,8 @@ def lib():
                 "or_embed": (None, [vp, i32, i32, i32, vp, vp]),
                 "or_argmax": (i32, [vp, i32]),
                 "or_delay_code": (i32, [i32, i32, i32, i32]),
+                "or_philox4x32_10": (None, [vp, vp, vp]),
+                "or_sample_code": (i32, [vp, i32, dbl, ctypes.c_uint64, i32, i32, vp]),
                 "or_decode_step": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
                                          ctypes.POINTER(_State), vp, vp, vp, vp]),
                 "or_prefill": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
@@ -200,6 +202,23 @@ def argmax(v: np.ndarray) -> int:
 
 def delay_code(k: int, t: int, eoc: int, am: int) -> int:
     return lib().or_delay_code(k, t, eoc, am)
+
+
+def philox4x32_10(ctr, key):
+    c = np.ascontiguousarray(ctr, np.uint32)
+    kk = np.ascontiguousarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib().or_philox4x32_10(_p(c), _p(kk), _p(out))
+    return [int(x) for x in out]
+
+
+def sample_code(logits, T: float, seed: int, t: int, k: int):
+    """(code, margin): the temperature draw of one codebook, and how far
+    u * total lies from the nearest running sum (relative to the total)."""
+    v = np.ascontiguousarray(logits, np.float64)
+    m = np.zeros(1, np.float64)
+    c = lib().or_sample_code(_p(v), v.size, float(T), int(seed) & 0xFFFFFFFFFFFFFFFF, t, k, _p(m))
+    return c, float(m[0])
 
 
 # ---- the whole step ----

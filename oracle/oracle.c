@@ -245,6 +245,56 @@ int or_argmax(const double* v, int n) {
     return best;
 }
 
+/* Philox4x32-10 [Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC'11]: ten rounds; a round multiplies words 0 and 2 by
+ * the two Philox multipliers and recombines the high and low halves with
+ * words 1 and 3 and the round key; the key advances by the two Weyl
+ * constants (golden ratio and sqrt(3) - 1, scaled to 32 bits) per round. */
+void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Temperature sampling [FlashRT s4 sampling policy: stable softmax, a
+ * stateless categorical draw keyed by the request seed]: inverse CDF in index
+ * order, fp64. */
+int or_sample_code(const double* logits, int V, double T, uint64_t seed, int t, int k, double* margin) {
+    const uint32_t ctr[4] = {(uint32_t)t, (uint32_t)k, 0u, 0u};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    or_philox4x32_10(ctr, key, r);
+    const double u = (double)(r[0] >> 8) / 16777216.0;
+    double mx = -INFINITY;
+    for (int v = 0; v < V; ++v)
+        if (logits[v] > mx) mx = logits[v];
+    double total = 0.0;
+    for (int v = 0; v < V; ++v) total += exp((logits[v] - mx) / T);
+    const double target = u * total;
+    double run = 0.0, best = INFINITY;
+    int code = -1;
+    for (int v = 0; v < V; ++v) {
+        run += exp((logits[v] - mx) / T);
+        const double dist = fabs(run - target);
+        if (dist < best) best = dist;
+        if (code < 0 && run > target) code = v;
+    }
+    if (code < 0) code = V - 1;
+    if (margin) *margin = fabs(target) < INFINITY ? best / total : 0.0;
+    return code;
+}
+
 /* Delay pattern [FlashRT header "delay pattern"; FlashRT s5 "BOC/EOC";
  * SGLang arch]: codebook k runs k frames behind codebook 0.  At frame t,
  * codebook k has not started while t < k and emits BOS-pad (1024); once

@@ -14,7 +14,8 @@
  * page header (Qwen3-4B backbone: 36 layers, hidden 2560, GQA 32q/8kv,
  * head_dim 128, SwiGLU, RoPE theta 1e6; fused 8 x 1026 codebook head, delay
  * pattern); the decode chain in section 5 "What runs under the hood"; the
- * sampling policy in section 4 (greedy argmax + delay mask + embedding); the
+ * sampling policy in section 4 (greedy argmax + delay mask + embedding, or a
+ * seeded categorical draw at a positive temperature); the
  * FP8 W8A8 description in the Performance section and section 8.  The fused
  * multi-codebook embedding (sum of 8 codebook embeddings) is from the
  * SGLang-Omni Higgs Audio v3 post, architecture paragraph.
@@ -83,6 +84,16 @@ void   or_attention(const double* q, const uint16_t* Kc, const uint16_t* Vc,
                     int n_q, int n_kv, int D, int max_pos, int len, double* out);
 void   or_embed(const uint16_t* E, int n_cb, int V, int H, const int32_t* codes, double* x);
 int    or_argmax(const double* v, int n);
+/* Philox4x32-10 (Salmon et al., SC'11): out = the 4 words for counter ctr
+ * and key key. */
+void   or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+/* Temperature sampling of one codebook (FlashRT section 4 sampling policy):
+ * u = top 24 bits of the first Philox word for counter (t, k, 0, 0), key
+ * seed, over 2^24; the first v whose running sum of exp((logit_v - max)/T)
+ * exceeds u times the total (fp64).  Also writes, when margin != NULL, the
+ * distance of u * total from the nearest running sum, relative to the total
+ * (how far the draw is from flipping to a neighbouring code). */
+int    or_sample_code(const double* logits, int V, double T, uint64_t seed, int t, int k, double* margin);
 int    or_delay_code(int k, int t, int eoc, int argmax_code);
 
 /* ---- the step ---- */
