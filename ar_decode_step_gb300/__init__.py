@@ -58,6 +58,8 @@ SIGNATURES = {
     "tts_decode_steps": (_I, [_VP, _I, _VP]),
     "tts_rewind": (_I, [_VP, _I, _I]),
     "tts_set_sampling": (_I, [_VP, ctypes.c_float, ctypes.c_ulonglong]),
+    "tts_prefix_save": (_I, [_VP]),
+    "tts_prefix_restore": (_I, [_VP]),
     "tts_set_kv": (_I, [_VP, _VP, _VP, _I, _I]),
     "tts_get_kv": (_I, [_VP, _VP, _VP, _I, _I]),
     "tts_get_logits": (_I, [_VP, _VP]),
@@ -273,6 +275,14 @@ class Decoder:
         """tts_set_sampling: 0 = greedy argmax; > 0 = seeded categorical draws
         from softmax(logits / temperature)."""
         _call("tts_set_sampling", self._ctx, float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF)
+
+    def prefix_save(self):
+        """tts_prefix_save: snapshot the cache rows [0, pos) and the state."""
+        _call("tts_prefix_save", self._ctx)
+
+    def prefix_restore(self):
+        """tts_prefix_restore: back to the saved prefix (cache rows and state)."""
+        _call("tts_prefix_restore", self._ctx)
 
     def rewind(self, pos: int, t: int = 0):
         _call("tts_rewind", self._ctx, pos, t)

@@ -41,6 +41,11 @@ struct tts_ctx {
     bool pdl = true;
     float temperature = 0.f;     // sampling head: <= 0 greedy
     unsigned long long seed = 0;
+    // saved prefix (tts_prefix_save): K/V rows [0, pre_len) of every layer and
+    // kv head, packed [n_layers][n_kv][pre_len][128], and the state after them
+    __nv_bfloat16 *pre_k = nullptr, *pre_v = nullptr;
+    int pre_cap = 0, pre_len = 0;
+    DevState pre_state{};
 
     const __nv_bfloat16 *embed = nullptr, *head = nullptr, *final_norm = nullptr;
     std::vector<LayerW> L;
@@ -538,6 +543,8 @@ void destroy(tts_ctx* c) {
     if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
     if (c->prefill_exec) cudaGraphExecDestroy(c->prefill_exec);
     for (void* p : c->allocs) cudaFree(p);
+    if (c->pre_k) cudaFree(c->pre_k);
+    if (c->pre_v) cudaFree(c->pre_v);
     if (c->h_in) cudaFreeHost(c->h_in);
     if (c->h_out) cudaFreeHost(c->h_out);
     if (c->ev0) cudaEventDestroy(c->ev0);
@@ -656,6 +663,50 @@ int tts_rewind(tts_ctx* ctx, int pos, int t) {
     if (!ctx) return TTS_ERR_STATE;
     if (pos < 0 || pos > ctx->pos || t < 0) return TTS_ERR_ARG;
     return push_state(ctx, bos_state(ctx, pos, t, -1));
+}
+
+int tts_prefix_save(tts_ctx* ctx) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    const DevState s = *ctx->h_out;
+    const int P = s.pos;
+    if (P <= 0) return TTS_ERR_ARG;
+    const size_t rows = (size_t)k.n_layers * k.n_kv_heads;
+    if (P > ctx->pre_cap) {
+        if (ctx->pre_k) cudaFree(ctx->pre_k);
+        if (ctx->pre_v) cudaFree(ctx->pre_v);
+        ctx->pre_k = ctx->pre_v = nullptr;
+        ctx->pre_cap = ctx->pre_len = 0;
+        const size_t bytes = rows * P * kHeadDim * sizeof(__nv_bfloat16);
+        TTS_CK(cudaMalloc(&ctx->pre_k, bytes));
+        TTS_CK(cudaMalloc(&ctx->pre_v, bytes));
+        ctx->pre_cap = P;
+    }
+    const size_t row = (size_t)P * kHeadDim * sizeof(__nv_bfloat16);
+    const size_t cpitch = (size_t)k.max_pos * kHeadDim * sizeof(__nv_bfloat16);
+    TTS_CK(cudaMemcpy2DAsync(ctx->pre_k, row, ctx->kc, cpitch, row, rows, cudaMemcpyDeviceToDevice, ctx->stream));
+    TTS_CK(cudaMemcpy2DAsync(ctx->pre_v, row, ctx->vc, cpitch, row, rows, cudaMemcpyDeviceToDevice, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    ctx->pre_len = P;
+    ctx->pre_state = s;
+    return TTS_OK;
+}
+
+int tts_prefix_restore(tts_ctx* ctx) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (ctx->pre_len <= 0) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    const size_t rows = (size_t)k.n_layers * k.n_kv_heads;
+    const size_t row = (size_t)ctx->pre_len * kHeadDim * sizeof(__nv_bfloat16);
+    const size_t cpitch = (size_t)k.max_pos * kHeadDim * sizeof(__nv_bfloat16);
+    TTS_CK(cudaMemcpy2DAsync(ctx->kc, cpitch, ctx->pre_k, row, row, rows, cudaMemcpyDeviceToDevice, ctx->stream));
+    TTS_CK(cudaMemcpy2DAsync(ctx->vc, cpitch, ctx->pre_v, row, row, rows, cudaMemcpyDeviceToDevice, ctx->stream));
+    DevState s = ctx->pre_state;
+    s.err = 0;
+    s.hist_idx = 0;
+    return push_state(ctx, s);
 }
 
 int tts_set_kv(tts_ctx* ctx, const void* kd, const void* vd, int len, int len_stride) {

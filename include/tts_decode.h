@@ -148,6 +148,19 @@ int tts_decode_steps(tts_ctx* ctx, int n, int32_t* codes_out);
  * input is processed).  The next decode step's input is the all-BOS frame. */
 int tts_rewind(tts_ctx* ctx, int pos, int t);
 
+/* Prefix reuse (FlashRT page, section 4 and Performance "prompt prefill": a
+ * resident system prompt's KV is kept and each request prefills only its own
+ * suffix, bit-identically).  tts_prefix_save snapshots cache positions
+ * [0, pos) of every layer and kv head into a library-owned device buffer,
+ * together with the decode state (position, frame, EOC frame, next input
+ * codes); tts_prefix_restore copies them back and restores that state, so a
+ * later tts_prefill(suffix) continues exactly as right after the prefix --
+ * also after a tts_rewind below the prefix or a tts_reset overwrote it.  One
+ * snapshot per context; a new save replaces it.  Errors: TTS_ERR_ARG when
+ * pos is 0 (nothing to save), TTS_ERR_STATE when restoring without a save. */
+int tts_prefix_save(tts_ctx* ctx);
+int tts_prefix_restore(tts_ctx* ctx);
+
 /* Copy a KV prefix into the cache and set the position to len.  k, v: DEVICE
  * bf16 [n_layers][n_kv_heads][len_stride][head_dim] with len <= len_stride;
  * positions [0, len) are copied.  Frame and EOC state are not changed. */

@@ -1,0 +1,111 @@
+"""Prefix reuse (tts_prefix_save / tts_prefix_restore; "Higgs Audio v3 TTS-4B
+on FlashRT", section 4 and Performance "prompt prefill": a resident system
+prompt's KV is reused and each request prefills only its suffix,
+bit-identically).  A request served after a restore -- even after the cache
+rows of the prefix were overwritten in between -- must give the same K/V
+rows and the same codes, bit for bit, as the same request served right after
+the prefix, and as a fresh context that prefills the prefix and the suffix."""
+import numpy as np
+import pytest
+
+import synth
+from helpers import reduced_dims, to_binding_dims
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ads():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import ar_decode_step_gb300.build as b
+    b.build()
+    import ar_decode_step_gb300 as m
+    m.load()
+    return m
+
+
+@pytest.fixture(scope="module")
+def model():
+    d = reduced_dims(2)
+    return d, synth.make_weights(d, gamma_variant=True)
+
+
+def request(dec, suffix, frames):
+    dec.prefill(suffix)
+    codes = dec.decode_steps(frames)
+    return codes, dec.state()
+
+
+def test_prefix_restore_is_bit_identical(ads, model):
+    d, w = model
+    dw = ads.DeviceWeights(w, precision=0)
+    system = synth.delayed_prompt_codes(13)
+    suf_a = synth.random_codes(7, seed=2, stream=31)
+    suf_b = synth.random_codes(5, seed=2, stream=32)
+    end = 13 + 7 + 4
+
+    dec = ads.Decoder(to_binding_dims(d), dw, 64)
+    dec.prefill(system)
+    dec.prefix_save()
+    a1, st1 = request(dec, suf_a, 4)
+    ka1, va1 = dec.get_kv(0, end)
+    # another request, then one that overwrites the prefix rows themselves
+    dec.prefix_restore()
+    request(dec, suf_b, 3)
+    dec.rewind(0)
+    dec.prefill(suf_b)
+    dec.prefix_restore()
+    assert dec.state() == (13, 0, -1)
+    a2, st2 = request(dec, suf_a, 4)
+    ka2, va2 = dec.get_kv(0, end)
+    assert np.array_equal(a1, a2) and st1 == st2
+    assert np.array_equal(ka1, ka2) and np.array_equal(va1, va2)
+    dec.close()
+
+    # a fresh context serving the same request without reuse
+    fresh = ads.Decoder(to_binding_dims(d), dw, 64)
+    fresh.prefill(system)
+    a3, st3 = request(fresh, suf_a, 4)
+    kf, vf = fresh.get_kv(0, end)
+    assert np.array_equal(a1, a3) and st1 == st3
+    assert np.array_equal(ka1, kf) and np.array_equal(va1, vf)
+    fresh.close()
+
+
+def test_prefix_errors(ads, model):
+    d, w = model
+    dw = ads.DeviceWeights(w, precision=0)
+    dec = ads.Decoder(to_binding_dims(d), dw, 32)
+    with pytest.raises(ads.TtsError):
+        dec.prefix_restore()  # nothing saved
+    with pytest.raises(ads.TtsError):
+        dec.prefix_save()     # position 0: nothing to save
+    dec.prefill(synth.delayed_prompt_codes(5))
+    dec.prefix_save()
+    dec.decode_steps(2)
+    dec.prefix_restore()
+    assert dec.state() == (5, 0, -1)
+    dec.close()
+
+
+def test_one_call_and_split_prefill_agree(ads, model):
+    """prefill(prefix + suffix) in one call against prefill(prefix) then
+    prefill(suffix): the rows are the same computation (the GEMMs reduce each
+    row alone in a fixed k order, attention is per row), so the caches agree
+    bit for bit."""
+    d, w = model
+    dw = ads.DeviceWeights(w, precision=0)
+    system = synth.delayed_prompt_codes(13)
+    suf = synth.random_codes(7, seed=2, stream=33)
+    one = ads.Decoder(to_binding_dims(d), dw, 64)
+    one.prefill(np.concatenate([system, suf]))
+    two = ads.Decoder(to_binding_dims(d), dw, 64)
+    two.prefill(system)
+    two.prefill(suf)
+    k1, v1 = one.get_kv(0, 20)
+    k2, v2 = two.get_kv(0, 20)
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    assert np.array_equal(one.decode_steps(3), two.decode_steps(3))
+    one.close()
+    two.close()
