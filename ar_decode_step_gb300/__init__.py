@@ -58,6 +58,7 @@ SIGNATURES = {
     "tts_decode_steps": (_I, [_VP, _I, _VP]),
     "tts_rewind": (_I, [_VP, _I, _I]),
     "tts_set_sampling": (_I, [_VP, ctypes.c_float, ctypes.c_ulonglong]),
+    "tts_decode_until_eoc": (_I, [_VP, _I, _VP, _VP]),
     "tts_prefix_save": (_I, [_VP]),
     "tts_prefix_restore": (_I, [_VP]),
     "tts_set_kv": (_I, [_VP, _VP, _VP, _I, _I]),
@@ -275,6 +276,14 @@ class Decoder:
         """tts_set_sampling: 0 = greedy argmax; > 0 = seeded categorical draws
         from softmax(logits / temperature)."""
         _call("tts_set_sampling", self._ctx, float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF)
+
+    def decode_until_eoc(self, max_frames: int) -> np.ndarray:
+        """tts_decode_until_eoc: free-running frames with one frame of
+        lookahead until the last codebook's EOC; returns the codes [n][n_cb]."""
+        out = np.empty((max_frames, self.dims.n_cb), np.int32)
+        n = ctypes.c_int()
+        _call("tts_decode_until_eoc", self._ctx, max_frames, _ptr(out), ctypes.byref(n))
+        return out[:n.value]
 
     def prefix_save(self):
         """tts_prefix_save: snapshot the cache rows [0, pos) and the state."""

@@ -73,6 +73,10 @@ struct tts_ctx {
     cudaGraphExec_t step_exec = nullptr;     // one decode step
     cudaGraphExec_t prefill_exec = nullptr;  // one prefill position (no head)
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    // lookahead loop (tts_decode_until_eoc): double-buffered pinned copies of
+    // the state after each frame, and the events that mark them
+    DevState* h_ring = nullptr;
+    cudaEvent_t ev_ring[2] = {nullptr, nullptr};
     float last_ms = 0.f;
     int pos = 0;  // host shadow of st->pos
 
@@ -402,6 +406,7 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     TTS_CK(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking));
     TTS_CK(cudaEventCreate(&c->ev0));
     TTS_CK(cudaEventCreate(&c->ev1));
+    for (auto& e : c->ev_ring) TTS_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
 
     c->embed = static_cast<const __nv_bfloat16*>(w->embed);
     c->head = static_cast<const __nv_bfloat16*>(w->head);
@@ -441,6 +446,7 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     TTS_CK(cudaMemsetAsync(c->logits, 0, (size_t)k.n_codebooks * k.cb_vocab * sizeof(float), c->stream));
     TTS_CK(cudaHostAlloc((void**)&c->h_in, sizeof(DevState), cudaHostAllocDefault));
     TTS_CK(cudaHostAlloc((void**)&c->h_out, sizeof(DevState), cudaHostAllocDefault));
+    TTS_CK(cudaHostAlloc((void**)&c->h_ring, 2 * sizeof(DevState), cudaHostAllocDefault));
 
     // RoPE table: inverse frequencies theta^(-2i/D), angle pos * inv_f in fp64,
     // cos/sin rounded to fp32.
@@ -547,6 +553,9 @@ void destroy(tts_ctx* c) {
     if (c->pre_v) cudaFree(c->pre_v);
     if (c->h_in) cudaFreeHost(c->h_in);
     if (c->h_out) cudaFreeHost(c->h_out);
+    if (c->h_ring) cudaFreeHost(c->h_ring);
+    for (auto& e : c->ev_ring)
+        if (e) cudaEventDestroy(e);
     if (c->ev0) cudaEventDestroy(c->ev0);
     if (c->ev1) cudaEventDestroy(c->ev1);
     if (c->cap) cudaStreamDestroy(c->cap);
@@ -657,6 +666,49 @@ int tts_prefill(tts_ctx* ctx, const int32_t* codes, int P) {
     DevState after = *ctx->h_out;
     for (int i = 0; i < kMaxCodebooks; ++i) after.codes[i] = k.cb_vocab - 2;  // next input: all-BOS frame
     return push_state(ctx, after);
+}
+
+int tts_decode_until_eoc(tts_ctx* ctx, int max_frames, int32_t* codes_out, int* n_frames) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (max_frames < 0 || !n_frames) return TTS_ERR_ARG;
+    const tts_config& k = ctx->cfg;
+    *n_frames = 0;
+    const int room = k.max_pos - ctx->pos;  // frames that fit the cache
+    if (max_frames > room) max_frames = room;
+    if (max_frames == 0) return room == 0 ? TTS_ERR_FULL : TTS_OK;
+    // queue frame f: one graph replay, then the state it leaves into ring slot f & 1
+    auto queue = [&](int f) -> int {
+        TTS_CK(cudaGraphLaunch(ctx->step_exec, ctx->stream));
+        TTS_CK(cudaMemcpyAsync(ctx->h_ring + (f & 1), ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost,
+                               ctx->stream));
+        TTS_CK(cudaEventRecord(ctx->ev_ring[f & 1], ctx->stream));
+        return TTS_OK;
+    };
+    TTS_TRY(queue(0));
+    int rc = TTS_OK;
+    for (int f = 0; f < max_frames; ++f) {
+        const bool ahead = f + 1 < max_frames;
+        if (ahead) TTS_TRY(queue(f + 1));  // the GPU runs frame f + 1 while the host reads frame f
+        TTS_CK(cudaEventSynchronize(ctx->ev_ring[f & 1]));
+        const DevState s = ctx->h_ring[f & 1];  // read before slot f & 1 is queued again
+        if (s.err) {
+            rc = TTS_ERR_DEVICE;
+            break;
+        }
+        if (codes_out) std::memcpy(codes_out + (size_t)f * k.n_codebooks, s.codes, sizeof(int32_t) * k.n_codebooks);
+        *n_frames = f + 1;
+        // stop once the last codebook has emitted EOC (delay pattern: frame eoc + n_cb - 1)
+        const int frame = s.t - 1;
+        if (s.eoc >= 0 && frame >= s.eoc + k.n_codebooks - 1) {
+            if (ahead) {  // undo the frame queued past the stop: back to the state after frame f
+                TTS_CK(cudaStreamSynchronize(ctx->stream));
+                return push_state(ctx, s);
+            }
+            break;
+        }
+    }
+    const int prc = pull_state(ctx);
+    return rc != TTS_OK ? rc : prc;
 }
 
 int tts_rewind(tts_ctx* ctx, int pos, int t) {

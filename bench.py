@@ -370,6 +370,16 @@ def run_gpu(args, wl_name, wl):
     te1 = time.perf_counter()
     e2e_fps = world * n_e2e / (te1 - te0)
 
+    # the same frames through the lookahead loop (tts_decode_until_eoc): the
+    # device feeds codes back, the host reads each frame's state one frame behind
+    dec.rewind(ctx0, 0)
+    n_la = min(args.steps, seg)
+    torch.cuda.synchronize()
+    tl0 = time.perf_counter()
+    la = dec.decode_until_eoc(n_la)
+    tl1 = time.perf_counter()
+    lookahead_fps = world * la.shape[0] / (tl1 - tl0)
+
     # batched prompt prefill (tensor-core path) at P = 512, same weights: the
     # median of timed prefills after warm-up, with CUDA events
     prefill_512 = None
@@ -423,7 +433,10 @@ def run_gpu(args, wl_name, wl):
         "roofline": roofline,
         "clocks": clock_info,
         "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 4 * d.n_cb,
-                "d2h_bytes_per_step": 64, "frames": n_e2e},
+                "d2h_bytes_per_step": 128, "frames": n_e2e},
+        "e2e_lookahead": {"value": lookahead_fps, "unit": "frames/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 128, "frames": int(la.shape[0]),
+                          "api": "tts_decode_until_eoc (codes fed back on the device, state read one frame behind)"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu_baseline,
         "prefill_ms": prefill_ms,

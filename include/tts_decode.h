@@ -141,6 +141,22 @@ int tts_decode_step(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes_out);
  * TTS_ERR_FULL if pos+n > max_pos.  Synchronises the stream. */
 int tts_decode_steps(tts_ctx* ctx, int n, int32_t* codes_out);
 
+/* Free-running decode with a one-frame lookahead (the pages' zero-sync host
+ * loop: "Higgs Audio v3 TTS-4B on FlashRT", section 4 and the SGLang-Omni
+ * post's AR backbone loop).  Frame f + 1 is queued on the GPU before the host
+ * reads frame f's codes, which arrive by an asynchronous copy of the state
+ * into a double-buffered pinned ring, so the GPU never waits on the host
+ * between frames.  Stops after max_frames frames, at the end of the cache, or
+ * after the frame in which the last codebook emits EOC (frame eoc +
+ * n_codebooks - 1 of the delay pattern); a frame queued past the stop is
+ * undone (the state returns to the one after the last reported frame; the
+ * cache row it wrote lies past that position).  The first frame's input is
+ * the device-resident codes, as in tts_decode_steps.  codes_out: HOST int32
+ * [max_frames][n_codebooks] (may be NULL); *n_frames: frames produced.
+ * Errors: TTS_ERR_FULL if the cache is already full, TTS_ERR_DEVICE if a
+ * kernel recorded a failure (the frames before it are reported). */
+int tts_decode_until_eoc(tts_ctx* ctx, int max_frames, int32_t* codes_out, int* n_frames);
+
 /* Rewind to position pos (0 <= pos <= current position) and frame t, with no
  * EOC: cache positions [0, pos) are kept and later ones are overwritten as
  * decoding proceeds, so a prompt prefilled once can start many utterances
