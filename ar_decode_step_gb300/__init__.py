@@ -60,6 +60,8 @@ SIGNATURES = {
     "tts_set_sampling": (_I, [_VP, ctypes.c_float, ctypes.c_ulonglong]),
     "tts_decode_until_eoc": (_I, [_VP, _I, _VP, _VP]),
     "tts_prefix_save": (_I, [_VP]),
+    "tts_set_fp8_scales": (_I, [_VP, _VP]),
+    "tts_fp8_calibrate": (_I, [_VP, _I, _VP]),
     "tts_prefix_restore": (_I, [_VP]),
     "tts_set_kv": (_I, [_VP, _VP, _VP, _I, _I]),
     "tts_get_kv": (_I, [_VP, _VP, _VP, _I, _I]),
@@ -284,6 +286,22 @@ class Decoder:
         n = ctypes.c_int()
         _call("tts_decode_until_eoc", self._ctx, max_frames, _ptr(out), ctypes.byref(n))
         return out[:n.value]
+
+    def set_fp8_scales(self, scales=None):
+        """tts_set_fp8_scales: static activation scales [n_layers][4] (0 =
+        dynamic for that site), or None for all dynamic."""
+        if scales is None:
+            _call("tts_set_fp8_scales", self._ctx, None)
+            return
+        a = np.ascontiguousarray(scales, np.float32).reshape(self.dims.n_layers, 4)
+        _call("tts_set_fp8_scales", self._ctx, _ptr(a))
+
+    def fp8_calibrate(self, n_frames: int) -> np.ndarray:
+        """tts_fp8_calibrate: per-site amax [n_layers][4] over n_frames
+        discarded free-running frames."""
+        out = np.zeros((self.dims.n_layers, 4), np.float32)
+        _call("tts_fp8_calibrate", self._ctx, n_frames, _ptr(out))
+        return out
 
     def prefix_save(self):
         """tts_prefix_save: snapshot the cache rows [0, pos) and the state."""

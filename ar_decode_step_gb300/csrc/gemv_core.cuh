@@ -373,6 +373,11 @@ struct XStats {
     const float2* h;   // per producing CTA: {sum of squares, max |h * gamma_next|} (RMSNorm inputs)
     const float* mx;   // per producing unit: max |x| (plain FP8 inputs)
     int n;             // entries
+    // FP8 only, both optional: this site's static activation scale (used when
+    // > 0 instead of the per-token amax / 448), and an amax accumulator that
+    // calibration runs raise to the largest amax seen
+    const float* sa_static = nullptr;
+    float* calib = nullptr;
 };
 
 // Stage an activation vector whose statistics the producing phase published,
@@ -440,6 +445,12 @@ __device__ __forceinline__ float stage_x_stats(const float* x, const __nv_bfloat
             am = warp_max(am);
             if constexpr (RMS) am *= r;
             sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+            // non-negative floats order like their bit patterns
+            if (st.calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(st.calib), __float_as_int(am));
+            if (st.sa_static) {
+                const float ss_ = __ldcg(st.sa_static);
+                if (ss_ > 0.f) sa = ss_;  // static: values beyond 448 * sa saturate
+            }
         }
     }
     for (int base = 0; base < n4; base += kB * kConsumers) {

@@ -180,6 +180,11 @@ struct StepParams {
     int ns, slot_bytes, xs_bytes, part_bytes;
     int pf_stages;  // how many stages the L2 prefetch runs ahead of the ring copies
     int pf_max;     // ... and how far it may run ahead while the ring is full
+    // FP8: static activation scales [n_layers][4] (QKV, O, gate/up, down
+    // inputs; a site <= 0 is dynamic), and the calibration accumulators
+    // (same layout; null outside calibration runs)
+    const float* fp8_sa;
+    float* fp8_calib;
     // optional phase trace: per CTA, trace_stride globaltimer stamps (ns)
     unsigned long long* trace;
     int trace_stride;

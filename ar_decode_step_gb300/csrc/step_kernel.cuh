@@ -346,6 +346,9 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
     const Proj j = step_proj(p, m.sl, cs, KIND, l, FP8);
     const int ev = 1 + 14 * l + (KIND == 0 ? 0 : KIND == 1 ? 5 : KIND == 2 ? 8 : KIND == 3 ? 11 : 0);
     const int A = p.n_q * kHeadDim;
+    // FP8 activation site of this projection: static scale and calibration
+    const float* site_sa = FP8 && p.fp8_sa ? p.fp8_sa + 4 * l + KIND : nullptr;
+    float* site_cal = FP8 && p.fp8_calib ? p.fp8_calib + 4 * l + KIND : nullptr;
     float sa;
     if constexpr (KIND == 0) {
         // warm L2 with the cache rows this CTA's attention unit of this layer will read
@@ -358,19 +361,20 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
                 prefetch_l2_bulk(p.vc + off, (uint32_t)((a1 - a0) * kHeadDim * 2));
             }
         }
-        sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_in, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},
-                                      m.xs);
+        sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_in, p.hidden, p.eps,
+                                      XStats{p.h_stats, nullptr, (int)gridDim.x, site_sa, site_cal}, m.xs);
     } else if constexpr (KIND == 1) {
         // bf16: the attention output goes straight from L2 into the lanes' registers
-        sa = FP8 ? stage_x_stats<FP8, false>(p.attn, nullptr, A, p.eps, XStats{nullptr, p.attn_mx, p.n_kv}, m.xs)
+        sa = FP8 ? stage_x_stats<FP8, false>(p.attn, nullptr, A, p.eps,
+                                             XStats{nullptr, p.attn_mx, p.n_kv, site_sa, site_cal}, m.xs)
                  : 1.0f;
     } else if constexpr (KIND == 2) {
         sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_post, p.hidden, p.eps,
-                                      XStats{p.h_stats, nullptr, (int)gridDim.x}, m.xs);
+                                      XStats{p.h_stats, nullptr, (int)gridDim.x, site_sa, site_cal}, m.xs);
     } else if constexpr (KIND == 3) {
         // bf16: the MLP activation goes straight from L2 into the lanes' registers
         sa = FP8 ? stage_x_stats<FP8, false>(p.act, nullptr, p.inter, p.eps,
-                                             XStats{nullptr, p.act_mx, (int)gridDim.x}, m.xs)
+                                             XStats{nullptr, p.act_mx, (int)gridDim.x, site_sa, site_cal}, m.xs)
                  : 1.0f;
     } else {
         sa = stage_x_stats<false, true>(p.h, p.final_norm, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},

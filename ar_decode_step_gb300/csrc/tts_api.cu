@@ -356,6 +356,14 @@ int setup_persistent(tts_ctx* c) {
     TTS_TRY(dalloc(c, &p.h_stats, (size_t)grid));
     TTS_TRY(dalloc(c, &p.attn_mx, (size_t)k.n_kv_heads));
     TTS_TRY(dalloc(c, &p.act_mx, (size_t)grid));
+    p.fp8_sa = nullptr;
+    p.fp8_calib = nullptr;
+    if (prec == kFP8) {  // static activation scales, all dynamic until set
+        float* sa = nullptr;
+        TTS_TRY(dalloc(c, &sa, (size_t)k.n_layers * 4));
+        TTS_CK(cudaMemset(sa, 0, sizeof(float) * (size_t)k.n_layers * 4));
+        p.fp8_sa = sa;
+    }
     TTS_CK(step_prepare(prec, c->G, c->step_smem));
 
     p.layers = c->d_layers;
@@ -759,6 +767,51 @@ int tts_prefix_restore(tts_ctx* ctx) {
     s.err = 0;
     s.hist_idx = 0;
     return push_state(ctx, s);
+}
+
+int tts_set_fp8_scales(tts_ctx* ctx, const float* scales) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (k.precision != TTS_FP8 || !ctx->persistent || !ctx->sp.fp8_sa) return TTS_ERR_UNSUPPORTED;
+    const size_t n = (size_t)k.n_layers * 4;
+    std::vector<float> h(n, 0.f);
+    if (scales)
+        for (size_t i = 0; i < n; ++i) {
+            if (!(scales[i] >= 0.f) || !std::isfinite(scales[i])) return TTS_ERR_ARG;
+            h[i] = scales[i];
+        }
+    TTS_CK(cudaMemcpyAsync(const_cast<float*>(ctx->sp.fp8_sa), h.data(), n * sizeof(float), cudaMemcpyHostToDevice,
+                           ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    return TTS_OK;
+}
+
+int tts_fp8_calibrate(tts_ctx* ctx, int n_frames, float* amax_out) {
+    if (!ctx) return TTS_ERR_STATE;
+    const tts_config& k = ctx->cfg;
+    if (k.precision != TTS_FP8 || !ctx->persistent) return TTS_ERR_UNSUPPORTED;
+    if (n_frames < 1 || !amax_out) return TTS_ERR_ARG;
+    if (ctx->pos + n_frames > k.max_pos) return TTS_ERR_FULL;
+    const size_t n = (size_t)k.n_layers * 4;
+    TTS_CK(cudaMemcpyAsync(ctx->h_out, ctx->st, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    const DevState saved = *ctx->h_out;
+    float* cal = nullptr;
+    TTS_CK(cudaMalloc(&cal, n * sizeof(float)));
+    cudaError_t e = cudaMemsetAsync(cal, 0, n * sizeof(float), ctx->stream);
+    StepParams p = ctx->sp;
+    p.decode = 1;
+    p.fp8_calib = cal;
+    for (int f = 0; f < n_frames && e == cudaSuccess; ++f) {
+        e = cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream);
+        if (e == cudaSuccess) e = launch_step(p, kFP8, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream);
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(amax_out, cal, n * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    cudaFree(cal);
+    if (e != cudaSuccess) return report(e, "tts_fp8_calibrate");
+    TTS_TRY(pull_state(ctx));  // reports a device error of the calibration frames
+    return push_state(ctx, saved);  // the frames are discarded: back to the state before them
 }
 
 int tts_set_kv(tts_ctx* ctx, const void* kd, const void* vd, int len, int len_stride) {

@@ -164,6 +164,27 @@ int tts_decode_until_eoc(tts_ctx* ctx, int max_frames, int32_t* codes_out, int* 
  * input is processed).  The next decode step's input is the all-BOS frame. */
 int tts_rewind(tts_ctx* ctx, int pos, int t);
 
+/* FP8 static activation scales (FlashRT page, FP8 W8A8 and section 5: the
+ * production FP8 path quantises each projection input with a per-tensor
+ * scale calibrated offline as amax / 448, instead of the per-token amax).
+ * scales: HOST fp32 [n_layers][4] for the inputs of the QKV, O, gate/up and
+ * down projections of each layer; a site set to 0 keeps the per-token
+ * (dynamic) scale; NULL makes every site dynamic again.  With a static scale
+ * s, x quantises to e4m3(x / s), values beyond 448 s saturating.  Applies to
+ * every later step.  TTS_ERR_UNSUPPORTED for BF16 contexts or without the
+ * persistent step kernel; TTS_ERR_ARG for a negative or non-finite scale. */
+int tts_set_fp8_scales(tts_ctx* ctx, const float* scales);
+
+/* FP8 calibration run: n_frames free-running decode frames from the current
+ * state (as tts_decode_steps) with the current scales, recording for every
+ * activation site the largest amax of its (normalised) input over the frames
+ * into amax_out, HOST fp32 [n_layers][4] (same order as tts_set_fp8_scales;
+ * the static scale is amax / 448).  The frames are then discarded: position,
+ * frame, EOC frame and next input are restored (cache rows at and past the
+ * position are left stale).  Errors as tts_set_fp8_scales, TTS_ERR_FULL if
+ * the frames do not fit the cache. */
+int tts_fp8_calibrate(tts_ctx* ctx, int n_frames, float* amax_out);
+
 /* Prefix reuse (FlashRT page, section 4 and Performance "prompt prefill": a
  * resident system prompt's KV is kept and each request prefills only its own
  * suffix, bit-identically).  tts_prefix_save snapshots cache positions

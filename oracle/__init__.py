@@ -46,12 +46,13 @@ _PP = ctypes.POINTER(ctypes.c_void_p)
 class _Weights(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("head", ctypes.c_void_p), ("final_norm", ctypes.c_void_p)] + \
                [(n, _PP) for n in ("wqkv", "wo", "wgu", "wd", "qqkv", "qo", "qgu", "qd",
-                                   "sqkv", "so", "sgu", "sd", "ln_in", "ln_post", "q_norm", "k_norm")]
+                                   "sqkv", "so", "sgu", "sd", "ln_in", "ln_post", "q_norm", "k_norm")] + \
+               [("act_scales", ctypes.c_void_p)]
 
 
 class _State(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("pos", ctypes.c_int),
-                ("t", ctypes.c_int), ("eoc", ctypes.c_int)]
+                ("t", ctypes.c_int), ("eoc", ctypes.c_int), ("amax_acc", ctypes.c_void_p)]
 
 
 def lib():
@@ -70,6 +71,7 @@ def lib():
                 "or_rmsnorm": (None, [vp, vp, i32, dbl, vp]),
                 "or_linear_bf16": (None, [vp, i32, i32, vp, vp]),
                 "or_quant_act": (None, [vp, i32, vp, vp]),
+                "or_quant_act_static": (None, [vp, i32, flt, vp]),
                 "or_linear_fp8": (None, [vp, vp, i32, i32, vp, flt, vp]),
                 "or_quant_weight": (None, [vp, i32, i32, vp, vp]),
                 "or_rope": (None, [vp, i32, i32, dbl]),
@@ -146,6 +148,13 @@ def quant_act(x: np.ndarray):
     s = ctypes.c_float()
     lib().or_quant_act(_p(x), x.size, _p(q), ctypes.addressof(s))
     return q, s.value
+
+
+def quant_act_static(x: np.ndarray, scale: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float64)
+    q = np.empty(x.size, np.uint8)
+    lib().or_quant_act_static(_p(x), x.size, float(scale), _p(q))
+    return q
 
 
 def linear_fp8(W8: np.ndarray, sw: np.ndarray, a8: np.ndarray, sa: float) -> np.ndarray:
@@ -262,7 +271,9 @@ class Oracle:
         shape = (L, d.n_kv, max_pos, d.head_dim)
         self.k = np.zeros(shape, np.uint16)
         self.v = np.zeros(shape, np.uint16)
-        self.st = _State(_p(self.k), _p(self.v), 0, 0, -1)
+        self.st = _State(_p(self.k), _p(self.v), 0, 0, -1, None)
+        self._scales = None
+        self._amax = None
 
     # state
     @property
@@ -271,6 +282,26 @@ class Oracle:
 
     def reset(self):
         self.st.pos, self.st.t, self.st.eoc = 0, 0, -1
+
+    def set_fp8_scales(self, scales=None):
+        """Static activation scales [n_layers][4] (precision 1; 0 = per-token
+        for that site), or None for per-token everywhere."""
+        if scales is None:
+            self._scales = None
+            self.cw.act_scales = None
+        else:
+            self._scales = np.ascontiguousarray(scales, np.float32).reshape(self.dims.n_layers, 4)
+            self.cw.act_scales = _p(self._scales)
+
+    def start_calibration(self):
+        """Record the largest input amax of every activation site from now on."""
+        self._amax = np.zeros((self.dims.n_layers, 4), np.float32)
+        self.st.amax_acc = _p(self._amax)
+
+    def stop_calibration(self) -> np.ndarray:
+        self.st.amax_acc = None
+        a, self._amax = self._amax, None
+        return a
 
     def set_frame(self, t: int, eoc: int = -1):
         self.st.t, self.st.eoc = t, eoc

@@ -143,6 +143,35 @@ void or_quant_act(const double* x, int n, uint8_t* q, float* scale) {
     *scale = s;
 }
 
+/* Static activation scale [FlashRT perf "FP8 W8A8", s5 "quantize_fp8_static":
+ * a per-tensor scale calibrated offline as amax / 448]: the same fp32
+ * division and saturating encode as the per-token path, scale given. */
+void or_quant_act_static(const double* x, int n, float scale, uint8_t* q) {
+    for (int i = 0; i < n; ++i) q[i] = or_e4m3_encode((float)x[i] / scale);
+}
+
+/* One FP8 activation site (layer l, site 0..3 = QKV, O, gate/up, down input):
+ * records the input's amax for calibration runs, then quantises with the
+ * site's static scale if one is set, else per token. */
+static void quant_site(const or_weights* w, or_state* st, int l, int site, const double* x, int n, uint8_t* q,
+                       float* scale) {
+    if (st->amax_acc) {
+        float amax = 0.0f;
+        for (int i = 0; i < n; ++i) {
+            const float a = fabsf((float)x[i]);
+            if (a > amax) amax = a;
+        }
+        if (amax > st->amax_acc[4 * l + site]) st->amax_acc[4 * l + site] = amax;
+    }
+    const float s = w->act_scales ? w->act_scales[4 * l + site] : 0.0f;
+    if (s > 0.0f) {
+        or_quant_act_static(x, n, s, q);
+        *scale = s;
+    } else {
+        or_quant_act(x, n, q, scale);
+    }
+}
+
 /* FP8 W8A8 projection [FlashRT perf "FP8 W8A8"; FlashRT s5 "M=1 FP8 GEMV"]:
  * acc = sum_k w8[n][k] * a8[k] (exact in fp64: every e4m3 product has at most
  * 8 significant bits and the exponent span fits in 53 bits), then the output
@@ -348,7 +377,7 @@ static void stack_layers(const or_dims* d, const or_weights* w, or_state* st, in
         or_rmsnorm(h, w->ln_in[l], H, d->rms_eps, a);
         if (fp8) {
             float s;
-            or_quant_act(a, H, q8, &s);
+            quant_site(w, st, l, 0, a, H, q8, &s);
             or_linear_fp8(w->qqkv[l], w->sqkv[l], QKV, H, q8, s, qkv);
         } else {
             if (a16) for (int i = 0; i < H; ++i) a[i] = round_bf16(a[i]);
@@ -380,7 +409,7 @@ static void stack_layers(const or_dims* d, const or_weights* w, or_state* st, in
         /* output projection with the residual add h += W_o attn */
         if (fp8) {
             float s;
-            or_quant_act(attn, A, q8, &s);
+            quant_site(w, st, l, 1, attn, A, q8, &s);
             or_linear_fp8(w->qo[l], w->so[l], H, A, q8, s, o);
         } else {
             if (a16) for (int i = 0; i < A; ++i) attn[i] = round_bf16(attn[i]);
@@ -392,7 +421,7 @@ static void stack_layers(const or_dims* d, const or_weights* w, or_state* st, in
         or_rmsnorm(h, w->ln_post[l], H, d->rms_eps, a);
         if (fp8) {
             float s;
-            or_quant_act(a, H, q8, &s);
+            quant_site(w, st, l, 2, a, H, q8, &s);
             or_linear_fp8(w->qgu[l], w->sgu[l], 2 * I, H, q8, s, gu);
             for (int i = 0; i < I; ++i) m[i] = round_bf16(or_silu(gu[i]) * gu[I + i]);
         } else {
@@ -404,7 +433,7 @@ static void stack_layers(const or_dims* d, const or_weights* w, or_state* st, in
         /* down projection with the residual add h += W_d m */
         if (fp8) {
             float s;
-            or_quant_act(m, I, q8, &s);
+            quant_site(w, st, l, 3, m, I, q8, &s);
             or_linear_fp8(w->qd[l], w->sd[l], H, I, q8, s, o);
         } else {
             if (a16) for (int i = 0; i < I; ++i) m[i] = round_bf16(m[i]);

@@ -54,6 +54,8 @@ typedef struct {
     const uint16_t* const* ln_post; /* bf16 [hidden] */
     const uint16_t* const* q_norm;  /* bf16 [D] */
     const uint16_t* const* k_norm;  /* bf16 [D] */
+    const float* act_scales;        /* precision 1, optional: static activation scales [n_layers][4]
+                                       (QKV, O, gate/up, down inputs; a site <= 0, or NULL: per-token) */
 } or_weights;
 
 typedef struct {
@@ -62,6 +64,8 @@ typedef struct {
     int pos;       /* next position to write */
     int t;         /* decode frame index since the last reset */
     int eoc;       /* frame at which codebook 0 first emitted EOC, -1 if none */
+    float* amax_acc; /* precision 1, optional: [n_layers][4] raised to the largest input amax seen
+                        at each activation site (calibration) */
 } or_state;
 
 /* ---- scalar formats ---- */
@@ -75,6 +79,9 @@ uint8_t  or_e4m3_encode(float x);           /* nearest even, saturating to +-448
 void   or_rmsnorm(const double* x, const uint16_t* gamma, int n, double eps, double* y);
 void   or_linear_bf16(const uint16_t* W, int N, int K, const double* x, double* y);
 void   or_quant_act(const double* x, int n, uint8_t* q, float* scale);
+/* FP8 quantisation with a given (static, calibrated) scale: q = e4m3(x / scale)
+ * in fp32, saturating beyond +-448. */
+void   or_quant_act_static(const double* x, int n, float scale, uint8_t* q);
 void   or_linear_fp8(const uint8_t* W8, const float* sw, int N, int K,
                      const uint8_t* a8, float sa, double* y);
 void   or_quant_weight(const uint16_t* W, int N, int K, uint8_t* W8, float* sw);
