@@ -74,6 +74,7 @@ SIGNATURES = {
     "tts_trace_step": (_I, [_VP, _VP, _I, _VP, _VP]),
     "tts_debug_layer_states": (_I, [_VP, _VP, _VP, _VP, _I]),
     "tts_gemm_bf16": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tts_gemm_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "tts_debug_prefill_states": (_I, [_VP, _VP, _I, _VP, ctypes.c_longlong]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -136,6 +137,16 @@ def gemm_bf16(a_dev, b_dev, c_dev, epi: int = 0, splits: int = 1, stream=None):
     M, K = a_dev.shape
     N = c_dev.shape[1]
     _call("tts_gemm_bf16", a_dev.data_ptr(), b_dev.data_ptr(), c_dev.data_ptr(), M, N, K, epi, splits, stream)
+
+
+def gemm_fp8(a8_dev, b8_dev, a_scale_dev, b_scale_dev, c_dev, epi: int = 0, stream=None):
+    """tts_gemm_fp8: a8_dev [M][K] and b8_dev [N][K] (epi 2: [2N][K]) uint8
+    E4M3 CUDA tensors with fp32 scales [M] and [N] (epi 2: [2N]); c_dev fp32
+    [M][N] (epi 0, 1) or bf16 [M][N] (epi 2)."""
+    M, K = a8_dev.shape
+    N = c_dev.shape[1]
+    _call("tts_gemm_fp8", a8_dev.data_ptr(), b8_dev.data_ptr(), a_scale_dev.data_ptr(), b_scale_dev.data_ptr(),
+          c_dev.data_ptr(), M, N, K, epi, stream)
 
 
 def quantize_fp8_weight(w_dev, stream=None):

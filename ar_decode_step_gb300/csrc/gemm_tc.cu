@@ -114,10 +114,30 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <int EPI, int MMA_N>
+// kind::f8f6f4 with E4M3 A and B (type code 0), fp32 D; same field layout
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ float round_bf16f(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// F8: E4M3 operands; a k-block is then 128 elements (still one 128-byte
+// swizzle row), an MMA takes K = 32 (still 32 bytes), and every accumulator
+// is scaled by its row's and column's scales and rounded to bf16 before the
+// epilogue's operation.
+template <int EPI, int MMA_N, bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams p) {
+    constexpr int kBKE = F8 ? 2 * kBK : kBK;  // elements per k-block
     extern __shared__ unsigned char smem_raw[];
     constexpr int kStages = gemm_stages<MMA_N>();
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
@@ -138,7 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nt = EPI == kGemmSwiglu ? MMA_N / 2 : MMA_N;  // output columns of this tile
     const int n0 = blockIdx.y * nt;
     const int kb0 = blockIdx.z * p.kb_per_split;
-    const int kb1 = min(p.K / kBK, kb0 + p.kb_per_split);
+    const int kb1 = min(p.K / kBKE, kb0 + p.kb_per_split);
     const int nkb = kb1 - kb0;
 
     if (threadIdx.x == 0) {
@@ -168,7 +188,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             unsigned char* st = smem + (size_t)s * kStageBytes;
             mbar_arrive_expect_tx(&full[s], kStageBytes);
-            const int kx = (kb0 + i) * kBK;
+            const int kx = (kb0 + i) * kBKE;
             tma_load_2d(st, &tmA, kx, m0, &full[s]);
             if constexpr (EPI == kGemmSwiglu) {
                 tma_load_2d(st + kATileBytes, &tmB, kx, n0, &full[s]);                     // gate rows
@@ -182,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
       if (lane == 0) {
         // MMA issuer
-        constexpr uint32_t idesc = idesc_bf16(kBM, MMA_N);
+        constexpr uint32_t idesc = F8 ? idesc_e4m3(kBM, MMA_N) : idesc_bf16(kBM, MMA_N);
         int i = 0;
         for (; i < nkb; ++i) {
             const int s = i % kStages;
@@ -195,8 +215,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t ad = smem_desc_sw128(st);
             const uint64_t bd = smem_desc_sw128(st + kATileBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)  // 16 bf16 = 32 bytes = +2 in the address field
-                tc_mma(tmem_d, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {  // 32 bytes per MMA (16 bf16 or 32 E4M3) = +2 in the address field
+                if constexpr (F8) tc_mma_f8(tmem_d, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                else tc_mma(tmem_d, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            }
             tc_commit(&empty[s]);
         }
         tc_commit(&done);  // after every MMA issued above (also on failure: lets them drain)
@@ -211,12 +233,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (ok && !s_fail && nkb > 0) {
         const int row = m0 + warp * 32 + lane;
         const uint32_t tbase = tmem_d + ((uint32_t)(warp * 32) << 16);
+        const float sa = F8 && row < p.M ? __ldg(p.a_scale + row) : 1.0f;
         for (int c = 0; c < nt; c += 16) {
             float v[16];
             tmem_ld16(tbase + c, v);
+            if constexpr (F8) {  // the FP8 projection output: bf16(acc * (s_a * s_w[n]))
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = round_bf16f(v[e] * (sa * __ldg(p.b_scale + n0 + c + e)));
+            }
             if constexpr (EPI == kGemmSwiglu) {
                 float u[16];
                 tmem_ld16(tbase + nt + c, u);
+                if constexpr (F8) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        u[e] = round_bf16f(u[e] * (sa * __ldg(p.b_scale + p.n_half + n0 + c + e)));
+                }
                 if (row < p.M) {
                     __nv_bfloat16* dst = p.out_bf16 + (size_t)row * p.ldc + n0 + c;
 #pragma unroll
@@ -275,14 +307,16 @@ EncodeTiledFn encode_fn() {
 
 // 2-D bf16 [rows][K] row-major tensor, box of box_rows x 64, 128-byte swizzle;
 // rows past `rows` read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows, bool e4m3 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const int esz = e4m3 ? 1 : 2;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * esz};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};  // one 128-byte row per box row
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    return fn(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+              dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -292,17 +326,17 @@ constexpr int gemm_smem_bytes() {
     return gemm_stages<MMA_N>() * (int)(kATileBytes + MMA_N * kBK * 2) + 1024;
 }
 
-template <int EPI, int MMA_N>
+template <int EPI, int MMA_N, bool F8 = false>
 cudaError_t launch_t(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, dim3 grid, cudaStream_t s) {
     constexpr int smem = gemm_smem_bytes<EPI, MMA_N>();
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<EPI, MMA_N>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<EPI, MMA_N, F8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    gemm_bf16_kernel<EPI, MMA_N><<<grid, kGemmThreads, smem, s>>>(a, b, p);
+    gemm_bf16_kernel<EPI, MMA_N, F8><<<grid, kGemmThreads, smem, s>>>(a, b, p);
     return cudaGetLastError();
 }
 
@@ -330,6 +364,36 @@ int gemm_pick_bn(int M, int N, int epi, int num_sms) {
         }
     }
     return best ? best : 128;
+}
+
+bool gemm_shape_ok_fp8(int M, int N, int K, int epi, int bn) {
+    return gemm_shape_ok(M, N, K, epi, bn) && K % (2 * kBK) == 0;
+}
+
+cudaError_t launch_gemm_fp8(const void* A8, const void* B8, const GemmParams& p_in, int epi, cudaStream_t s) {
+    GemmParams p = p_in;
+    if (p.bn == 0) p.bn = 128;
+    if (!gemm_shape_ok_fp8(p.M, p.N, p.K, epi, p.bn) || !p.a_scale || !p.b_scale) return cudaErrorInvalidValue;
+    p.kb_per_split = p.K / (2 * kBK);  // no split-K: one writer per element
+    p.atomic = 0;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A8, p.M, p.K, kBM, true)) return cudaErrorInvalidValue;
+    const dim3 grid((p.M + kBM - 1) / kBM, p.N / p.bn, 1);
+    if (epi == kGemmSwiglu) {
+        if (!make_map(&mb, B8, 2 * p.n_half, p.K, 128, true)) return cudaErrorInvalidValue;
+        return launch_t<kGemmSwiglu, 256, true>(ma, mb, p, grid, s);
+    }
+    if (!make_map(&mb, B8, p.N, p.K, p.bn, true)) return cudaErrorInvalidValue;
+#define TTS_GEMM_BN8(EP)                                                     \
+    switch (p.bn) {                                                          \
+        case 64: return launch_t<EP, 64, true>(ma, mb, p, grid, s);          \
+        case 80: return launch_t<EP, 80, true>(ma, mb, p, grid, s);          \
+        case 192: return launch_t<EP, 192, true>(ma, mb, p, grid, s);        \
+        default: return launch_t<EP, 128, true>(ma, mb, p, grid, s);         \
+    }
+    if (epi == kGemmStore) TTS_GEMM_BN8(kGemmStore)
+    TTS_GEMM_BN8(kGemmAdd)
+#undef TTS_GEMM_BN8
 }
 
 cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p_in, int epi, int splits,
@@ -392,6 +456,39 @@ extern "C" int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N
     const cudaError_t e = launch_gemm_bf16(A, B, p, epi, splits, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         std::fprintf(stderr, "tts: tts_gemm_bf16 failed: %s\n", cudaGetErrorString(e));
+        return TTS_ERR_CUDA;
+    }
+    return TTS_OK;
+}
+
+extern "C" int tts_gemm_fp8(const void* A8, const void* B8, const float* a_scale, const float* b_scale, void* C, int M,
+                            int N, int K, int epi, void* stream) {
+    using namespace tts;
+    if (!A8 || !B8 || !a_scale || !b_scale || !C || epi < kGemmStore || epi > kGemmSwiglu) return TTS_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(A8) | reinterpret_cast<uintptr_t>(B8) | reinterpret_cast<uintptr_t>(C)) & 15)
+        return TTS_ERR_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TTS_ERR_CUDA;
+    const int bn = gemm_pick_bn(M, N, epi, sms);
+    if (!gemm_shape_ok_fp8(M, N, K, epi, bn)) return TTS_ERR_ARG;
+    GemmParams p{};
+    p.bn = bn;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.ldc = N;
+    p.a_scale = a_scale;
+    p.b_scale = b_scale;
+    if (epi == kGemmSwiglu) {
+        p.n_half = N;
+        p.out_bf16 = static_cast<__nv_bfloat16*>(C);
+    } else {
+        p.C = static_cast<float*>(C);
+    }
+    const cudaError_t e = launch_gemm_fp8(A8, B8, p, epi, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "tts: tts_gemm_fp8 failed: %s\n", cudaGetErrorString(e));
         return TTS_ERR_CUDA;
     }
     return TTS_OK;

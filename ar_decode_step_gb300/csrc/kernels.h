@@ -231,15 +231,27 @@ struct GemmParams {
     int kb_per_split;  // filled in by launch_gemm_bf16
     int atomic;        // filled in: split-K partials are added atomically
     int* err;          // error word (kErrTimeout on an expired wait), may be NULL
+    // E4M3 operands (launch_gemm_fp8): per-row activation scales [M] and
+    // per-row weight scales [N] (SwiGLU: [2 n_half]); every output is
+    // bf16(acc * (a_scale[m] * b_scale[n])) before the epilogue's operation
+    const float* a_scale;
+    const float* b_scale;
 };
 bool gemm_shape_ok(int M, int N, int K, int epi, int bn);
 int gemm_pick_bn(int M, int N, int epi, int num_sms);  // tile width that fills the SMs best
+bool gemm_shape_ok_fp8(int M, int N, int K, int epi, int bn);
+cudaError_t launch_gemm_fp8(const void* A8, const void* B8, const GemmParams& p, int epi, cudaStream_t s);
 cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p, int epi, int splits,
                              cudaStream_t s);
 
 // Batched prefill glue (prefill.cu): P rows at positions pos0 .. pos0+P-1.
 cudaError_t launch_prefill_embed(const __nv_bfloat16* E, const int* codes, float* H, int P, int n_cb, int V,
                                  int hidden, cudaStream_t s);
+cudaError_t launch_prefill_rmsnorm_fp8(const float* H, const __nv_bfloat16* gamma, uint8_t* out, float* scale, int P,
+                                       int hidden, float eps, cudaStream_t s);
+cudaError_t launch_prefill_quant_rows(const __nv_bfloat16* X, uint8_t* out, float* scale, int P, int n,
+                                      cudaStream_t s);
+cudaError_t launch_prefill_quant_rows_f32(const float* X, uint8_t* out, float* scale, int P, int n, cudaStream_t s);
 cudaError_t launch_prefill_rmsnorm(const float* H, const __nv_bfloat16* gamma, __nv_bfloat16* out, int P,
                                    int hidden, float eps, cudaStream_t s);
 cudaError_t launch_prefill_qk_rope_kv(const float* QKV, const __nv_bfloat16* qn, const __nv_bfloat16* kn,
@@ -247,7 +259,7 @@ cudaError_t launch_prefill_qk_rope_kv(const float* QKV, const __nv_bfloat16* qn,
                                       int P, int n_q, int n_kv, int max_pos, float eps, cudaStream_t s);
 cudaError_t launch_prefill_attention(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                                      __nv_bfloat16* out, int pos0, int P, int n_q, int n_kv, int max_pos,
-                                     cudaStream_t s);
+                                     cudaStream_t s, float* out_f32 = nullptr);
 
 // Per-row E4M3 weight quantisation.
 cudaError_t launch_quantize_weight(const __nv_bfloat16* W, int N, int K, uint8_t* W8, float* s,

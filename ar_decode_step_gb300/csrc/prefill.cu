@@ -92,6 +92,52 @@ __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const floa
     }
 }
 
+// FP8 W8A8 rows: the projection inputs quantised per row (per token) as the
+// decode step does ("Higgs Audio v3 TTS-4B on FlashRT", Performance "FP8
+// W8A8"): s = max(amax, 1e-12) / 448, q = e4m3(x / s) with IEEE fp32 division,
+// saturating.
+__device__ __forceinline__ uint8_t e4m3_sat(float x) {
+    return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// a = RMSNorm(h) * gamma, then quantised (the QKV and gate/up inputs)
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_rows_kernel(const float* H, const __nv_bfloat16* gamma,
+                                                                         uint8_t* out, float* scale, int hidden,
+                                                                         float eps) {
+    __shared__ float red[32];
+    const int p = blockIdx.x;
+    const float* h = H + (size_t)p * hidden;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x) ss += h[i] * h[i];
+    ss = block_sum(ss, red);
+    const float r = 1.0f / sqrtf(ss / (float)hidden + eps);
+    float am = 0.f;
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x)
+        am = fmaxf(am, fabsf(h[i] * r * __bfloat162float(gamma[i])));
+    am = block_max(am, red);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x)
+        out[(size_t)p * hidden + i] = e4m3_sat(__fdiv_rn(h[i] * r * __bfloat162float(gamma[i]), sa));
+    if (threadIdx.x == 0) scale[p] = sa;
+}
+
+// rows quantised as they are: the attention output (fp32) and the MLP
+// activation (bf16, already rounded as the FP8 SwiGLU defines it)
+__device__ __forceinline__ float as_f32(float v) { return v; }
+__device__ __forceinline__ float as_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(const T* X, uint8_t* out, float* scale, int n) {
+    __shared__ float red[32];
+    const int p = blockIdx.x;
+    const T* x = X + (size_t)p * n;
+    float am = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) am = fmaxf(am, fabsf(as_f32(x[i])));
+    am = block_max(am, red);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) out[(size_t)p * n + i] = e4m3_sat(__fdiv_rn(as_f32(x[i]), sa));
+    if (threadIdx.x == 0) scale[p] = sa;
+}
+
 // ---- causal GQA attention on the tensor cores --------------------------------
 // Rows [row0, row0 + 16) of the prompt against the G query heads of kv head g:
 // warp w takes query head g*G + w for the 16 rows.  Per 64-key tile,
@@ -144,7 +190,8 @@ __device__ __forceinline__ void cp_async_wait_group() {
 template <int G>
 __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, const __nv_bfloat16* kc,
                                                                const __nv_bfloat16* vc, __nv_bfloat16* out,
-                                                               int pos0, int P, int n_q, int max_pos) {
+                                                               float* out_f32, int pos0, int P, int n_q,
+                                                               int max_pos) {
     extern __shared__ __align__(16) __nv_bfloat16 kvs[];  // [2 buffers][K, V][64 keys][kMmaPad]
     const int rb = gridDim.x - 1 - blockIdx.x;             // the longest rows first
     const int g = blockIdx.y;
@@ -301,19 +348,24 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
 #pragma unroll
     for (int d = 0; d < kHeadDim / 8; ++d) {
         const int col = d * 8 + 2 * ti;
-        if (gi < nrows)
-            *reinterpret_cast<__nv_bfloat162*>(out + ((size_t)(row0 + gi) * n_q + h) * kHeadDim + col) =
-                __floats2bfloat162_rn(o[d][0] * inv0, o[d][1] * inv0);
-        if (gi + 8 < nrows)
-            *reinterpret_cast<__nv_bfloat162*>(out + ((size_t)(row0 + gi + 8) * n_q + h) * kHeadDim + col) =
-                __floats2bfloat162_rn(o[d][2] * inv1, o[d][3] * inv1);
+        const size_t i0 = ((size_t)(row0 + gi) * n_q + h) * kHeadDim + col;
+        const size_t i1 = ((size_t)(row0 + gi + 8) * n_q + h) * kHeadDim + col;
+        if (out_f32) {  // FP8 contexts: fp32, quantised per row next (as the decode step does)
+            if (gi < nrows) *reinterpret_cast<float2*>(out_f32 + i0) = make_float2(o[d][0] * inv0, o[d][1] * inv0);
+            if (gi + 8 < nrows) *reinterpret_cast<float2*>(out_f32 + i1) = make_float2(o[d][2] * inv1, o[d][3] * inv1);
+        } else {
+            if (gi < nrows)
+                *reinterpret_cast<__nv_bfloat162*>(out + i0) = __floats2bfloat162_rn(o[d][0] * inv0, o[d][1] * inv0);
+            if (gi + 8 < nrows)
+                *reinterpret_cast<__nv_bfloat162*>(out + i1) = __floats2bfloat162_rn(o[d][2] * inv1, o[d][3] * inv1);
+        }
     }
 }
 
 template <int G>
 cudaError_t launch_attention_rows_t(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
-                                    __nv_bfloat16* out, int pos0, int P, int n_q, int n_kv, int max_pos,
-                                    cudaStream_t s) {
+                                    __nv_bfloat16* out, float* out_f32, int pos0, int P, int n_q, int n_kv,
+                                    int max_pos, cudaStream_t s) {
     constexpr int smem = attention_mma_smem<G>();
     static bool attr = false;
     if (!attr) {
@@ -323,7 +375,7 @@ cudaError_t launch_attention_rows_t(const float* Q, const __nv_bfloat16* kc, con
         attr = true;
     }
     const dim3 grid((P + kMmaRows - 1) / kMmaRows, n_kv);
-    attention_mma_kernel<G><<<grid, 32 * G, smem, s>>>(Q, kc, vc, out, pos0, P, n_q, max_pos);
+    attention_mma_kernel<G><<<grid, 32 * G, smem, s>>>(Q, kc, vc, out, out_f32, pos0, P, n_q, max_pos);
     return cudaGetLastError();
 }
 
@@ -341,6 +393,22 @@ cudaError_t launch_prefill_rmsnorm(const float* H, const __nv_bfloat16* gamma, _
     return cudaGetLastError();
 }
 
+cudaError_t launch_prefill_rmsnorm_fp8(const float* H, const __nv_bfloat16* gamma, uint8_t* out, float* scale, int P,
+                                       int hidden, float eps, cudaStream_t s) {
+    rmsnorm_quant_rows_kernel<<<P, kRowThreads, 0, s>>>(H, gamma, out, scale, hidden, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_quant_rows(const __nv_bfloat16* X, uint8_t* out, float* scale, int P, int n,
+                                      cudaStream_t s) {
+    quant_rows_kernel<__nv_bfloat16><<<P, kRowThreads, 0, s>>>(X, out, scale, n);
+    return cudaGetLastError();
+}
+cudaError_t launch_prefill_quant_rows_f32(const float* X, uint8_t* out, float* scale, int P, int n, cudaStream_t s) {
+    quant_rows_kernel<float><<<P, kRowThreads, 0, s>>>(X, out, scale, n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_qk_rope_kv(const float* QKV, const __nv_bfloat16* qn, const __nv_bfloat16* kn,
                                       const float2* rope, float* Q, __nv_bfloat16* kc, __nv_bfloat16* vc, int pos0,
                                       int P, int n_q, int n_kv, int max_pos, float eps, cudaStream_t s) {
@@ -351,12 +419,12 @@ cudaError_t launch_prefill_qk_rope_kv(const float* QKV, const __nv_bfloat16* qn,
 // The G query heads of a kv head share one CTA's K/V tiles: 64 (row, head) pairs.
 cudaError_t launch_prefill_attention(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                                      __nv_bfloat16* out, int pos0, int P, int n_q, int n_kv, int max_pos,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, float* out_f32) {
     const int G = n_q / n_kv;
-    if (G == 4) return launch_attention_rows_t<4>(Q, kc, vc, out, pos0, P, n_q, n_kv, max_pos, s);
-    if (G == 8) return launch_attention_rows_t<8>(Q, kc, vc, out, pos0, P, n_q, n_kv, max_pos, s);
-    if (G == 2) return launch_attention_rows_t<2>(Q, kc, vc, out, pos0, P, n_q, n_kv, max_pos, s);
-    if (G == 1) return launch_attention_rows_t<1>(Q, kc, vc, out, pos0, P, n_q, n_kv, max_pos, s);
+    if (G == 4) return launch_attention_rows_t<4>(Q, kc, vc, out, out_f32, pos0, P, n_q, n_kv, max_pos, s);
+    if (G == 8) return launch_attention_rows_t<8>(Q, kc, vc, out, out_f32, pos0, P, n_q, n_kv, max_pos, s);
+    if (G == 2) return launch_attention_rows_t<2>(Q, kc, vc, out, out_f32, pos0, P, n_q, n_kv, max_pos, s);
+    if (G == 1) return launch_attention_rows_t<1>(Q, kc, vc, out, out_f32, pos0, P, n_q, n_kv, max_pos, s);
     return cudaErrorInvalidValue;
 }
 

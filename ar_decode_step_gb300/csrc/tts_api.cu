@@ -81,7 +81,8 @@ struct tts_ctx {
     int pos = 0;  // host shadow of st->pos
 
     // batched prefill scratch (allocated on first use, kPrefillChunk rows)
-    float *pf_h = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
+    float *pf_h = nullptr, *pf_qkv = nullptr, *pf_q = nullptr, *pf_sa = nullptr, *pf_attn_f = nullptr;
+    uint8_t* pf_a8 = nullptr;  // FP8 prefill: the quantised projection input rows
     __nv_bfloat16 *pf_a = nullptr, *pf_attn = nullptr, *pf_m = nullptr;
     bool batched_prefill = true;
 };
@@ -493,16 +494,58 @@ constexpr int kPrefillChunk = 512;  // rows per batched pass (the prompt is spli
 bool batched_prefill_ok(const tts_ctx* c) {
     const tts_config& k = c->cfg;
     const int G = k.n_q_heads / k.n_kv_heads;
-    return c->batched_prefill && k.precision == TTS_BF16 && k.head_dim == kHeadDim &&
-           gemm_shape_ok(1, c->qkv_rows, k.hidden, kGemmStore, 64) &&
-           gemm_shape_ok(1, k.hidden, c->attn_dim, kGemmAdd, 64) &&
-           gemm_shape_ok(1, k.inter, k.hidden, kGemmSwiglu, 128) && gemm_shape_ok(1, k.hidden, k.inter, kGemmAdd, 64) &&
-           (G == 1 || G == 2 || G == 4 || G == 8);
+    auto ok = k.precision == TTS_FP8 ? gemm_shape_ok_fp8 : gemm_shape_ok;
+    return c->batched_prefill && k.head_dim == kHeadDim && ok(1, c->qkv_rows, k.hidden, kGemmStore, 64) &&
+           ok(1, k.hidden, c->attn_dim, kGemmAdd, 64) && ok(1, k.inter, k.hidden, kGemmSwiglu, 128) &&
+           ok(1, k.hidden, k.inter, kGemmAdd, 64) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
 // P rows (codes already on the device at c->prompt) through every layer at
 // positions pos0 .. pos0+P-1: W16A16 tensor-core GEMMs, fp32 residual stream,
 // bf16 K/V written to the cache.  P <= kPrefillChunk.
+// The batched prefill of an FP8 context: the same layer as prefill_chunk with
+// W8A8 projections (per-token activation scales, per-row weight scales, bf16
+// projection outputs; the SwiGLU of the bf16-rounded gate and up, rounded to
+// bf16 before its own quantisation), as the FP8 decode step computes them.
+int prefill_chunk_fp8(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap) {
+    const tts_config& k = c->cfg;
+    const int H = k.hidden, I = k.inter, A = c->attn_dim, QD = c->qkv_rows;
+    cudaStream_t s = c->stream;
+    int* err = &c->st->err;
+    TTS_CK(launch_prefill_embed(c->embed, d_codes, c->pf_h, P, k.n_codebooks, k.cb_vocab, H, s));
+    const size_t rows_bytes = sizeof(float) * (size_t)P * H;
+    if (snap) TTS_CK(cudaMemcpyAsync(snap, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
+    for (int l = 0; l < k.n_layers; ++l) {
+        const LayerW& w = c->L[l];
+        const size_t coff = (size_t)l * k.n_kv_heads * k.max_pos * kHeadDim;
+        GemmParams g{};
+        g.M = P; g.err = err; g.a_scale = c->pf_sa;
+        TTS_CK(launch_prefill_rmsnorm_fp8(c->pf_h, w.ln_in, c->pf_a8, c->pf_sa, P, H, k.rms_eps, s));
+        g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H; g.b_scale = w.sqkv;
+        g.bn = gemm_pick_bn(P, QD, kGemmStore, c->num_sms);
+        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wqkv, g, kGemmStore, s));
+        TTS_CK(launch_prefill_qk_rope_kv(c->pf_qkv, w.qn, w.kn, c->rope, c->pf_q, c->kc + coff, c->vc + coff, pos0,
+                                         P, k.n_q_heads, k.n_kv_heads, k.max_pos, k.rms_eps, s));
+        // fp32 attention output, quantised per row next
+        TTS_CK(launch_prefill_attention(c->pf_q, c->kc + coff, c->vc + coff, nullptr, pos0, P, k.n_q_heads,
+                                        k.n_kv_heads, k.max_pos, s, c->pf_attn_f));
+        TTS_CK(launch_prefill_quant_rows_f32(c->pf_attn_f, c->pf_a8, c->pf_sa, P, A, s));
+        g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A; g.b_scale = w.so;
+        g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
+        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wo, g, kGemmAdd, s));
+        TTS_CK(launch_prefill_rmsnorm_fp8(c->pf_h, w.ln_post, c->pf_a8, c->pf_sa, P, H, k.rms_eps, s));
+        g.C = nullptr; g.out_bf16 = c->pf_m; g.ldc = I; g.N = I; g.n_half = I; g.K = H; g.b_scale = w.sgu; g.bn = 0;
+        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wgu, g, kGemmSwiglu, s));
+        TTS_CK(launch_prefill_quant_rows(c->pf_m, c->pf_a8, c->pf_sa, P, I, s));
+        g.out_bf16 = nullptr; g.C = c->pf_h; g.ldc = H; g.N = H; g.n_half = 0; g.K = I; g.b_scale = w.sd;
+        g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
+        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wd, g, kGemmAdd, s));
+        if (snap)
+            TTS_CK(cudaMemcpyAsync(snap + (size_t)(l + 1) * P * H, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
+    }
+    return TTS_OK;
+}
+
 int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap = nullptr) {
     const tts_config& k = c->cfg;
     const int H = k.hidden, I = k.inter, A = c->attn_dim, QD = c->qkv_rows;
@@ -515,7 +558,13 @@ int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap =
         TTS_TRY(dalloc(c, &c->pf_a, R * H));
         TTS_TRY(dalloc(c, &c->pf_attn, R * A));
         TTS_TRY(dalloc(c, &c->pf_m, R * I));
+        if (k.precision == TTS_FP8) {
+            TTS_TRY(dalloc(c, &c->pf_a8, R * (size_t)std::max({H, A, I})));
+            TTS_TRY(dalloc(c, &c->pf_sa, R));
+            TTS_TRY(dalloc(c, &c->pf_attn_f, R * A));
+        }
     }
+    if (k.precision == TTS_FP8) return prefill_chunk_fp8(c, d_codes, pos0, P, snap);
     int* err = &c->st->err;
     TTS_CK(launch_prefill_embed(c->embed, d_codes, c->pf_h, P, k.n_codebooks, k.cb_vocab, H, s));
     const size_t rows_bytes = sizeof(float) * (size_t)P * H;

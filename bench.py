@@ -383,7 +383,7 @@ def run_gpu(args, wl_name, wl):
     # batched prompt prefill (tensor-core path) at P = 512, same weights: the
     # median of timed prefills after warm-up, with CUDA events
     prefill_512 = None
-    if wl["precision"] == 0 and not args.no_prefill:
+    if not args.no_prefill:
         Pp = 512
         pdec = ads.Decoder(ads.Dims(**{f: getattr(d, f) for f in ("n_layers", "hidden", "n_q", "n_kv", "head_dim",
                                                                    "inter", "n_cb", "cb_vocab")}),
@@ -405,10 +405,13 @@ def run_gpu(args, wl_name, wl):
         proj = (d.n_q + 2 * d.n_kv) * D * H + H * d.n_q * D + 2 * I * H + H * I
         gemm_flop = 2.0 * Pp * d.n_layers * proj
         attn_flop = 2.0 * 2 * d.n_layers * d.n_q * D * (Pp * (Pp + 1) / 2)
+        # the peak of the GEMMs' own operand type: fp8 dense = 2 x bf16 (nominal ratio)
+        peak = read_bf16_peak() * (2.0 if wl["precision"] else 1.0)
         prefill_512 = {"positions": Pp, "ms": pms, "tokens_per_s": Pp / (pms * 1e-3),
-                       "gemm_tflops": gemm_flop / (pms * 1e-3) / 1e12,
-                       "flop": gemm_flop + attn_flop, "bf16_peak_tflops": read_bf16_peak(),
-                       "frac_of_bf16_peak": gemm_flop / (pms * 1e-3) / 1e12 / read_bf16_peak()}
+                       "gemm_tflops": gemm_flop / (pms * 1e-3) / 1e12, "gemm_dtype": "fp8-e4m3" if wl["precision"] else "bf16",
+                       "flop": gemm_flop + attn_flop, "peak_tflops": peak,
+                       "peak_source": "measured bf16" + (" x 2 (nominal fp8/bf16 ratio)" if wl["precision"] else ""),
+                       "frac_of_peak": gemm_flop / (pms * 1e-3) / 1e12 / peak}
         pdec.close()
 
     cpu_baseline = None

@@ -276,8 +276,8 @@ int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes
  * of every prompt row after the embedding and after every layer into
  * `host_h` ([n_layers + 1][P][hidden], caller-owned, `capacity` floats), so a
  * check can start the CPU oracle's layer l from the GPU's input to it.
- * TTS_ERR_UNSUPPORTED when the context does not prefill on the batched path
- * (FP8 weights); otherwise as tts_prefill.  Synchronises. */
+ * TTS_ERR_UNSUPPORTED when the context does not prefill on the batched path;
+ * otherwise as tts_prefill.  Synchronises. */
 int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* host_h, long long capacity);
 
 /* Stand-alone op: C = A . B^T on the tensor cores (tcgen05 MMA, TMEM
@@ -297,6 +297,22 @@ int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* h
  * `stream` (NULL: the default stream); does not synchronise.  Returns
  * TTS_ERR_ARG for bad sizes, NULL or misaligned pointers. */
 int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, int epi, int splits, void* stream);
+
+/* Stand-alone op: the FP8 W8A8 GEMM of the batched prefill of FP8 contexts
+ * (FlashRT page, "FP8 W8A8": E4M3 weights with a per-row scale, E4M3
+ * activations with a per-token scale), on the tensor cores
+ * (tcgen05.mma kind::f8f6f4, fp32 accumulation in tensor memory).
+ *   A8: device E4M3 [M][K] (activations), a_scale: device fp32 [M];
+ *   B8: device E4M3 [N][K] (epi 2: [2N][K], gate rows then up rows),
+ *   b_scale: device fp32 [N] (epi 2: [2N]); all borrowed.
+ * Every product sum is turned into y = bf16(acc * (a_scale[m] * b_scale[n]))
+ * (the FP8 projection's bf16 output), then epi 0: C fp32 [M][N] = y;
+ * epi 1: C += y; epi 2: C bf16 [M][N] = bf16(silu(y_gate) * y_up).
+ * K % 128 == 0, N as tts_gemm_bf16, any M >= 1; no split-K.  Enqueued on
+ * `stream`; does not synchronise.  TTS_ERR_ARG for bad sizes, NULL or
+ * misaligned pointers (A8, B8, C 16-byte aligned). */
+int tts_gemm_fp8(const void* A8, const void* B8, const float* a_scale, const float* b_scale, void* C, int M, int N,
+                 int K, int epi, void* stream);
 
 /* Per-output-row FP8 weight quantisation on the GPU (FlashRT page,
  * Performance "FP8 W8A8"; section 8, scale amax/448): for each row n,

@@ -80,3 +80,43 @@ def test_gemm_swiglu(env):
     ref = g / (1.0 + np.exp(-g)) * u
     # one bf16 rounding of an fp32 value: within 2^-8 relative (plus tiny values)
     assert np.allclose(got, ref, rtol=2 ** -7, atol=1e-3 * np.abs(ref).max())
+
+
+def fp8_operands(torch, seed, rows, K, std):
+    """E4M3 rows with a per-row scale (the oracle's quantisation of bf16 draws)."""
+    Wb = synth.normal_bf16(2, seed, (rows, K), std=std)
+    q, sw = oracle.quant_weight(Wb)
+    return q, sw, torch.from_numpy(np.ascontiguousarray(q)).cuda(), torch.from_numpy(np.ascontiguousarray(sw)).cuda()
+
+
+def ref_fp8(q_a, sa, q_w, sw):
+    """Oracle FP8 projection per row: bf16(fp32(sum a8 w8) * fp32(sa * sw[n]))."""
+    return np.stack([oracle.linear_fp8(q_w, sw, q_a[i], float(sa[i])) for i in range(q_a.shape[0])])
+
+
+@pytest.mark.parametrize("M,N,K,epi", [(37, 128, 256, 0), (300, 384, 2560, 0), (130, 256, 512, 1), (260, 256, 1024, 2)])
+def test_gemm_fp8(env, M, N, K, epi):
+    ads, torch = env
+    qa, sa, qa_d, sa_d = fp8_operands(torch, 111, M, K, 1.0)
+    rows = 2 * N if epi == 2 else N
+    qw, sw, qw_d, sw_d = fp8_operands(torch, 112, rows, K, 0.02)
+    if epi == 2:
+        C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    elif epi == 1:
+        base = synth.normal_f32(2, 113, (M, N))
+        C = torch.from_numpy(base.copy()).cuda()
+    else:
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ads.gemm_fp8(qa_d, qw_d, sa_d, sw_d, C, epi=epi)
+    torch.cuda.synchronize()
+    got = C.float().cpu().numpy().astype(np.float64)
+    y = ref_fp8(qa, sa, qw, sw)
+    if epi == 2:
+        g, u = y[:, :N], y[:, N:]
+        silu = g / (1.0 + np.exp(-g))
+        ref = silu * u
+        assert np.allclose(got, ref, rtol=2 ** -6, atol=2e-3 * np.abs(ref).max())
+    else:
+        ref = y if epi == 0 else base.astype(np.float64) + y
+        # bf16 outputs: the GPU's fp32 sum may round to the neighbouring bf16 value
+        assert np.allclose(got, ref, rtol=2 ** -7, atol=1e-6 * np.abs(ref).max())

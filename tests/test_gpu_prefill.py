@@ -58,6 +58,64 @@ def run_case(ads, d, P, prefix, seed_stream, gamma_variant=False):
     return kv_stat, stat
 
 
+def run_case_fp8(ads, d, P, prefix, seed_stream):
+    """The batched FP8 W8A8 prefill (tcgen05 kind::f8f6f4 GEMMs, per-token
+    activation scales) against the oracle's FP8 layers, layer by layer from
+    the GPU's own residual stream (as the FP8 decode step is checked: every
+    layer re-quantises per token, so e4m3 rounding flips from fp32-versus-fp64
+    sums compound across layers).  The layer's K/V rows reach the FP8 bar
+    (cos >= 0.999).  Each row's layer contribution must reach 0.998 and their
+    mean 0.9995: the prefill's attention runs on the tensor cores with bf16 Q
+    and P, so single e4m3 codes of its output (steps of 6-12 %) flip where the
+    oracle's exact attention lands near a rounding boundary, and at this
+    reduced width (1024-wide attention output) one flip moves a row's
+    contribution by up to ~1e-3 of cosine.  The first frame after the
+    prefill, run from the GPU's cache, meets the FP8 frame bar."""
+    max_pos = prefix + P + 4
+    w = synth.make_weights(d, gamma_variant=True)
+    dw = ads.DeviceWeights(w, precision=1)
+    dec = ads.Decoder(to_binding_dims(d), dw, max_pos)
+    orc = oracle.Oracle(w, max_pos, precision=1)
+    if prefix:
+        k, v = synth.make_kv_prefix(d, prefix, max_pos)
+        kd, vd = upload_kv(k, v, prefix)
+        dec.set_kv(kd, vd, prefix)
+        orc.set_kv(k, v, prefix)
+    prompt = synth.delayed_prompt_codes(P, stream=seed_stream)
+    hs = dec.prefill_states(prompt).astype(np.float64)
+    assert dec.state()[0] == prefix + P
+    gk, gv = dec.get_kv(prefix, prefix + P)
+    worst, coss = 1.0, []
+    for l in range(d.n_layers):
+        for p in range(P):
+            out = orc.layer(l, prefix + p, hs[l, p])
+            c = cosine(hs[l + 1, p] - hs[l, p], out - hs[l, p])
+            worst = min(worst, c)
+            coss.append(c)
+            assert c >= 0.998, f"FP8 prefill P={P} layer {l} row {p}: contribution cos {c}"
+        for name, g_, o_ in (("K", gk[l], orc.k[l, :, prefix:prefix + P]), ("V", gv[l], orc.v[l, :, prefix:prefix + P])):
+            c = cosine(bf16_f64(g_).ravel(), bf16_f64(o_).ravel())
+            assert c >= 0.999, f"FP8 prefill P={P} {name} layer {l}: cos {c}"
+    assert float(np.mean(coss)) >= 0.9995, f"FP8 prefill P={P}: mean contribution cos {np.mean(coss)}"
+    adopt_gpu_cache(dec, orc, prefix + P)
+    orc.st.pos = prefix + P
+    g = dec.decode_step()
+    o, ol, og = orc.decode_step(np.full(8, 1024, np.int32))
+    stat = check_frame(g, dec.get_logits(), o, ol, og, True, 0, -1, f"FP8 frame after prefill P={P}")
+    dec.close()
+    return worst, float(np.mean(coss)), stat
+
+
+def test_prefill_fp8_batched(ads):
+    print(run_case_fp8(ads, reduced_dims(2), 40, 0, 6))
+
+
+def test_prefill_fp8_after_prefix(ads):
+    # one chunk (the states hook records up to 512 rows); the chunk loop is
+    # the same for both precisions and runs two chunks in the BF16 case below
+    print(run_case_fp8(ads, reduced_dims(2), 480, 24, 7))
+
+
 def test_prefill_two_chunks_after_prefix(ads):
     print(run_case(ads, reduced_dims(2), 600, 24, 3, gamma_variant=True))
 
