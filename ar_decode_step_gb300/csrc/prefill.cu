@@ -92,6 +92,52 @@ __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const floa
     }
 }
 
+// RMSNorm rows, one warp per row held in registers (NV float4 per lane,
+// hidden <= 128 NV, NV up to kRowVec): one read of h, warp reductions only.
+constexpr int kRowVec = 32;
+constexpr int kRowWarps = kRowThreads / 32;
+template <int NV>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_rows_warp_kernel(const float* H, const __nv_bfloat16* gamma,
+                                                                        __nv_bfloat16* out, int P, int hidden,
+                                                                        float eps) {
+    const int row = blockIdx.x * kRowWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= P) return;
+    const float4* h4 = reinterpret_cast<const float4*>(H + (size_t)row * hidden);
+    const uint2* g4 = reinterpret_cast<const uint2*>(gamma);
+    const int n4 = hidden / 4;
+    float4 v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = lane + 32 * i;
+        if (j < n4) {
+            v[i] = h4[j];
+            ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        }
+    }
+    ss = warp_sum(ss);
+    const float r = 1.0f / sqrtf(ss / (float)hidden + eps);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = lane + 32 * i;
+        if (j < n4) {
+            const uint2 g = g4[j];
+            v[i] = make_float4(v[i].x * r * bf16lo(g.x), v[i].y * r * bf16hi(g.x), v[i].z * r * bf16lo(g.y),
+                               v[i].w * r * bf16hi(g.y));
+        }
+    }
+    uint2* o = reinterpret_cast<uint2*>(out + (size_t)row * hidden);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = lane + 32 * i;
+        if (j < n4) {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(v[i].x, v[i].y);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v[i].z, v[i].w);
+            o[j] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+        }
+    }
+}
+
 // FP8 W8A8 rows: the projection inputs quantised per row (per token) as the
 // decode step does ("Higgs Audio v3 TTS-4B on FlashRT", Performance "FP8
 // W8A8"): s = max(amax, 1e-12) / 448, q = e4m3(x / s) with IEEE fp32 division,
@@ -387,14 +433,38 @@ cudaError_t launch_prefill_embed(const __nv_bfloat16* E, const int* codes, float
     return cudaGetLastError();
 }
 
+// the smallest register row that holds `hidden` (a multiple of 4 floats per lane)
+cudaError_t launch_rows_warp(const float* H, const __nv_bfloat16* gamma, __nv_bfloat16* out, int P, int hidden,
+                             float eps, cudaStream_t s) {
+    const dim3 grid((P + kRowWarps - 1) / kRowWarps);
+    const int nv = (hidden / 4 + 31) / 32;
+#define TTS_ROWS_NV(NV)                                                                                            \
+    if (nv <= NV) {                                                                                                \
+        rmsnorm_rows_warp_kernel<NV><<<grid, kRowThreads, 0, s>>>(H, gamma, out, P, hidden, eps);                 \
+        return cudaGetLastError();                                                                                 \
+    }
+    TTS_ROWS_NV(4)
+    TTS_ROWS_NV(8)
+    TTS_ROWS_NV(16)
+    TTS_ROWS_NV(20)
+    TTS_ROWS_NV(24)
+    TTS_ROWS_NV(32)
+#undef TTS_ROWS_NV
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_prefill_rmsnorm(const float* H, const __nv_bfloat16* gamma, __nv_bfloat16* out, int P,
                                    int hidden, float eps, cudaStream_t s) {
-    rmsnorm_rows_kernel<<<P, kRowThreads, 0, s>>>(H, gamma, out, hidden, eps);
+    if (hidden % 4 == 0 && hidden <= 128 * kRowVec)
+        return launch_rows_warp(H, gamma, out, P, hidden, eps, s);
+    else
+        rmsnorm_rows_kernel<<<P, kRowThreads, 0, s>>>(H, gamma, out, hidden, eps);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_rmsnorm_fp8(const float* H, const __nv_bfloat16* gamma, uint8_t* out, float* scale, int P,
                                        int hidden, float eps, cudaStream_t s) {
+    // a CTA per row: the IEEE divisions of the quantisation spread over all its threads
     rmsnorm_quant_rows_kernel<<<P, kRowThreads, 0, s>>>(H, gamma, out, scale, hidden, eps);
     return cudaGetLastError();
 }
