@@ -15,6 +15,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "kernels.h"
@@ -46,6 +49,10 @@ struct tts_ctx {
     __nv_bfloat16 *pre_k = nullptr, *pre_v = nullptr;
     int pre_cap = 0, pre_len = 0;
     DevState pre_state{};
+    // batched prefill chunks captured as graphs, by (first position, rows,
+    // prompt row offset); a chunk shape runs directly the first time
+    std::map<std::tuple<int, int, int>, cudaGraphExec_t> pf_graphs;
+    std::set<std::tuple<int, int, int>> pf_seen;
 
     const __nv_bfloat16 *embed = nullptr, *head = nullptr, *final_norm = nullptr;
     std::vector<LayerW> L;
@@ -598,12 +605,51 @@ int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap =
     return TTS_OK;
 }
 
+// One batched prefill chunk, replayed from a captured graph once its shape
+// has run before (the first run also does the lazy set-up: buffers, kernel
+// attributes): the ~250 launches of a 36-layer chunk then cost one.
+constexpr size_t kMaxPrefillGraphs = 16;
+int run_prefill_chunk(tts_ctx* c, int r, int pos0, int rows) {
+    const int* d_codes = c->prompt + (size_t)r * c->cfg.n_codebooks;
+    const auto key = std::make_tuple(pos0, rows, r);
+    auto it = c->pf_graphs.find(key);
+    if (it != c->pf_graphs.end()) {
+        TTS_CK(cudaGraphLaunch(it->second, c->stream));
+        return TTS_OK;
+    }
+    if (!c->pf_seen.count(key) || c->pf_graphs.size() >= kMaxPrefillGraphs) {
+        c->pf_seen.insert(key);
+        return prefill_chunk(c, d_codes, pos0, rows);
+    }
+    // captured on the context's own capture stream (the caller's may be the
+    // legacy default stream, which cannot be captured)
+    cudaGraph_t g = nullptr;
+    cudaStream_t user = c->stream;
+    TTS_CK(cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+    c->stream = c->cap;
+    const int rc = prefill_chunk(c, d_codes, pos0, rows);
+    c->stream = user;
+    const cudaError_t e = cudaStreamEndCapture(c->cap, &g);  // always: leaves the stream usable
+    if (rc != TTS_OK || e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return rc != TTS_OK ? rc : report(e, "prefill capture");
+    }
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ei = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) return report(ei, "prefill graph");
+    c->pf_graphs[key] = exec;
+    TTS_CK(cudaGraphLaunch(exec, c->stream));
+    return TTS_OK;
+}
+
 void destroy(tts_ctx* c) {
     if (!c) return;
     if (c->stream) cudaStreamSynchronize(c->stream);
     else cudaDeviceSynchronize();
     // graphs first: they reference the buffers below
     if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
+    for (auto& kv : c->pf_graphs) cudaGraphExecDestroy(kv.second);
     if (c->prefill_exec) cudaGraphExecDestroy(c->prefill_exec);
     for (void* p : c->allocs) cudaFree(p);
     if (c->pre_k) cudaFree(c->pre_k);
@@ -704,8 +750,7 @@ int tts_prefill(tts_ctx* ctx, const int32_t* codes, int P) {
         // the whole prompt as M = P tensor-core passes, kPrefillChunk rows at a time
         DevState s = *ctx->h_out;
         for (int r = 0; r < P; r += kPrefillChunk)
-            TTS_TRY(prefill_chunk(ctx, ctx->prompt + (size_t)r * k.n_codebooks, s.pos + r,
-                                  std::min(kPrefillChunk, P - r)));
+            TTS_TRY(run_prefill_chunk(ctx, r, s.pos + r, std::min(kPrefillChunk, P - r)));
         TTS_CK(cudaStreamSynchronize(ctx->stream));
         int rc = pull_state(ctx);  // reports a GEMM wait that expired (device error word)
         if (rc != TTS_OK) return rc;

@@ -109,3 +109,29 @@ def test_one_call_and_split_prefill_agree(ads, model):
     assert np.array_equal(one.decode_steps(3), two.decode_steps(3))
     one.close()
     two.close()
+
+
+@pytest.mark.parametrize("precision", [0, 1])
+def test_repeated_prefill_replays_identically(ads, model, precision):
+    """A batched prefill chunk runs directly the first time its shape is seen,
+    is captured as a graph the second time and replayed after that: the three
+    runs of one request must leave the same cache rows and codes, bit for bit,
+    and a chunk of another shape in between must not disturb the replay."""
+    d, w = model
+    dw = ads.DeviceWeights(w, precision=precision)
+    prompt = synth.delayed_prompt_codes(21)
+    other = synth.random_codes(9, seed=2, stream=34)
+    dec = ads.Decoder(to_binding_dims(d), dw, 64)
+    runs = []
+    for rep in range(4):
+        dec.reset()
+        if rep == 2:
+            dec.prefill(other)
+            dec.reset()
+        dec.prefill(prompt)
+        k, v = dec.get_kv(0, 21)
+        runs.append((k, v, dec.decode_steps(3), dec.state()))
+    for k, v, codes, st in runs[1:]:
+        assert np.array_equal(k, runs[0][0]) and np.array_equal(v, runs[0][1])
+        assert np.array_equal(codes, runs[0][2]) and st == runs[0][3]
+    dec.close()
