@@ -75,6 +75,7 @@ SIGNATURES = {
     "tts_debug_layer_states": (_I, [_VP, _VP, _VP, _VP, _I]),
     "tts_gemm_bf16": (_I, [_VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tts_gemm_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "tts_gemm_tiled": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "tts_debug_prefill_states": (_I, [_VP, _VP, _I, _VP, ctypes.c_longlong]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -130,10 +131,11 @@ def _to_dev_u16(a: np.ndarray, device):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device, non_blocking=False)
 
 
-def gemm_bf16(a_dev, b_dev, c_dev, epi: int = 0, splits: int = 1, stream=None):
+def gemm_bf16(a_dev, b_dev, c_dev, epi: int = 0, splits: int = 0, stream=None):
     """C = A . B^T on the tensor cores (see tts_gemm_bf16): a_dev [M][K] and
     b_dev [N][K] (epi 2: [2N][K]) bf16 CUDA tensors; c_dev fp32 [M][N]
-    (epi 0, 1) or bf16 [M][N] (epi 2)."""
+    (epi 0, 1) or bf16 [M][N] (epi 2); splits 0 lets the library choose the
+    K split, n > 0 fixes it."""
     M, K = a_dev.shape
     N = c_dev.shape[1]
     _call("tts_gemm_bf16", a_dev.data_ptr(), b_dev.data_ptr(), c_dev.data_ptr(), M, N, K, epi, splits, stream)
@@ -147,6 +149,19 @@ def gemm_fp8(a8_dev, b8_dev, a_scale_dev, b_scale_dev, c_dev, epi: int = 0, stre
     N = c_dev.shape[1]
     _call("tts_gemm_fp8", a8_dev.data_ptr(), b8_dev.data_ptr(), a_scale_dev.data_ptr(), b_scale_dev.data_ptr(),
           c_dev.data_ptr(), M, N, K, epi, stream)
+
+
+def gemm_tiled(a_dev, b_dev, c_dev, epi: int, tile_rows: int, tile_cols: int, splits: int,
+               a_scale_dev=None, b_scale_dev=None, stream=None):
+    """tts_gemm_tiled: tts_gemm_bf16 (uint8 operands with scales: tts_gemm_fp8)
+    with an explicit tile of tile_rows (128 or 256) x tile_cols output
+    columns and the K range split over `splits` CTAs."""
+    M, K = a_dev.shape
+    N = c_dev.shape[1]
+    fp8 = a_scale_dev is not None
+    _call("tts_gemm_tiled", a_dev.data_ptr(), b_dev.data_ptr(), a_scale_dev.data_ptr() if fp8 else None,
+          b_scale_dev.data_ptr() if fp8 else None, c_dev.data_ptr(), M, N, K, epi, 1 if fp8 else 0,
+          tile_rows, tile_cols, splits, stream)
 
 
 def quantize_fp8_weight(w_dev, stream=None):

@@ -216,10 +216,11 @@ int step_attn_scratch_bytes(int G);
 int step_threads();
 cudaError_t launch_step(const StepParams& p, int prec, int G, int grid, int smem, cudaStream_t s);
 
-// C = A . B^T on the tensor cores (gemm_tc.cu): A [M][K] and B [N][K] bf16,
-// K-major, fp32 accumulation.  Epilogues: store fp32 C[M][ldc]; add into fp32
-// C (residual stream: deterministic with one k-split, atomic with several); SwiGLU: B = [gate rows; up rows] of
-// a [2 n_half][K] matrix, out_bf16[M][ldc] = bf16(silu(gate) * up), N = n_half.
+// C = A . B^T on the tensor cores (gemm_tc.cu): A [M][K] and B [N][K], bf16
+// or E4M3, K-major, fp32 accumulation.  Epilogues: store fp32 C[M][ldc]; add
+// into fp32 C (the residual stream; one writer per element, deterministic);
+// SwiGLU: B = [gate rows; up rows] of a [2 n_half][K] matrix,
+// out_bf16[M][ldc] = bf16(silu(gate) * up), N = n_half.
 enum GemmEpi { kGemmStore = 0, kGemmAdd = 1, kGemmSwiglu = 2 };
 struct GemmParams {
     float* C;
@@ -227,22 +228,25 @@ struct GemmParams {
     int ldc;
     int M, N, K;
     int n_half;
-    int bn;            // output columns per tile: 64, 80, 128 (0 = default) or 192; SwiGLU: 128
-    int kb_per_split;  // filled in by launch_gemm_bf16
-    int atomic;        // filled in: split-K partials are added atomically
+    int kb_per_split;  // filled in by launch_gemm
     int* err;          // error word (kErrTimeout on an expired wait), may be NULL
-    // E4M3 operands (launch_gemm_fp8): per-row activation scales [M] and
-    // per-row weight scales [N] (SwiGLU: [2 n_half]); every output is
+    // E4M3 operands: per-row activation scales [M] and per-row weight scales
+    // [N] (SwiGLU: [2 n_half]); every product sum becomes
     // bf16(acc * (a_scale[m] * b_scale[n])) before the epilogue's operation
     const float* a_scale;
     const float* b_scale;
 };
-bool gemm_shape_ok(int M, int N, int K, int epi, int bn);
-int gemm_pick_bn(int M, int N, int epi, int num_sms);  // tile width that fills the SMs best
-bool gemm_shape_ok_fp8(int M, int N, int K, int epi, int bn);
-cudaError_t launch_gemm_fp8(const void* A8, const void* B8, const GemmParams& p, int epi, cudaStream_t s);
-cudaError_t launch_gemm_bf16(const void* A, const void* B, const GemmParams& p, int epi, int splits,
-                             cudaStream_t s);
+// A CTA's tile: 128 mt rows (mt = 1 or 2 accumulators sharing each weight
+// tile) x bn output columns (64, 80, 128, 160 or 192; SwiGLU: 128 gate + 128
+// up), the K range cut over `splits` CTAs of a cluster whose partial sums are
+// added in a fixed order.  mt = 0: chosen by gemm_pick (splits > 0 fixes the split).
+struct GemmTile {
+    int mt, bn, splits;
+};
+GemmTile gemm_pick(int M, int N, int K, int epi, bool fp8, int num_sms, int splits);
+bool gemm_shape_ok(int N, int K, int epi, bool fp8);  // some tile covers N x K
+cudaError_t launch_gemm(const void* A, const void* B, const GemmParams& p, int epi, bool fp8, GemmTile t,
+                        int num_sms, cudaStream_t s);
 
 // Batched prefill glue (prefill.cu): P rows at positions pos0 .. pos0+P-1.
 cudaError_t launch_prefill_embed(const __nv_bfloat16* E, const int* codes, float* H, int P, int n_cb, int V,

@@ -501,10 +501,10 @@ constexpr int kPrefillChunk = 512;  // rows per batched pass (the prompt is spli
 bool batched_prefill_ok(const tts_ctx* c) {
     const tts_config& k = c->cfg;
     const int G = k.n_q_heads / k.n_kv_heads;
-    auto ok = k.precision == TTS_FP8 ? gemm_shape_ok_fp8 : gemm_shape_ok;
-    return c->batched_prefill && k.head_dim == kHeadDim && ok(1, c->qkv_rows, k.hidden, kGemmStore, 64) &&
-           ok(1, k.hidden, c->attn_dim, kGemmAdd, 64) && ok(1, k.inter, k.hidden, kGemmSwiglu, 128) &&
-           ok(1, k.hidden, k.inter, kGemmAdd, 64) && (G == 1 || G == 2 || G == 4 || G == 8);
+    const bool f8 = k.precision == TTS_FP8;
+    return c->batched_prefill && k.head_dim == kHeadDim && gemm_shape_ok(c->qkv_rows, k.hidden, kGemmStore, f8) &&
+           gemm_shape_ok(k.hidden, c->attn_dim, kGemmAdd, f8) && gemm_shape_ok(k.inter, k.hidden, kGemmSwiglu, f8) &&
+           gemm_shape_ok(k.hidden, k.inter, kGemmAdd, f8) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
 // P rows (codes already on the device at c->prompt) through every layer at
@@ -529,8 +529,7 @@ int prefill_chunk_fp8(tts_ctx* c, const int* d_codes, int pos0, int P, float* sn
         g.M = P; g.err = err; g.a_scale = c->pf_sa;
         TTS_CK(launch_prefill_rmsnorm_fp8(c->pf_h, w.ln_in, c->pf_a8, c->pf_sa, P, H, k.rms_eps, s));
         g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H; g.b_scale = w.sqkv;
-        g.bn = gemm_pick_bn(P, QD, kGemmStore, c->num_sms);
-        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wqkv, g, kGemmStore, s));
+        TTS_CK(launch_gemm(c->pf_a8, w.wqkv, g, kGemmStore, true, GemmTile{}, c->num_sms, s));
         TTS_CK(launch_prefill_qk_rope_kv(c->pf_qkv, w.qn, w.kn, c->rope, c->pf_q, c->kc + coff, c->vc + coff, pos0,
                                          P, k.n_q_heads, k.n_kv_heads, k.max_pos, k.rms_eps, s));
         // fp32 attention output, quantised per row next
@@ -538,15 +537,13 @@ int prefill_chunk_fp8(tts_ctx* c, const int* d_codes, int pos0, int P, float* sn
                                         k.n_kv_heads, k.max_pos, s, c->pf_attn_f));
         TTS_CK(launch_prefill_quant_rows_f32(c->pf_attn_f, c->pf_a8, c->pf_sa, P, A, s));
         g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A; g.b_scale = w.so;
-        g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
-        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wo, g, kGemmAdd, s));
+        TTS_CK(launch_gemm(c->pf_a8, w.wo, g, kGemmAdd, true, GemmTile{}, c->num_sms, s));
         TTS_CK(launch_prefill_rmsnorm_fp8(c->pf_h, w.ln_post, c->pf_a8, c->pf_sa, P, H, k.rms_eps, s));
-        g.C = nullptr; g.out_bf16 = c->pf_m; g.ldc = I; g.N = I; g.n_half = I; g.K = H; g.b_scale = w.sgu; g.bn = 0;
-        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wgu, g, kGemmSwiglu, s));
+        g.C = nullptr; g.out_bf16 = c->pf_m; g.ldc = I; g.N = I; g.n_half = I; g.K = H; g.b_scale = w.sgu;
+        TTS_CK(launch_gemm(c->pf_a8, w.wgu, g, kGemmSwiglu, true, GemmTile{}, c->num_sms, s));
         TTS_CK(launch_prefill_quant_rows(c->pf_m, c->pf_a8, c->pf_sa, P, I, s));
         g.out_bf16 = nullptr; g.C = c->pf_h; g.ldc = H; g.N = H; g.n_half = 0; g.K = I; g.b_scale = w.sd;
-        g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
-        TTS_CK(launch_gemm_fp8(c->pf_a8, w.wd, g, kGemmAdd, s));
+        TTS_CK(launch_gemm(c->pf_a8, w.wd, g, kGemmAdd, true, GemmTile{}, c->num_sms, s));
         if (snap)
             TTS_CK(cudaMemcpyAsync(snap + (size_t)(l + 1) * P * H, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
     }
@@ -576,29 +573,27 @@ int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap =
     TTS_CK(launch_prefill_embed(c->embed, d_codes, c->pf_h, P, k.n_codebooks, k.cb_vocab, H, s));
     const size_t rows_bytes = sizeof(float) * (size_t)P * H;
     if (snap) TTS_CK(cudaMemcpyAsync(snap, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
-    // tile widths chosen per GEMM so that the grid fills the SMs in whole
-    // waves; the residual GEMMs keep one writer per element (deterministic, no split-K)
+    // each GEMM's tile and K split chosen to fill the SMs (gemm_pick); split
+    // sums are added in a fixed order, so the residual stream is deterministic
     for (int l = 0; l < k.n_layers; ++l) {
         const LayerW& w = c->L[l];
         const size_t coff = (size_t)l * k.n_kv_heads * k.max_pos * kHeadDim;
         TTS_CK(launch_prefill_rmsnorm(c->pf_h, w.ln_in, c->pf_a, P, H, k.rms_eps, s));
         GemmParams g{};
         g.M = P; g.err = err;
-        g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H; g.bn = gemm_pick_bn(P, QD, kGemmStore, c->num_sms);
-        TTS_CK(launch_gemm_bf16(c->pf_a, w.wqkv, g, kGemmStore, 1, s));
+        g.C = c->pf_qkv; g.ldc = QD; g.N = QD; g.K = H;
+        TTS_CK(launch_gemm(c->pf_a, w.wqkv, g, kGemmStore, false, GemmTile{}, c->num_sms, s));
         TTS_CK(launch_prefill_qk_rope_kv(c->pf_qkv, w.qn, w.kn, c->rope, c->pf_q, c->kc + coff, c->vc + coff, pos0,
                                          P, k.n_q_heads, k.n_kv_heads, k.max_pos, k.rms_eps, s));
         TTS_CK(launch_prefill_attention(c->pf_q, c->kc + coff, c->vc + coff, c->pf_attn, pos0, P, k.n_q_heads,
                                         k.n_kv_heads, k.max_pos, s));
-        g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A; g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
-        TTS_CK(launch_gemm_bf16(c->pf_attn, w.wo, g, kGemmAdd, 1, s));
-        g.bn = 0;
+        g.C = c->pf_h; g.ldc = H; g.N = H; g.K = A;
+        TTS_CK(launch_gemm(c->pf_attn, w.wo, g, kGemmAdd, false, GemmTile{}, c->num_sms, s));
         TTS_CK(launch_prefill_rmsnorm(c->pf_h, w.ln_post, c->pf_a, P, H, k.rms_eps, s));
         g.C = nullptr; g.out_bf16 = c->pf_m; g.ldc = I; g.N = I; g.n_half = I; g.K = H;
-        TTS_CK(launch_gemm_bf16(c->pf_a, w.wgu, g, kGemmSwiglu, 1, s));
+        TTS_CK(launch_gemm(c->pf_a, w.wgu, g, kGemmSwiglu, false, GemmTile{}, c->num_sms, s));
         g.out_bf16 = nullptr; g.C = c->pf_h; g.ldc = H; g.N = H; g.n_half = 0; g.K = I;
-        g.bn = gemm_pick_bn(P, H, kGemmAdd, c->num_sms);
-        TTS_CK(launch_gemm_bf16(c->pf_m, w.wd, g, kGemmAdd, 1, s));
+        TTS_CK(launch_gemm(c->pf_m, w.wd, g, kGemmAdd, false, GemmTile{}, c->num_sms, s));
         if (snap)
             TTS_CK(cudaMemcpyAsync(snap + (size_t)(l + 1) * P * H, c->pf_h, rows_bytes, cudaMemcpyDeviceToDevice, s));
     }

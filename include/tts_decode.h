@@ -287,15 +287,17 @@ int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* h
  *   A: device bf16 [M][K] row-major (activations), B: device bf16 [N][K]
  *   (weights, one output feature per row), both borrowed, 16-byte aligned.
  *   epi 0: C = device fp32 [M][N], overwritten.
- *   epi 1: C = device fp32 [M][N], C += A . B^T (fp32 atomic adds; with
- *          splits > 1 the K range is split over that many CTAs per tile).
+ *   epi 1: C = device fp32 [M][N], C += A . B^T.
  *   epi 2: SwiGLU: B = [gate rows; up rows], a [2N][K] matrix; C = device
  *          bf16 [M][N] = bf16(silu(A . gate^T) * (A . up^T)).
- * fp32 accumulation; K % 64 == 0, N a multiple of 64 or 80 (epi 2: of
- * 128), any M >= 1; the tile width (64, 80, 128 or 192 columns) is chosen to
- * fill the SMs.  Enqueued on
- * `stream` (NULL: the default stream); does not synchronise.  Returns
- * TTS_ERR_ARG for bad sizes, NULL or misaligned pointers. */
+ * fp32 accumulation; K % 64 == 0, N a multiple of 64, 80, 128, 160 or 192
+ * (epi 2: of 128), any M >= 1.  The tile (128 or 256 rows x one of those
+ * widths) is chosen to fill the SMs; splits > 0 fixes how many CTAs share
+ * the K range of a tile (1..4, epi 2: 1), splits <= 0 lets the library
+ * choose.  Split sums are added in a fixed order: every result is
+ * deterministic.  Enqueued on `stream` (NULL: the default stream); does not
+ * synchronise.  Returns TTS_ERR_ARG for bad sizes, NULL or misaligned
+ * pointers. */
 int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, int epi, int splits, void* stream);
 
 /* Stand-alone op: the FP8 W8A8 GEMM of the batched prefill of FP8 contexts
@@ -308,11 +310,21 @@ int tts_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, in
  * Every product sum is turned into y = bf16(acc * (a_scale[m] * b_scale[n]))
  * (the FP8 projection's bf16 output), then epi 0: C fp32 [M][N] = y;
  * epi 1: C += y; epi 2: C bf16 [M][N] = bf16(silu(y_gate) * y_up).
- * K % 128 == 0, N as tts_gemm_bf16, any M >= 1; no split-K.  Enqueued on
- * `stream`; does not synchronise.  TTS_ERR_ARG for bad sizes, NULL or
- * misaligned pointers (A8, B8, C 16-byte aligned). */
+ * K % 128 == 0, N as tts_gemm_bf16, any M >= 1; tile and K split chosen as
+ * by tts_gemm_bf16.  Enqueued on `stream`; does not synchronise.
+ * TTS_ERR_ARG for bad sizes, NULL or misaligned pointers (A8, B8, C
+ * 16-byte aligned). */
 int tts_gemm_fp8(const void* A8, const void* B8, const float* a_scale, const float* b_scale, void* C, int M, int N,
                  int K, int epi, void* stream);
+
+/* Stand-alone op: tts_gemm_bf16 (fp8 = 0; a_scale, b_scale unused) or
+ * tts_gemm_fp8 (fp8 = 1) with the tile fixed by the caller: tile_rows 128
+ * or 256 (two 128-row accumulators sharing each weight tile), tile_cols
+ * 64, 80, 128, 160 or 192 (epi 2: 128), the K range split over `splits`
+ * CTAs of a cluster (1..4; epi 2: 1; at most the number of k-blocks).
+ * TTS_ERR_ARG when the tile does not fit the shape; otherwise as those. */
+int tts_gemm_tiled(const void* A, const void* B, const float* a_scale, const float* b_scale, void* C, int M, int N,
+                   int K, int epi, int fp8, int tile_rows, int tile_cols, int splits, void* stream);
 
 /* Per-output-row FP8 weight quantisation on the GPU (FlashRT page,
  * Performance "FP8 W8A8"; section 8, scale amax/448): for each row n,

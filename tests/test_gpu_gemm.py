@@ -1,8 +1,10 @@
-"""The tensor-core GEMM of the batched prefill (tts_gemm_bf16) against the CPU
-oracle's linear layer (fp64 sums of the same bf16 operands): plain store,
-additive epilogue with split-K, and the fused gate/up + SwiGLU epilogue, on
-shapes with ragged M (rows past M are masked), several N tiles and several
-k-blocks, covering the 64-, 80-, 128- and 192-column tile widths."""
+"""The tensor-core GEMM of the batched prefill (tts_gemm_bf16, tts_gemm_fp8,
+tts_gemm_tiled) against the CPU oracle's linear layer (fp64 sums of the same
+operands): plain store, additive epilogue, and the fused gate/up + SwiGLU
+epilogue, on shapes with ragged M (rows past M are masked), several N tiles
+and several k-blocks, covering every tile width, 128- and 256-row tiles and
+the cluster split of the K range (its partial sums added in a fixed order:
+bit-identical from run to run)."""
 import numpy as np
 import pytest
 
@@ -120,3 +122,86 @@ def test_gemm_fp8(env, M, N, K, epi):
         ref = y if epi == 0 else base.astype(np.float64) + y
         # bf16 outputs: the GPU's fp32 sum may round to the neighbouring bf16 value
         assert np.allclose(got, ref, rtol=2 ** -7, atol=1e-6 * np.abs(ref).max())
+
+
+TILED = [  # M, N, K, epi, tile rows, tile columns, K split
+    (300, 320, 512, 1, 256, 160, 4),
+    (300, 384, 1024, 0, 256, 192, 2),
+    (37, 256, 1024, 1, 128, 128, 3),
+    (200, 160, 256, 0, 256, 80, 1),
+    (260, 256, 512, 2, 256, 128, 1),
+    (130, 192, 512, 1, 256, 64, 1),
+    (90, 320, 768, 0, 128, 160, 3),
+]
+
+
+@pytest.mark.parametrize("M,N,K,epi,rows,cols,splits", TILED)
+def test_gemm_tiled_bf16(env, M, N, K, epi, rows, cols, splits):
+    ads, torch = env
+    Ab = synth.normal_bf16(2, 121, (M, K))
+    Wb = synth.normal_bf16(2, 122, ((2 * N if epi == 2 else N), K), std=0.05 if epi == 2 else 0.02)
+    base = synth.normal_f32(2, 123, (M, N))
+    runs = []
+    for _ in range(2):
+        if epi == 2:
+            C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+        elif epi == 1:
+            C = torch.from_numpy(base.copy()).cuda()
+        else:
+            C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        ads.gemm_tiled(bf16_dev(torch, Ab), bf16_dev(torch, Wb), C, epi, rows, cols, splits)
+        torch.cuda.synchronize()
+        runs.append(C.float().cpu().numpy())
+    assert np.array_equal(runs[0], runs[1]), "split sums must be deterministic"
+    got = runs[0].astype(np.float64)
+    y = ref_rows(Wb, Ab)
+    if epi == 2:
+        g, u = y[:, :N], y[:, N:]
+        ref = g / (1.0 + np.exp(-g)) * u
+        assert np.allclose(got, ref, rtol=2 ** -7, atol=1e-3 * np.abs(ref).max())
+    else:
+        ref = y if epi == 0 else base.astype(np.float64) + y
+        assert np.isfinite(got).all()
+        assert np.allclose(got, ref, rtol=1e-4, atol=2e-4 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("M,N,K,epi,rows,cols,splits", [
+    (300, 320, 1024, 1, 256, 160, 4),
+    (300, 384, 1024, 0, 256, 192, 2),
+    (260, 256, 512, 2, 256, 128, 1),
+    (45, 192, 512, 0, 128, 64, 2),
+])
+def test_gemm_tiled_fp8(env, M, N, K, epi, rows, cols, splits):
+    ads, torch = env
+    qa, sa, qa_d, sa_d = fp8_operands(torch, 131, M, K, 1.0)
+    qw, sw, qw_d, sw_d = fp8_operands(torch, 132, 2 * N if epi == 2 else N, K, 0.02)
+    base = synth.normal_f32(2, 133, (M, N))
+    if epi == 2:
+        C = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    elif epi == 1:
+        C = torch.from_numpy(base.copy()).cuda()
+    else:
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    ads.gemm_tiled(qa_d, qw_d, C, epi, rows, cols, splits, a_scale_dev=sa_d, b_scale_dev=sw_d)
+    torch.cuda.synchronize()
+    got = C.float().cpu().numpy().astype(np.float64)
+    y = ref_fp8(qa, sa, qw, sw)
+    if epi == 2:
+        g, u = y[:, :N], y[:, N:]
+        ref = g / (1.0 + np.exp(-g)) * u
+        assert np.allclose(got, ref, rtol=2 ** -6, atol=2e-3 * np.abs(ref).max())
+    else:
+        ref = y if epi == 0 else base.astype(np.float64) + y
+        assert np.allclose(got, ref, rtol=2 ** -7, atol=1e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("rows,cols,splits", [(192, 128, 1), (128, 96, 1), (256, 128, 5), (128, 64, 17)])
+def test_gemm_tiled_rejects_bad_tiles(env, rows, cols, splits):
+    """Tiles the kernel does not build (row count, width, split count, a split
+    with no k-block) are refused before any launch."""
+    ads, torch = env
+    A = torch.zeros((64, 1024), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((128, 1024), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(ads.TtsError):
+        ads.gemm_tiled(A, B, C, 0, rows, cols, splits)
