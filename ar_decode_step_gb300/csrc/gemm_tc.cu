@@ -1,23 +1,30 @@
-// BF16 GEMM on the 5th-generation tensor cores (sm_103a): C = A . B^T with
-// A [M][K] activations and B [N][K] weights, both K-major bf16, fp32
-// accumulation in tensor memory.  The batched prefill's projections
+// GEMM on the 5th-generation tensor cores (sm_103a): C = A . B^T with
+// A [M][K] activations and B [N][K] weights, both K-major bf16 (or both
+// E4M3), fp32 accumulation in tensor memory.  The batched prefill's projections
 // ("Higgs Audio v3 TTS-4B on FlashRT", Performance: "BF16 W16A16", prompt
 // prefill; section 7: the prompt runs as one M = P pass, weights read once)
 // are dense contractions of P rows against every weight matrix, so they run
 // here rather than on the M = 1 weight-streaming path.
 //
-// One CTA per 128 x BN output tile (BN = 64 or 128; 256 for the fused gate/up tile):
-//   warp 0 (one thread)  TMA producer: 128 x 64 A box and BN x 64 B box(es)
-//                        per k-block into a ring of 4-8 stages (128-byte swizzle),
-//                        completion counted on the stage's "full" mbarrier;
-//   warp 1 (one thread)  MMA issuer: four tcgen05.mma (K = 16 each) per
-//                        k-block into the TMEM accumulator, then
+// One CTA per (128 MT) x BN output tile (MT = 1 or 2 accumulators of 128
+// rows sharing each weight tile; BN = 64, 80, 128, 160 or 192; 128 gate +
+// 128 up columns for the fused gate/up tile), optionally one of S <= 4 CTAs
+// of a cluster that share the tile's K range:
+//   warp 0 (one thread)  TMA producer: (128 MT) x 64 A box and BN x 64 B
+//                        box(es) per k-block into a ring of 3-8 stages
+//                        (128-byte swizzle), completion counted on the
+//                        stage's "full" mbarrier;
+//   warp 1 (one thread)  MMA issuer: 4 MT tcgen05.mma (K = 16 each) per
+//                        k-block into the TMEM accumulators, then
 //                        tcgen05.commit frees the stage ("empty") and, after
 //                        the last block, signals "done";
 //   warp 2               allocates / frees the TMEM columns;
 //   warps 0-3            epilogue: tcgen05.ld of their 32 accumulator lanes
-//                        (one output row per thread), then store fp32, add
-//                        into fp32 (residual, split-K), or SwiGLU -> bf16.
+//                        (one output row per thread), staged in the freed
+//                        ring and written by TMA (store, or add at the
+//                        destination for the residual); SwiGLU -> bf16; with
+//                        a K split, the partial rows are first gathered and
+//                        added in rank order through distributed shared memory.
 // Every wait is bounded; on expiry the kernel records an error, lets its
 // copies and MMAs finish and frees its tensor memory before returning.
 #include <cuda.h>
