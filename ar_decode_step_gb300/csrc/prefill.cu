@@ -184,6 +184,98 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(const T* X, uin
     if (threadIdx.x == 0) scale[p] = sa;
 }
 
+// The same two quantisations with each row held in registers: one read of
+// the row, 16-byte loads and 8-byte stores (8 elements per vector, NV
+// vectors per thread); the arithmetic is that of the kernels above.
+__device__ __forceinline__ void load8(const float* x, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(x), b = *reinterpret_cast<const float4*>(x + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* x, float (&v)[8]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(x);
+    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+    v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+}
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], float sa) {
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        lo |= (uint32_t)e4m3_sat(__fdiv_rn(v[e], sa)) << (8 * e);
+        hi |= (uint32_t)e4m3_sat(__fdiv_rn(v[e + 4], sa)) << (8 * e);
+    }
+    return make_uint2(lo, hi);
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_rows_reg_kernel(const float* H,
+                                                                             const __nv_bfloat16* gamma, uint8_t* out,
+                                                                             float* scale, int hidden, float eps) {
+    __shared__ float red[32];
+    const int p = blockIdx.x, n8 = hidden / 8;
+    const float* h = H + (size_t)p * hidden;
+    float v[NV][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = threadIdx.x + i * kRowThreads;
+        if (j < n8) {
+            load8(h + 8 * j, v[i]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss += v[i][e] * v[i][e];
+        }
+    }
+    ss = block_sum(ss, red);
+    const float r = 1.0f / sqrtf(ss / (float)hidden + eps);
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = threadIdx.x + i * kRowThreads;
+        if (j < n8) {
+            float g[8];
+            load8(gamma + 8 * j, g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[i][e] = v[i][e] * r * g[e];
+                am = fmaxf(am, fabsf(v[i][e]));
+            }
+        }
+    }
+    am = block_max(am, red);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = threadIdx.x + i * kRowThreads;
+        if (j < n8) *reinterpret_cast<uint2*>(out + (size_t)p * hidden + 8 * j) = quant8(v[i], sa);
+    }
+    if (threadIdx.x == 0) scale[p] = sa;
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kRowThreads) quant_rows_reg_kernel(const T* X, uint8_t* out, float* scale, int n) {
+    __shared__ float red[32];
+    const int p = blockIdx.x, n8 = n / 8;
+    const T* x = X + (size_t)p * n;
+    float v[NV][8];
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = threadIdx.x + i * kRowThreads;
+        if (j < n8) {
+            load8(x + 8 * j, v[i]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(v[i][e]));
+        }
+    }
+    am = block_max(am, red);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j = threadIdx.x + i * kRowThreads;
+        if (j < n8) *reinterpret_cast<uint2*>(out + (size_t)p * n + 8 * j) = quant8(v[i], sa);
+    }
+    if (threadIdx.x == 0) scale[p] = sa;
+}
+
 // ---- causal GQA attention on the tensor cores --------------------------------
 // Rows [row0, row0 + 16) of the prompt against the G query heads of kv head g:
 // warp w takes query head g*G + w for the 16 rows.  Per 64-key tile,
@@ -465,18 +557,41 @@ cudaError_t launch_prefill_rmsnorm(const float* H, const __nv_bfloat16* gamma, _
 cudaError_t launch_prefill_rmsnorm_fp8(const float* H, const __nv_bfloat16* gamma, uint8_t* out, float* scale, int P,
                                        int hidden, float eps, cudaStream_t s) {
     // a CTA per row: the IEEE divisions of the quantisation spread over all its threads
+    const int nv = hidden % 8 == 0 ? (hidden / 8 + kRowThreads - 1) / kRowThreads : 0;
+#define TTS_RQ_NV(NV)                                                                                        \
+    if (nv >= 1 && nv <= NV) {                                                                               \
+        rmsnorm_quant_rows_reg_kernel<NV><<<P, kRowThreads, 0, s>>>(H, gamma, out, scale, hidden, eps);      \
+        return cudaGetLastError();                                                                           \
+    }
+    TTS_RQ_NV(2)
+    TTS_RQ_NV(4)
+    TTS_RQ_NV(6)
+#undef TTS_RQ_NV
     rmsnorm_quant_rows_kernel<<<P, kRowThreads, 0, s>>>(H, gamma, out, scale, hidden, eps);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_quant_rows(const __nv_bfloat16* X, uint8_t* out, float* scale, int P, int n,
-                                      cudaStream_t s) {
-    quant_rows_kernel<__nv_bfloat16><<<P, kRowThreads, 0, s>>>(X, out, scale, n);
+template <typename T>
+cudaError_t launch_quant_rows_t(const T* X, uint8_t* out, float* scale, int P, int n, cudaStream_t s) {
+    const int nv = n % 8 == 0 ? (n / 8 + kRowThreads - 1) / kRowThreads : 0;
+#define TTS_Q_NV(NV)                                                                 \
+    if (nv >= 1 && nv <= NV) {                                                       \
+        quant_rows_reg_kernel<T, NV><<<P, kRowThreads, 0, s>>>(X, out, scale, n);    \
+        return cudaGetLastError();                                                   \
+    }
+    TTS_Q_NV(2)
+    TTS_Q_NV(4)
+    TTS_Q_NV(6)
+#undef TTS_Q_NV
+    quant_rows_kernel<T><<<P, kRowThreads, 0, s>>>(X, out, scale, n);
     return cudaGetLastError();
 }
+cudaError_t launch_prefill_quant_rows(const __nv_bfloat16* X, uint8_t* out, float* scale, int P, int n,
+                                      cudaStream_t s) {
+    return launch_quant_rows_t(X, out, scale, P, n, s);
+}
 cudaError_t launch_prefill_quant_rows_f32(const float* X, uint8_t* out, float* scale, int P, int n, cudaStream_t s) {
-    quant_rows_kernel<float><<<P, kRowThreads, 0, s>>>(X, out, scale, n);
-    return cudaGetLastError();
+    return launch_quant_rows_t(X, out, scale, P, n, s);
 }
 
 cudaError_t launch_prefill_qk_rope_kv(const float* QKV, const __nv_bfloat16* qn, const __nv_bfloat16* kn,
