@@ -609,7 +609,8 @@ int cluster_capacity(int S, int num_sms) {
 
 // Modelled time of one tile configuration, in microseconds: whole waves of
 // CTAs, each taking its k-blocks at a per-k-block time plus ~2 us of
-// prologue and epilogue, plus ~5 us for the cluster reduction of a split.
+// prologue and epilogue, plus ~5 us (E4M3: ~8) for the cluster reduction
+// of a split.
 // The per-k-block times are fits to this kernel's timings on GB300 at
 // M = 512 (the prefill's shapes): the main loop is bound neither by L2 nor
 // by the MMAs alone but by the SM's shared-memory traffic (TMA writes plus
@@ -627,7 +628,8 @@ double tile_cost(int M, int N, int K, int epi, bool fp8, const GemmTile& t, int 
     if (epi == kGemmSwiglu) t_kb = t.mt == 2 ? 0.84 : 0.48;
     else t_kb = t.mt == 2 ? 0.30 + 0.0015 * t.bn : 0.262 + 0.00085 * t.bn;
     if (fp8) t_kb *= 1.4;
-    return (double)waves * (kb * t_kb + 2.0) + (t.splits > 1 ? 5.0 : 0.0);
+    // the reduction of an E4M3 split also scales and rounds every element
+    return (double)waves * (kb * t_kb + 2.0) + (t.splits > 1 ? (fp8 ? 8.0 : 5.0) : 0.0);
 }
 
 bool tile_ok(int M, int N, int K, int epi, bool fp8, const GemmTile& t) {
