@@ -88,9 +88,10 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def read_traffic(wl_name: str):
-    """DRAM bytes (read + write) per launch of step_kernel for this workload,
-    from the ncu summary under profiles/ (null when absent or stale)."""
+def read_traffic(wl_name: str, n_layers: int):
+    """DRAM bytes (read + write) per launch of step_kernel for this workload
+    at n_layers layers (the capture's fixed part + n_layers x its per-layer
+    part), from the ncu summary under profiles/ (null when absent or stale)."""
     p = os.path.join(ROOT, "profiles", "step_kernel_traffic.txt")
     if not os.path.exists(p):
         return None, "no ncu capture"
@@ -101,7 +102,7 @@ def read_traffic(wl_name: str):
     w = j.get("workloads", {}).get(wl_name)
     if not w:
         return None, "workload not captured"
-    return float(w["bytes_per_launch"]), j.get("method", "ncu")
+    return float(w["fixed"]) + n_layers * float(w["per_layer"]), j.get("method", "ncu")
 
 
 class ClockSampler:
@@ -349,7 +350,8 @@ def run_gpu(args, wl_name, wl):
     peak, peak_kind = read_peaks()
     persistent = os.environ.get("TTS_STEP_MODE", "") != "kernels"
     achieved = mean_bytes / (ms_per_step * 1e-3) / 1e9
-    traffic, traffic_note = read_traffic(wl_name) if persistent else (None, "not captured for separate kernels")
+    traffic, traffic_note = (read_traffic(wl_name, d.n_layers) if persistent
+                             else (None, "not captured for separate kernels"))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "kernel": "step_kernel (whole decode step, one launch per frame)"
                 if persistent else "whole step as separate kernels (per-frame graph)",
