@@ -249,6 +249,21 @@ def run_reference(args, wl_name, wl):
 # The GPU arm
 # ----------------------------------------------------------------------------
 
+def replica_timing(ms_local: float, steps: int, dist=None, device: str = "cpu"):
+    """The timed region over all replicas and the whole-job frames/s.  Every
+    rank decodes `steps` frames of its own model copy (replicas: no data is
+    exchanged); the job's time is the slowest rank's (all_reduce MAX of the
+    event-timed milliseconds), the value all ranks' frames over that time."""
+    ms, world = ms_local, 1
+    if dist is not None:
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * steps / (ms / 1e3)
+
+
 def run_gpu(args, wl_name, wl):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -322,17 +337,12 @@ def run_gpu(args, wl_name, wl):
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, value = replica_timing(ev0.elapsed_time(ev1), args.steps, dist, "cuda")
     time.sleep(0.25)
     clocks.stop()
     clock_info = clocks.summary(t_wall0 - 0.05, t_wall1 + 0.05)
 
     ms_per_step = ms_total / args.steps
-    value = world * args.steps / (ms_total / 1e3)
 
     # roofline of the dominant kernel.  Persistent mode: the step is one launch
     # of step_kernel per frame, so its mean duration is the timed region / frames
