@@ -168,3 +168,29 @@ def test_errors_leave_state_unchanged(ads):
     dec.reset()
     assert dec.state() == (0, 0, -1)
     dec.close()
+
+
+def test_prefill_edge_sizes(ads):
+    """An empty prompt is a no-op; a prompt that fills the cache exactly is
+    accepted, after which the next frame has no position left."""
+    d = reduced_dims(1)
+    w = synth.make_weights(d)
+    dw = ads.DeviceWeights(w)
+    a = ads.Decoder(to_binding_dims(d), dw, 16)
+    b = ads.Decoder(to_binding_dims(d), dw, 16)
+    prompt = synth.delayed_prompt_codes(6)
+    a.prefill(np.zeros((0, 8), np.int32))
+    assert a.state() == (0, 0, -1)
+    a.prefill(prompt)
+    b.prefill(prompt)
+    assert np.array_equal(a.decode_steps(3), b.decode_steps(3))
+    a.close()
+    b.close()
+    full = ads.Decoder(to_binding_dims(d), dw, 16)
+    full.prefill(synth.delayed_prompt_codes(16))
+    assert full.state()[0] == 16
+    with pytest.raises(ads.TtsError) as e:
+        full.decode_step()
+    assert e.value.status == -3
+    assert full.state()[0] == 16
+    full.close()
