@@ -605,8 +605,11 @@ int prefill_chunk(tts_ctx* c, const int* d_codes, int pos0, int P, float* snap =
 
 // One batched prefill chunk, replayed from a captured graph once its shape
 // has run before (the first run also does the lazy set-up: buffers, kernel
-// attributes): the ~250 launches of a 36-layer chunk then cost one.
+// attributes): the ~290 launches of a 36-layer chunk then cost one.  At most
+// kMaxPrefillGraphs graphs are kept; the record of shapes seen once is
+// bounded too (cleared when full).
 constexpr size_t kMaxPrefillGraphs = 16;
+constexpr size_t kMaxPrefillSeen = 1024;
 int run_prefill_chunk(tts_ctx* c, int r, int pos0, int rows) {
     const int* d_codes = c->prompt + (size_t)r * c->cfg.n_codebooks;
     const auto key = std::make_tuple(pos0, rows, r);
@@ -616,6 +619,7 @@ int run_prefill_chunk(tts_ctx* c, int r, int pos0, int rows) {
         return TTS_OK;
     }
     if (!c->pf_seen.count(key) || c->pf_graphs.size() >= kMaxPrefillGraphs) {
+        if (c->pf_seen.size() >= kMaxPrefillSeen) c->pf_seen.clear();
         c->pf_seen.insert(key);
         return prefill_chunk(c, d_codes, pos0, rows);
     }
