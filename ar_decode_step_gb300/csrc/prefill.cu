@@ -44,6 +44,12 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_rows_kernel(const float* 
         out[(size_t)p * hidden + i] = __float2bfloat16_rn(h[i] * r * __bfloat162float(gamma[i]));
 }
 
+// two floats as bf16 (nearest even), the first in the low half: 8-byte cache stores
+__device__ __forceinline__ uint32_t pack_bf16x2_rows(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const float* QKV, const __nv_bfloat16* qn,
                                                                       const __nv_bfloat16* kn, const float2* rope,
                                                                       float* Q, __nv_bfloat16* kc,
@@ -60,10 +66,7 @@ __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const floa
         if (hd >= n_q + n_kv) {  // v head: straight to the cache
             const int j = hd - n_q - n_kv;
             __nv_bfloat16* dst = vc + ((size_t)j * max_pos + pos) * kHeadDim + 4 * lane;
-            dst[0] = __float2bfloat16_rn(v.x);
-            dst[1] = __float2bfloat16_rn(v.y);
-            dst[2] = __float2bfloat16_rn(v.z);
-            dst[3] = __float2bfloat16_rn(v.w);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2_rows(v.x, v.y), pack_bf16x2_rows(v.z, v.w));
             continue;
         }
         // RMSNorm over the head (gain q_norm / k_norm), then rotate-half RoPE:
@@ -86,8 +89,7 @@ __global__ void __launch_bounds__(kRowThreads) qk_rope_kv_rows_kernel(const floa
         } else {
             const int j = hd - n_q;
             __nv_bfloat16* dst = kc + ((size_t)j * max_pos + pos) * kHeadDim + 4 * lane;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) dst[jj] = __float2bfloat16_rn(o[jj]);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2_rows(o[0], o[1]), pack_bf16x2_rows(o[2], o[3]));
         }
     }
 }
