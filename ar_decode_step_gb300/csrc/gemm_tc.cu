@@ -725,6 +725,7 @@ int gemm_entry(const void* A, const void* B, const float* a_scale, const float* 
     if (fp8 && (!a_scale || !b_scale)) return TTS_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15)
         return TTS_ERR_ARG;
+    if (t.mt != 0 && !tile_ok(M, N, K, epi, fp8, t)) return TTS_ERR_ARG;  // before any device call
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return TTS_ERR_CUDA;

@@ -77,3 +77,32 @@ def test_calls_without_context(lib):
     assert lib.tts_reset(None) == -6
     assert lib.tts_shutdown(None) == 0
     assert lib.tts_quantize_fp8_weight(None, 4, 4, None, None, None) == -1
+
+
+def test_gemm_tiled_rejects_bad_tiles_before_any_device_call(lib):
+    """Host validation of tts_gemm_tiled: pointers are checked for NULL and
+    16-byte alignment, the tile (rows, width, K split, one k-block per
+    split) against the shape; none of these reach the device."""
+    P = ctypes.c_void_p(0x1000)  # aligned stand-ins, never dereferenced
+    f = lib.tts_gemm_tiled
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    ok_shape = (256, 1024)  # N, K
+    bad = [
+        (192, 128, 1),   # 192-row tile
+        (128, 96, 1),    # width not built
+        (256, 128, 5),   # K split over 5
+        (128, 64, 17),   # more splits than k-blocks (16)
+        (256, 192, 1),   # N = 256 not a multiple of 192
+    ]
+    for rows, cols, splits in bad:
+        assert f(P, P, None, None, P, 64, ok_shape[0], ok_shape[1], 0, 0, rows, cols, splits, None) == -1, (rows, cols)
+    # SwiGLU: 128 + 128 columns only, no K split
+    assert f(P, P, None, None, P, 64, 256, 1024, 2, 0, 128, 64, 1, None) == -1
+    assert f(P, P, None, None, P, 64, 256, 1024, 2, 0, 128, 128, 2, None) == -1
+    # E4M3: scales required, K a multiple of 128
+    assert f(P, P, None, None, P, 64, 256, 1024, 0, 1, 128, 128, 1, None) == -1
+    assert f(P, P, P, P, P, 64, 256, 1088, 0, 1, 128, 128, 1, None) == -1
+    # misaligned or NULL operands
+    assert f(ctypes.c_void_p(0x1008), P, None, None, P, 64, 256, 1024, 0, 0, 128, 128, 1, None) == -1
+    assert f(None, P, None, None, P, 64, 256, 1024, 0, 0, 128, 128, 1, None) == -1
