@@ -35,7 +35,12 @@ class tts_config(ctypes.Structure):
                 ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "inter",
                  "n_codebooks", "cb_vocab", "max_pos")] + \
                [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
-                ("precision", ctypes.c_int), ("stream", ctypes.c_void_p)]
+                ("precision", ctypes.c_int), ("stream", ctypes.c_void_p), ("options", ctypes.c_int)]
+
+
+# tts_config.options bits
+OPT_SEPARATE_KERNELS = 1
+OPT_PREFILL_STEPS = 2
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -77,6 +82,7 @@ SIGNATURES = {
     "tts_gemm_fp8": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "tts_gemm_tiled": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "tts_debug_prefill_states": (_I, [_VP, _VP, _I, _VP, ctypes.c_longlong]),
+    "tts_debug_expire_wait": (_I, [_VP]),
     "tts_quantize_fp8_weight": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
     "tts_attention_decode": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
     "tts_attention_decode_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _F, _VP]),
@@ -252,12 +258,12 @@ class DeviceWeights:
 class Decoder:
     """One tts_ctx: KV cache, scratch and the captured decode-step graph."""
 
-    def __init__(self, dims, weights: DeviceWeights, max_pos: int, stream=None):
+    def __init__(self, dims, weights: DeviceWeights, max_pos: int, stream=None, options: int = 0):
         self.dims = dims
         self.weights = weights
         cfg = tts_config(dims.n_layers, dims.hidden, dims.n_q, dims.n_kv, dims.head_dim, dims.inter,
                          dims.n_cb, dims.cb_vocab, max_pos, dims.rms_eps, dims.rope_theta,
-                         weights.precision, stream)
+                         weights.precision, stream, options)
         self._cfg = cfg
         self._w = weights.struct()
         self._ctx = ctypes.c_void_p()
@@ -407,6 +413,12 @@ class Decoder:
         buf = np.zeros(n, np.float32)
         _call("tts_debug_prefill_states", self._ctx, _ptr(c), P, _ptr(buf), n)
         return buf.reshape(self.dims.n_layers + 1, P, self.dims.hidden)
+
+    def debug_expire_wait(self) -> int:
+        """tts_debug_expire_wait: one step launch whose first grid barrier
+        cannot complete and whose waits give up after 1 ms; returns the
+        status code (TTS_ERR_DEVICE, -5, when the timeout was detected)."""
+        return int(load().tts_debug_expire_wait(self._ctx))
 
     def last_steps_ms(self) -> float:
         ms = ctypes.c_float()

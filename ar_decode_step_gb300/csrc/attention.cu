@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_decode_kernel(const AttnPara
     const int t1 = min(len, t0 + chunk);
     const bool has_new = (t1 == len);  // this split ends at the current position
 
-    const float2* rope = p.rope + (size_t)pos * (kHeadDim / 2);
+    const float2* rope = p.rope_row ? p.rope_row : p.rope + (size_t)pos * (kHeadDim / 2);
     const float scale = 1.0f / sqrtf((float)kHeadDim);
 
     // q/k RMSNorm over head_dim then rotate-half RoPE: lane l holds dims
@@ -209,6 +209,16 @@ __global__ void __launch_bounds__(kWarps * 32) attn_decode_kernel(const AttnPara
 }
 
 }  // namespace
+
+cudaError_t attention_prepare() {
+    // querying a kernel's attributes loads its module on the current device
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, attn_decode_kernel<1>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, attn_decode_kernel<2>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, attn_decode_kernel<4>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, attn_decode_kernel<8>);
+    return e;
+}
 
 int attn_splits_for(int max_pos) {
     int s = (max_pos + kMinChunk - 1) / kMinChunk;

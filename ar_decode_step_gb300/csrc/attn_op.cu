@@ -68,10 +68,8 @@ cudaError_t run_attention(char* scratch, const AttnScratch& L, const float* qkv,
     a.qkv = qkv;
     a.q_norm = static_cast<const __nv_bfloat16*>(qn);
     a.k_norm = static_cast<const __nv_bfloat16*>(kn);
-    // the kernel reads table row `pos`; hand it a base address pos rows before
-    // the single row held in scratch (only that row is ever dereferenced)
-    a.rope = reinterpret_cast<const float2*>(reinterpret_cast<uintptr_t>(scratch + L.rope) -
-                                             (uintptr_t)pos * (kHeadDim / 2) * sizeof(float2));
+    a.rope = nullptr;
+    a.rope_row = reinterpret_cast<const float2*>(scratch + L.rope);  // the one row of this position
     a.kc = static_cast<__nv_bfloat16*>(kc);
     a.vc = static_cast<__nv_bfloat16*>(vc);
     a.out = out;
@@ -126,9 +124,16 @@ extern "C" int tts_attention_decode(const float* qkv, const void* q_norm, const 
 // caller holding no allocator of its own (an embedded or real-time host loop
 // that must never hit cudaMalloc's implicit synchronisation or failure), or a
 // process whose allocations are frozen after start-up.  This entry point takes
-// its scratch from one fixed array in device global memory instead.  The
-// array exists on every GPU that loads the library and stays there until the
-// process exits.
+// its scratch from one fixed array in device global memory instead.
+//
+// The array belongs to this file's device module.  Under lazy module loading
+// (the CUDA default) a module is loaded on a device -- and its global arrays
+// created there -- the first time the process touches it on that device: here
+// that is the address lookup below, and the attention kernel's module loads on
+// its first launch.  Both can allocate, so the first call on each device
+// belongs to the caller's set-up, while allocation is still allowed (tts_init
+// also performs the lookup for its device).  After that the array stays until
+// the process exits or the device is reset.
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -139,9 +144,16 @@ constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 void* g_static_addr[kMaxDevices] = {};
 
+}  // namespace
+
+namespace tts {
+
 // Device address of the array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached.  A device reset
+// (cudaDeviceReset) unloads the module, which makes the cached address stale:
+// a process that resets a device must not call the allocation-free entry
+// point on that device afterwards.
 int static_scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TTS_ERR_CUDA;
@@ -161,7 +173,7 @@ int static_scratch_address(void** out) {
     return TTS_OK;
 }
 
-}  // namespace
+}  // namespace tts
 
 extern "C" int tts_attention_decode_noalloc(const float* qkv, const void* q_norm, const void* k_norm,
                                             void* k_cache, void* v_cache, float* out, int n_q, int n_kv,

@@ -5,7 +5,7 @@
 // residual, fused codebook head) as its own kernel, built from the shared
 // blocks in gemv_core.cuh: a producer warp streams the CTA's row range of
 // the weights through a ring of 32-40 KB shared-memory stages (one bulk copy
-// each, TMA engine, L2 evict-first) and sixteen consumer warps reduce them
+// each, TMA engine, L2 evict-first) and eight consumer warps reduce them
 // against the staged activation vector.  The producer starts before
 // griddepcontrol.wait (weights do not depend on the previous kernel) and,
 // once its own copies are out, warms L2 with the leading part of the next

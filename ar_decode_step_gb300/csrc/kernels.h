@@ -106,7 +106,8 @@ struct AttnParams {
     const float* qkv;            // [(n_q + 2 n_kv) * 128] fp32
     const __nv_bfloat16* q_norm; // [128]
     const __nv_bfloat16* k_norm; // [128]
-    const float2* rope;          // [max_pos][64] (cos, sin)
+    const float2* rope;          // [max_pos][64] (cos, sin), row pos used; or null when rope_row is set
+    const float2* rope_row;      // if non-null: the (cos, sin) row [64] of this call's position itself
     __nv_bfloat16* kc;           // this layer's K cache [n_kv][max_pos][128]
     __nv_bfloat16* vc;
     float* out;                  // [n_q * 128] fp32
@@ -119,7 +120,12 @@ struct AttnParams {
     float eps;
 };
 int attn_splits_for(int max_pos);
+cudaError_t attention_prepare();  // load the attention kernels' module on the current device
 cudaError_t launch_attention(const AttnParams& p, const LaunchCfg& lc, cudaStream_t s);
+// Device address of the allocation-free attention entry point's static
+// scratch on the current device (looked up once per device, then cached).
+// Returns a TTS_* status.
+int static_scratch_address(void** out);
 
 // h = sum_k E_k[codes[k]], codes read from st->codes (or from `rows` when
 // non-NULL: row st->prefill_row of a [P][n_cb] prompt).
@@ -197,6 +203,12 @@ struct StepParams {
     // optional (traced launches): the residual stream after the embedding and
     // after every layer, [n_layers + 1][hidden] fp32
     float* hsnap;
+    // bound on each grid-barrier wait in ns (0: kWaitLimitNs), and a count
+    // added to every grid barrier's arrival target (0 on the product path; a
+    // test hook sets 1 so that the first barrier cannot complete and the
+    // bounded wait runs out)
+    unsigned long long wait_limit_ns;
+    unsigned bar_target_extra;
 };
 
 // Phase-trace layout of the persistent kernel, per CTA (see step.cu):

@@ -4,7 +4,7 @@
 // each CTA streams, back to back, every weight range the CTA owns over the
 // whole step -- QKV, O-proj, gate/up, down-proj of layer 0, then layer 1, ...,
 // then the codebook head -- through its ring of shared-memory stages, never
-// waiting on anything but free ring slots.  The sixteen consumer warps walk
+// waiting on anything but free ring slots.  The eight consumer warps walk
 // the phases of the step ("Higgs Audio v3 TTS-4B on FlashRT", section 5):
 //
 //   embed:   h = sum_k E_k[c_k] (this CTA's slice)               -> grid barrier
@@ -38,8 +38,10 @@ constexpr int kAttnMinChunk = 32;   // positions per attention split, at least (
 
 // Grid barrier among the consumer warps of all CTAs.  `gbar` counts arrivals
 // over the launch (zeroed before it); barrier k (1-based) waits for
-// k * gridDim.x.  Returns false if the wait ran out or another CTA failed.
-__device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned target, DevState* st, volatile int* abort) {
+// k * gridDim.x.  Returns false if the wait ran out (after limit_ns) or
+// another CTA failed.
+__device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned target, DevState* st, volatile int* abort,
+                                             uint64_t limit_ns) {
     consumer_sync();  // every consumer thread's writes of this phase precede the release below
     if (threadIdx.x == 0) {
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
@@ -53,7 +55,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned target, De
                 }
                 const uint64_t t = globaltimer_ns();
                 if (!t0) t0 = t;
-                else if (t - t0 > kWaitLimitNs) {
+                else if (t - t0 > limit_ns) {
                     atomicOr(&st->err, kErrTimeout);
                     *abort = 1;
                     break;
@@ -630,7 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         return;
     }
     unsigned nbar = 0;
-    auto barrier = [&]() { return grid_barrier(p.gbar, ++nbar * gridDim.x, p.st, &s_abort); };
+    const uint64_t bar_limit = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
+    auto barrier = [&]() {
+        return grid_barrier(p.gbar, ++nbar * gridDim.x + p.bar_target_extra, p.st, &s_abort, bar_limit);
+    };
 
     // embed: this CTA's slice of h = sum_k E_k[c_k]
     {

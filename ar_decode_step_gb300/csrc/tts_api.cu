@@ -125,6 +125,7 @@ int validate(const tts_config* c, const tts_weights* w) {
     if (c->max_pos < 1 || c->max_pos > 65536) return TTS_ERR_ARG;
     if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return TTS_ERR_ARG;
     if (c->precision != TTS_BF16 && c->precision != TTS_FP8) return TTS_ERR_ARG;
+    if (c->options & ~(TTS_OPT_SEPARATE_KERNELS | TTS_OPT_PREFILL_STEPS)) return TTS_ERR_ARG;
     if (!aligned16(w->embed) || !aligned16(w->head) || !aligned16(w->final_norm)) return TTS_ERR_ARG;
     if (!w->wqkv || !w->wo || !w->wgu || !w->wd || !w->ln_in || !w->ln_post || !w->q_norm || !w->k_norm)
         return TTS_ERR_ARG;
@@ -194,10 +195,16 @@ void set_next(const tts_ctx* c, GemvParams& g, int kind, int l, size_t pf_bytes)
     g.next_pf = pf_bytes;
 }
 
-size_t env_kb(const char* name, size_t dflt) {
-    const char* v = std::getenv(name);
-    return (v && *v) ? (size_t)std::strtoul(v, nullptr, 10) * 1024 : dflt * 1024;
-}
+// Separate-kernel mode: bytes of the next projection's weights each GEMV CTA
+// asks L2 for once its own copies are out (after the QKV GEMV, for the
+// attention kernel that follows: more, since attention streams no weights).
+constexpr size_t kGemvPrefetchBytes = 96 * 1024;
+constexpr size_t kGemvPrefetchAttnBytes = 160 * 1024;
+// Persistent kernel: how many ring stages the L2 prefetch cursor runs ahead
+// of the copies, and how far it may run ahead while the ring is full
+// (measured: 4 and 12 stages).
+constexpr int kStepPrefetchStages = 4;
+constexpr int kStepPrefetchMax = 12;
 
 // Persistent form: zero the grid-barrier counter, then one cooperative launch.
 int record_step_persistent(tts_ctx* c, cudaStream_t s, bool decode) {
@@ -215,7 +222,7 @@ int record_step(tts_ctx* c, cudaStream_t s, bool decode) {
     if (c->persistent) return record_step_persistent(c, s, decode);
     const tts_config& k = c->cfg;
     const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
-    const size_t pf = env_kb("TTS_PF_KB", 96), pf_attn = env_kb("TTS_PF_ATTN_KB", 160);
+    const size_t pf = kGemvPrefetchBytes, pf_attn = kGemvPrefetchAttnBytes;
     EmbedParams ep{c->embed, c->st, decode ? nullptr : c->prompt, c->h, k.n_codebooks, k.cb_vocab, k.hidden};
     TTS_CK(launch_embed(ep, LaunchCfg{0, 0, false}, s));
     for (int l = 0; l < k.n_layers; ++l) {
@@ -398,13 +405,9 @@ int setup_persistent(tts_ctx* c) {
     p.n_cb = k.n_codebooks; p.cb_vocab = k.cb_vocab; p.max_pos = k.max_pos;
     p.S = c->S;
     p.eps = k.rms_eps;
-    {
-        // L2 prefetch lookahead in ring stages: steady state, and while the ring is full
-        const char* v = std::getenv("TTS_PF_STAGES");
-        p.pf_stages = (v && *v) ? std::max(0, std::atoi(v)) : 4;
-        const char* vm = std::getenv("TTS_PF_MAX");
-        p.pf_max = std::max(p.pf_stages, (vm && *vm) ? std::atoi(vm) : 12);
-    }
+    // L2 prefetch lookahead in ring stages: steady state, and while the ring is full
+    p.pf_stages = kStepPrefetchStages;
+    p.pf_max = kStepPrefetchMax;
     return TTS_OK;
 }
 
@@ -416,10 +419,15 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     c->attn_dim = k.n_q_heads * kHeadDim;
     c->G = k.n_q_heads / k.n_kv_heads;
     c->S = attn_splits_for(k.max_pos);
-    const char* nopdl = std::getenv("TTS_NO_PDL");
-    c->pdl = !(nopdl && nopdl[0] == '1');
 
     TTS_CK(cudaGetDevice(&c->device));
+    {
+        // load the allocation-free attention entry point's modules (its static
+        // scratch and its kernel) on this device now, while allocating is allowed
+        void* scratch = nullptr;
+        TTS_TRY(static_scratch_address(&scratch));
+        TTS_CK(attention_prepare());
+    }
     TTS_CK(gemv_prepare());
     TTS_CK(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
     TTS_CK(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking));
@@ -479,13 +487,10 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
             }
         TTS_CK(cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
     }
-    {
-        const char* mode = std::getenv("TTS_STEP_MODE");
-        c->persistent = !(mode && std::strcmp(mode, "kernels") == 0);
-        // TTS_PREFILL=steps runs a prompt position by position through the decode step instead
-        const char* pf = std::getenv("TTS_PREFILL");
-        c->batched_prefill = !(pf && std::strcmp(pf, "steps") == 0);
-    }
+    // options: the step as a graph of separate kernels instead of the
+    // persistent kernel; prompts position by position through the decode step
+    c->persistent = (k.options & TTS_OPT_SEPARATE_KERNELS) == 0;
+    c->batched_prefill = (k.options & TTS_OPT_PREFILL_STEPS) == 0;
     // the persistent kernel keeps a normalised activation in registers while
     // its statistics arrive: longer hidden sizes take the graph of kernels
     if (c->cfg.hidden > kMaxRmsK || c->attn_dim > kMaxPlainK || c->cfg.inter > kMaxPlainK) c->persistent = false;
@@ -1006,7 +1011,7 @@ int tts_time_gemv(tts_ctx* ctx, int kind, int reps, float* ms_per_launch) {
     const int prec = (kind == kHead || k.precision == TTS_BF16) ? kBF16 : kFP8;
     const int pro = (kind == kO || kind == kDown) ? kProPlain : kProRms;
     const int epi = kind == kGU ? kEpiSwiglu : ((kind == kO || kind == kDown) ? kEpiResid : kEpiStore);
-    const size_t pf = env_kb("TTS_PF_KB", 96);
+    const size_t pf = kGemvPrefetchBytes;
     TTS_CK(cudaEventRecord(ctx->ev0, ctx->stream));
     for (int r = 0; r < reps; ++r)
         for (int l = 0; l < k.n_layers; ++l) {
@@ -1125,6 +1130,21 @@ int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* h
     s.prefill_row = 0;
     for (int i = 0; i < kMaxCodebooks; ++i) s.codes[i] = k.cb_vocab - 2;
     return push_state(ctx, s);
+}
+
+int tts_debug_expire_wait(tts_ctx* ctx) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!ctx->persistent) return TTS_ERR_UNSUPPORTED;
+    const tts_config& k = ctx->cfg;
+    if (ctx->pos >= k.max_pos) return TTS_ERR_FULL;
+    StepParams p = ctx->sp;
+    p.decode = 1;
+    p.wait_limit_ns = 1000ull * 1000ull;  // 1 ms
+    p.bar_target_extra = 1;               // the first grid barrier waits for one arrival too many
+    const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
+    TTS_CK(cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream));
+    TTS_CK(launch_step(p, prec, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream));
+    return pull_state(ctx);
 }
 
 int tts_quantize_fp8_weight(const void* W, int N, int K, void* W8, float* s, void* stream) {

@@ -53,6 +53,17 @@ enum {
 
 enum { TTS_BF16 = 0, TTS_FP8 = 1 };
 
+/* tts_config.options bits (0 = the default decode and prefill paths). */
+enum {
+    /* Run each decode step as a graph of one kernel per projection, attention
+     * and head (programmatic-dependent-launch edges) instead of the one
+     * persistent step kernel.  Kept for per-projection timing; slower. */
+    TTS_OPT_SEPARATE_KERNELS = 1,
+    /* Prefill a prompt position by position through the decode step kernel
+     * instead of the batched tensor-core pass. */
+    TTS_OPT_PREFILL_STEPS = 2
+};
+
 typedef struct tts_ctx tts_ctx;
 
 /* Model and run configuration.  Supported shapes: head_dim 128; n_q_heads a
@@ -75,6 +86,7 @@ typedef struct {
     float rope_theta;  /* 1e6 */
     int precision;     /* TTS_BF16 (W16, fp32 activations) or TTS_FP8 (E4M3 W8A8) */
     void* stream;      /* cudaStream_t; NULL = default stream */
+    int options;       /* TTS_OPT_* bits; 0 for the default paths */
 } tts_config;
 
 /* Device pointers to the weights (borrowed).  The per-layer members are HOST
@@ -280,6 +292,18 @@ int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes
  * otherwise as tts_prefill.  Synchronises. */
 int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* host_h, long long capacity);
 
+/* Test hook for failure detection (not part of the product path): one launch
+ * of the persistent step kernel, outside the graph, whose first grid barrier
+ * waits for one arrival more than the grid has and whose barrier waits give
+ * up after 1 ms instead of 1 s.  The wait runs out, the kernel records the
+ * timeout in the device error word, every CTA leaves at its next barrier or
+ * ring wait, the copies in flight land, and the launch ends; no spin is left
+ * running.  Returns TTS_ERR_DEVICE (the error word is cleared again);
+ * position, frame and cache are left as they were, so the next step runs
+ * normally.  TTS_ERR_UNSUPPORTED when the step runs as separate kernels.
+ * Synchronises the stream. */
+int tts_debug_expire_wait(tts_ctx* ctx);
+
 /* Stand-alone op: C = A . B^T on the tensor cores (tcgen05 MMA, TMEM
  * accumulators, TMA-staged operands), the GEMM of the batched prompt prefill
  * ("Higgs Audio v3 TTS-4B on FlashRT", Performance "BF16 W16A16" and section
@@ -358,18 +382,25 @@ int tts_attention_decode(const float* qkv, const void* q_norm, const void* k_nor
  * runtime's fixed memory budget, host loops that must not block on or fail in
  * cudaMalloc, or processes that freeze allocation after start-up.  The paper
  * has no counterpart; this is a library-level variant.
- * Same arguments, layouts and result as tts_attention_decode.  Its scratch (the
- * split partials, tickets, a state word and the RoPE row) lives in one static
- * device array of 2 MiB per GPU, held from library load until process exit.
- * Requests needing more (about n_q * min(64, ceil(max_pos/16)) * 520 bytes)
- * are rejected with TTS_ERR_ARG and a message on stderr; nothing is launched.
- * The first call on each device looks up the array's device address (with
- * that device current) and caches it: make that first call before any stream
- * capture.  Every call shares the one array, and each call clears the tickets
- * and state word before launching, so calls that overlap on the GPU (on
- * different streams, or without ordering) race on it: serialise them.  No
- * cudaMalloc, cudaFree or other allocating routine is called.  Synchronises
- * the stream. */
+ * Same arguments, layouts and result as tts_attention_decode (bit for bit:
+ * the same kernel, split count and merge order).  Its scratch (the split
+ * partials, tickets, a state word and the RoPE row) lives in one static
+ * device array of 2 MiB per GPU.  Requests needing more (about
+ * n_q * min(64, ceil(max_pos/16)) * 520 bytes) are rejected with
+ * TTS_ERR_ARG and a message on stderr; nothing is launched.
+ * Set-up: under lazy module loading (the CUDA default) the array is created
+ * on a device when its module is first loaded there, which happens at the
+ * first lookup of its address; the attention kernel's module loads on its
+ * first launch.  Both may allocate device memory.  The first call of this
+ * entry point on a device does both (and caches the address), and so does
+ * tts_init for its device: make one of them part of start-up, while
+ * allocation is still allowed.  A device reset unloads the module; do not
+ * call this entry point on a device after resetting it.  The call
+ * synchronises the stream.  Every call shares the one array; each call
+ * clears the tickets and state word before launching, so calls that overlap
+ * on the GPU (on different streams, or without ordering) race on it:
+ * serialise them.  No cudaMalloc, cudaFree or other allocating routine is
+ * called. */
 int tts_attention_decode_noalloc(const float* qkv, const void* q_norm, const void* k_norm, void* k_cache,
                                  void* v_cache, float* out, int n_q, int n_kv, int max_pos, int pos,
                                  float eps, float rope_theta, void* stream);

@@ -54,7 +54,7 @@ def test_status_strings(lib):
 
 def test_host_validation_rejects_bad_config(lib):
     import ar_decode_step_gb300 as m
-    cfg = m.tts_config(36, 2560, 32, 8, 128, 9728, 8, 1026, 256, 1e-6, 1e6, 0, None)
+    cfg = m.tts_config(36, 2560, 32, 8, 128, 9728, 8, 1026, 256, 1e-6, 1e6, 0, None, 0)
     w = m.tts_weights()
     ctx = ctypes.c_void_p()
     # NULL weights
@@ -62,7 +62,7 @@ def test_host_validation_rejects_bad_config(lib):
     assert lib.tts_init(None, ctypes.byref(w), ctypes.byref(ctx)) == -1
     assert lib.tts_init(ctypes.byref(cfg), ctypes.byref(w), None) == -1
     for field, bad in (("head_dim", 64), ("n_q_heads", 30), ("hidden", 2500), ("max_pos", 0),
-                       ("precision", 3), ("n_codebooks", 9), ("inter", 20000)):
+                       ("precision", 3), ("n_codebooks", 9), ("inter", 20000), ("options", 4)):
         c2 = m.tts_config.from_buffer_copy(cfg)
         setattr(c2, field, bad)
         assert lib.tts_init(ctypes.byref(c2), ctypes.byref(w), ctypes.byref(ctx)) == -1, field
