@@ -236,7 +236,10 @@ class Oracle:
     """Holds a model (host bf16 images from ``synth.make_weights``), its own
     FP8 quantisation when precision == 1, and a KV cache."""
 
-    def __init__(self, weights, max_pos: int, precision: int = 0):
+    def __init__(self, weights, max_pos: int, precision: int = 0, share: "Oracle" = None):
+        """share: another Oracle of the same weights and precision whose FP8
+        weight quantisation this one reuses (saves the quantisation pass and
+        its memory; each instance keeps its own cache and state)."""
         d = weights.dims
         self.dims = d
         self.w = weights
@@ -257,10 +260,13 @@ class Oracle:
         cw.wqkv, cw.wo, cw.wgu, cw.wd = (parr(weights.wqkv), parr(weights.wo),
                                          parr(weights.wgu), parr(weights.wd))
         if precision == 1:
-            self.q = {}
-            for name in ("wqkv", "wo", "wgu", "wd"):
-                qs = [quant_weight(m) for m in getattr(weights, name)]
-                self.q[name] = qs
+            if share is not None:
+                assert share.w is weights and share.precision == 1
+                self.q = share.q
+            else:
+                self.q = {}
+                for name in ("wqkv", "wo", "wgu", "wd"):
+                    self.q[name] = [quant_weight(m) for m in getattr(weights, name)]
             cw.qqkv, cw.qo, cw.qgu, cw.qd = (parr([x[0] for x in self.q[n]])
                                              for n in ("wqkv", "wo", "wgu", "wd"))
             cw.sqkv, cw.so, cw.sgu, cw.sd = (parr([x[1] for x in self.q[n]])

@@ -11,20 +11,23 @@ the 8 codes) against the CPU oracle run on the same seeded inputs:
 The oracle runs these full-size frames in fp64 on the host cores (tens of
 seconds).
 
-FP8 at full depth is checked layer by layer: the oracle's layer l starts from
-the GPU's own input to layer l (the traced step kernel records the residual
-stream after every layer) and the layer's contribution h_{l+1} - h_l must
-agree within the FP8 bar; the head is checked on the GPU's final stream.  A
-frame-level comparison is not meaningful at 36 FP8 layers: fp32 accumulation
-in any order flips some bf16-rounded projection outputs against the oracle's
-exact sums, and the per-token FP8 re-quantisation of every layer amplifies
-those flips (the oracle with only its FP8 sums taken sequentially in fp32
-already differs from itself by logits cos 0.992 at 36 layers)."""
+FP8 at full depth is checked twice.  Layer by layer, strictly: the oracle's
+layer l starts from the GPU's own input to layer l (the traced step kernel
+records the residual stream after every layer) and the layer's contribution
+h_{l+1} - h_l must reach the FP8 bar; the head is checked on the GPU's final
+stream with the BF16 bar.  And frame by frame, against the measured spread of
+fp32 implementations: over 36 FP8 layers any fp32 rounding difference is
+amplified by the bf16-rounded outputs and the per-token E4M3
+re-quantisation of every layer, so no fp32 implementation reaches the 0.999
+frame bar against the fp64 oracle (test_fp8_order_sensitivity.py).  The
+float32 restatement runs the same frames in three variants, and the GPU's
+frame cosines and code mismatches must be no worse than theirs."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
+from fp8_restatement import ORDERS, Fp8Fp32Step, frame_stats
 from helpers import adopt_gpu_cache, check_frame, check_kv_rows, cosine, to_binding_dims, upload_kv
 
 pytestmark = pytest.mark.gpu
@@ -116,16 +119,25 @@ def layerwise(orc, hs, pos, bar, where):
 def test_full36_fp8_kv1024(ads, full_weights):
     d, w = full_weights
     L = 1024
-    max_pos = L + 4
+    frames = 4
+    max_pos = L + frames + 1
     dw = ads.DeviceWeights(w, precision=1)
     dec = ads.Decoder(to_binding_dims(d), dw, max_pos)
-    orc = oracle.Oracle(w, max_pos, precision=1)
+    orc = oracle.Oracle(w, max_pos, precision=1)            # layer by layer from the GPU's inputs
+    orc_f = oracle.Oracle(w, max_pos, precision=1, share=orc)  # whole frames
     k, v = synth.make_kv_prefix(d, L, max_pos)
     kd, vd = upload_kv(k, v, L)
     dec.set_kv(kd, vd, L)
     orc.set_kv(k, v, L)
+    orc_f.set_kv(k, v, L)
     del kd, vd
-    for f, cin in enumerate([np.full(8, 1024, np.int32), synth.random_codes(1, seed=2, stream=9)[0]]):
+    refs = {}
+    for order in ORDERS:
+        refs[order] = Fp8Fp32Step(w, max_pos, order, share=refs.get(ORDERS[0]))
+        refs[order].set_kv(k, v, L)
+    inputs = [np.full(8, 1024, np.int32)] + list(synth.random_codes(frames - 1, seed=2, stream=9))
+    gpu_stats, ref_stats = [], {o: [] for o in ORDERS}
+    for f, cin in enumerate(inputs):
         pos, t = L + f, f
         g_codes, hs = dec.layer_states(cin)
         g_logits = dec.get_logits()
@@ -139,6 +151,26 @@ def test_full36_fp8_kv1024(ads, full_weights):
         print(f"fp8 36L kv1024 frame {f}: min layer cos {min(coss):.6f}, head {stat}")
         assert stat[2] >= 6
         orc.st.pos = pos + 1
+        # the whole frame against the oracle, beside the fp32 restatement variants
+        fo, fl, fg = orc_f.decode_step(cin)
+        gpu_stats.append(frame_stats(g_logits, fl, g_codes, fo, fg))
+        for order, r in refs.items():
+            c, lg = r.step(cin)
+            ref_stats[order].append(frame_stats(lg, fl, c, fo, fg))
+    show = lambda s: " ".join(f"{c:.5f}" for c, _, _ in s) + f"; codes differing {sum(b for _, _, b in s)}" \
+        f" of {sum(n for _, n, _ in s)}"
+    print("fp8 36L frames, GPU:", show(gpu_stats))
+    for order, s_ in ref_stats.items():
+        print(f"fp8 36L frames, fp32 restatement ({order}):", show(s_))
+    ref_min = min(c for s_ in ref_stats.values() for c, _, _ in s_)
+    ref_mean = min(np.mean([c for c, _, _ in s_]) for s_ in ref_stats.values())
+    ref_bad = max(sum(b for _, _, b in s_) for s_ in ref_stats.values())
+    g_cos = [c for c, _, _ in gpu_stats]
+    # no worse than the spread of fp32 implementations (a small allowance for
+    # four frames of a chaotic quantity)
+    assert min(g_cos) >= ref_min - 0.005, (g_cos, ref_min)
+    assert np.mean(g_cos) >= ref_mean - 0.003, (g_cos, ref_mean)
+    assert sum(b for _, _, b in gpu_stats) <= ref_bad + 1
     dec.close()
 
 

@@ -45,9 +45,10 @@ def fp8_weight(W64: torch.Tensor):
 class TorchRestatement:
     """The decode step as written from the model description, in torch float64."""
 
-    def __init__(self, w: synth.Weights, max_pos: int, fp8: bool = False):
+    def __init__(self, w: synth.Weights, max_pos: int, fp8: bool = False, a16: bool = False):
         self.d = w.dims
         self.fp8 = fp8
+        self.a16 = a16  # W16A16: every projection input rounded to bf16 (the batched prefill)
         d = self.d
         self.E = dec_bf16(w.embed)
         self.head = dec_bf16(w.head)
@@ -75,17 +76,20 @@ class TorchRestatement:
 
     def proj(self, layer, key, a):
         if not self.fp8:
-            return layer[key] @ a
+            return layer[key] @ (to_bf16_f64(a) if self.a16 else a)
         qa, sa = fp8_quant(a)
         qw, sw = layer[key + "_q"]
         acc = (qw @ qa).to(torch.float32)
         return to_bf16_f64(acc * (sa * sw))
 
-    def step(self, codes):
+    def layers(self, codes):
+        """The embedding and every layer at self.pos; returns the residual
+        stream after the embedding and after each layer."""
         d = self.d
         D, NQ, NKV, I = d.head_dim, d.n_q, d.n_kv, d.inter
         eps = d.rms_eps
         h = sum(self.E[k, int(codes[k])] for k in range(d.n_cb))
+        hs = [h]
         for l, P in enumerate(self.L):
             a = F.rms_norm(h, (d.hidden,), P["ln_in"], eps)
             qkv = self.proj(P, "qkv", a)
@@ -106,7 +110,13 @@ class TorchRestatement:
             if self.fp8:
                 m = to_bf16_f64(m)
             h = h + self.proj(P, "d", m)
-        f = F.rms_norm(h, (d.hidden,), self.fn, eps)
+            hs.append(h)
+        return hs
+
+    def step(self, codes):
+        d = self.d
+        h = self.layers(codes)[-1]
+        f = F.rms_norm(h, (d.hidden,), self.fn, d.rms_eps)
         logits = (self.head @ f).view(d.n_cb, d.cb_vocab)
         out = []
         for k in range(d.n_cb):
@@ -190,6 +200,39 @@ def test_prefill_equals_repeated_steps():
     c.prefill(codes[:3])
     c.prefill(codes[3:])
     assert np.array_equal(c.k, k_after_prefill) and np.array_equal(c.v, v_after_prefill)
+
+
+def test_prefill_a16_matches_torch_restatement():
+    """The W16A16 prefill (every projection input rounded to bf16 with torch's
+    own cast): the K/V rows it writes are bit-identical to the oracle's
+    or_prefill(a16), and the residual stream after every layer of every row
+    (the oracle's or_layer with a16, which also covers the last layer's O and
+    down inputs that no K/V row sees) agrees to fp64 rounding."""
+    w = _weights()
+    P = 6
+    codes = synth.delayed_prompt_codes(P)
+    orc = oracle.Oracle(w, MAXPOS)
+    orc.prefill(codes, a16=True)
+    ref = TorchRestatement(w, MAXPOS, a16=True)
+    per_row = []
+    for p in range(P):
+        per_row.append(ref.layers(codes[p]))
+        ref.pos += 1
+    to_bits = lambda x: x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.k[:, :, :P], to_bits(ref.K[:, :, :P]))
+    assert np.array_equal(orc.v[:, :, :P], to_bits(ref.V[:, :, :P]))
+    lay = oracle.Oracle(w, MAXPOS)
+    for p in range(P):
+        h = lay.embed(codes[p])
+        for l in range(TINY.n_layers):
+            h = lay.layer(l, p, h, a16=True)
+            assert np.allclose(h, per_row[p][l + 1].numpy(), rtol=1e-12, atol=1e-12), (p, l)
+    # the rounding matters: without it the restatement's rows differ
+    plain = TorchRestatement(w, MAXPOS, a16=False)
+    for p in range(P):
+        plain.layers(codes[p])
+        plain.pos += 1
+    assert not np.array_equal(orc.k[:, :, :P], to_bits(plain.K[:, :, :P]))
 
 
 def test_prefill_a16_rounds_projection_inputs():
