@@ -8,8 +8,9 @@ the prefix, and as a fresh context that prefills the prefix and the suffix."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
-from helpers import reduced_dims, to_binding_dims
+from helpers import adopt_gpu_cache, check_frame, check_kv_rows, reduced_dims, to_binding_dims
 
 pytestmark = pytest.mark.gpu
 
@@ -134,4 +135,45 @@ def test_repeated_prefill_replays_identically(ads, model, precision):
     for k, v, codes, st in runs[1:]:
         assert np.array_equal(k, runs[0][0]) and np.array_equal(v, runs[0][1])
         assert np.array_equal(codes, runs[0][2]) and st == runs[0][3]
+    dec.close()
+
+
+@pytest.mark.parametrize("precision", [0, 1])
+def test_request_after_restore_matches_the_oracle(ads, model, precision):
+    """A request served after a restore (the prefix rows overwritten in
+    between) against the CPU oracle: the prefix + suffix K/V rows meet the
+    prefill bar against the oracle's prefill of the whole prompt, and the
+    request's decode frames, teacher-forced from the same cache, meet the
+    frame bar."""
+    d, w = model
+    dw = ads.DeviceWeights(w, precision=precision)
+    system = synth.delayed_prompt_codes(13)
+    suf = synth.random_codes(7, seed=2, stream=35)
+    dec = ads.Decoder(to_binding_dims(d), dw, 64)
+    dec.prefill(system)
+    dec.prefix_save()
+    dec.prefill(synth.random_codes(6, seed=2, stream=36))  # another request
+    dec.rewind(0)
+    dec.prefill(synth.random_codes(9, seed=2, stream=37))  # overwrites the prefix rows
+    dec.prefix_restore()
+    dec.prefill(suf)
+    orc = oracle.Oracle(w, 64, precision=precision)
+    orc.prefill(np.concatenate([system, suf]), a16=True)
+    gk, gv = dec.get_kv(0, 20)
+    if precision == 0:
+        check_kv_rows(gk, orc.k[:, :, :20], "K after restore")
+        check_kv_rows(gv, orc.v[:, :, :20], "V after restore")
+    else:
+        from helpers import bf16_f64, cosine
+        for l in range(d.n_layers):
+            assert cosine(bf16_f64(gk[l]), bf16_f64(orc.k[l, :, :20])) >= 0.999
+            assert cosine(bf16_f64(gv[l]), bf16_f64(orc.v[l, :, :20])) >= 0.999
+    adopt_gpu_cache(dec, orc, 20)
+    cin = np.full(d.n_cb, d.cb_vocab - 2, np.int32)
+    for f in range(4):
+        t, e = orc.st.t, orc.st.eoc
+        g = dec.decode_step(cin)
+        o, ol, og = orc.decode_step(cin)
+        check_frame(g, dec.get_logits(), o, ol, og, precision == 1, t, e, f"request frame {f}")
+        cin = g
     dec.close()
