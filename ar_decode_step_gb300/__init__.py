@@ -62,6 +62,7 @@ SIGNATURES = {
     "tts_decode_step": (_I, [_VP, _VP, _VP]),
     "tts_decode_steps": (_I, [_VP, _I, _VP]),
     "tts_rewind": (_I, [_VP, _I, _I]),
+    "tts_set_input": (_I, [_VP, _VP]),
     "tts_set_sampling": (_I, [_VP, ctypes.c_float, ctypes.c_ulonglong]),
     "tts_decode_until_eoc": (_I, [_VP, _I, _VP, _VP]),
     "tts_prefix_save": (_I, [_VP]),
@@ -342,6 +343,11 @@ class Decoder:
     def prefix_restore(self):
         """tts_prefix_restore: back to the saved prefix (cache rows and state)."""
         _call("tts_prefix_restore", self._ctx)
+
+    def set_input(self, codes):
+        """tts_set_input: the next step's input frame (host codes [n_cb])."""
+        c = np.ascontiguousarray(codes, np.int32)
+        _call("tts_set_input", self._ctx, _ptr(c))
 
     def rewind(self, pos: int, t: int = 0):
         _call("tts_rewind", self._ctx, pos, t)

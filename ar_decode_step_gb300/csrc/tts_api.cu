@@ -820,6 +820,19 @@ int tts_decode_until_eoc(tts_ctx* ctx, int max_frames, int32_t* codes_out, int* 
     return rc != TTS_OK ? rc : prc;
 }
 
+int tts_set_input(tts_ctx* ctx, const int32_t* codes) {
+    if (!ctx) return TTS_ERR_STATE;
+    if (!codes) return TTS_ERR_ARG;
+    const tts_config& k = ctx->cfg;
+    for (int i = 0; i < k.n_codebooks; ++i)
+        if (codes[i] < 0 || codes[i] >= k.cb_vocab) return TTS_ERR_CODE;
+    std::memcpy(ctx->h_in->codes, codes, sizeof(int32_t) * k.n_codebooks);
+    TTS_CK(cudaMemcpyAsync(ctx->st->codes, ctx->h_in->codes, sizeof(int32_t) * k.n_codebooks,
+                           cudaMemcpyHostToDevice, ctx->stream));
+    TTS_CK(cudaStreamSynchronize(ctx->stream));
+    return TTS_OK;
+}
+
 int tts_rewind(tts_ctx* ctx, int pos, int t) {
     if (!ctx) return TTS_ERR_STATE;
     if (pos < 0 || pos > ctx->pos || t < 0) return TTS_ERR_ARG;

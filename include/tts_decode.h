@@ -176,6 +176,13 @@ int tts_decode_until_eoc(tts_ctx* ctx, int max_frames, int32_t* codes_out, int* 
  * input is processed).  The next decode step's input is the all-BOS frame. */
 int tts_rewind(tts_ctx* ctx, int pos, int t);
 
+/* Set the input frame of the next decode step (the codes the embedding
+ * reads) without running a step: teacher forcing for tts_decode_steps and
+ * tts_decode_until_eoc.  codes: HOST int32 [n_codebooks], each in
+ * [0, cb_vocab) (TTS_ERR_CODE otherwise, nothing changed).  Synchronises
+ * the stream. */
+int tts_set_input(tts_ctx* ctx, const int32_t* codes);
+
 /* FP8 static activation scales (FlashRT page, FP8 W8A8 and section 5: the
  * production FP8 path quantises each projection input with a per-tensor
  * scale calibrated offline as amax / 448, instead of the per-token amax).
