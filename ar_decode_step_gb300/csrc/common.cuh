@@ -53,6 +53,11 @@ __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
     return r;
 }
 
+// Prefetch the line holding p into L1 (no register waits for it).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Asynchronous bulk prefetch of [p, p+bytes) into L2 (bytes multiple of 16,
 // p 16-byte aligned).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
 
     constexpr bool FP8 = PREC == kFP8;
     const int cpr = p.K / (FP8 ? 16 : 8);
-    const int xbytes = p.K * (FP8 ? 2 : 4);
+    const int xbytes = p.K * (FP8 ? 1 : 4);
     Proj j{static_cast<const unsigned char*>(p.W), p.wscale, p.y, p.N, p.K, p.rs, p.wpr, FP8 ? 1 : 0,
            EPI == kEpiSwiglu ? 1 : 0, 0, 0};
     proj_split_rows(j);
@@ -147,7 +147,7 @@ GemvGeom gemv_geom(int prec, int epi, int N, int K, int grid) {
     const long long rows_max = grid > 0 ? (N + grid - 1) / grid : N;
     const long long nst_max = (rows_max + opst - 1) / opst;
     g.part_bytes = round128((int)(nst_max * g.rs * g.wpr * (long long)sizeof(float)));
-    const int xbytes = K * (prec == kBF16 ? 4 : 2);
+    const int xbytes = K * (prec == kBF16 ? 4 : 1);
     const long long stage = g.rs * rowb;
     long long ns = stage > 0 ? (kSmemBudget - kBarrierBytes - xbytes - g.part_bytes) / stage : 0;
     if (ns > kMaxStages) ns = kMaxStages;

@@ -9,15 +9,25 @@
 // counted on the slot's "full" mbarrier, consumers free the slot on its
 // "empty" mbarrier.
 //
-// Consumers: warp w owns column segment w % WPR of row slot w / WPR (WPR
-// segments per row, stage_geom); a stage's rows are taken one row slot per
-// pass: equal bytes per warp, direct activation indexing, one shuffle
-// reduction per row.  Per-(row, segment) partials are summed in segment order
+// Consumers, bf16 weights: warp w owns column segment w % WPR of row slot
+// w / WPR (WPR segments per row, stage_geom); a stage's rows are taken one row
+// slot per pass: equal bytes per warp, direct activation indexing, one shuffle
+// reduction per row, packed fp32 FMAs against fp32 activations.
+// Consumers, E4M3 weights: the stage loop runs on the tensor cores (E4M3 x
+// E4M3 mma.sync m16n8k32, fp32 accumulation), the stage's rows as A and the
+// quantised activation as B.  A stage of R rows is cut into P = 16 / R
+// K-subranges per row, and each subrange into one piece per warp, so a warp's
+// 16 MMA rows are all (row, subrange) pairs of the stage.  Each lane feeds
+// its own 16-byte chunks of its two MMA rows and the matching activation
+// chunk, so the products of MMA row m meet only in output column m mod 8: the
+// partial sums are the MMA's diagonal.  Lanes of odd and even MMA rows take
+// the two halves of each 128-byte group in opposite order, which keeps the
+// 16-byte shared-memory loads free of bank conflicts.
+// Either way, per-(row, segment) partials are summed in segment order
 // (deterministic) before the epilogue.
 //
 // Activations: staged in shared memory once per projection, fp32 planes for
-// bf16 weights, f16 planes (exact E4M3 values) for FP8 weights, which are
-// multiplied with the mixed-precision f16 x f16 + f32 FMA.
+// bf16 weights, E4M3 bytes (per-token scale) for FP8 weights.
 #pragma once
 
 #include <type_traits>
@@ -55,33 +65,20 @@ __device__ __forceinline__ void dot_bf16(const uint4 w, const float4 a, const fl
     ffma2(e, o, bf16lo(w.w), bf16hi(w.w), b.z, b.w);
 }
 
-// Two E4M3 weights (low 16 bits of w16) times two activations (exact E4M3
-// values held in fp32), f32 accumulate: the weights go through f16 and the
-// products are taken by the mixed-precision f16 x f16 + f32 FMA (the
-// activations are exact in f16).
-__device__ __forceinline__ float fma2_e4m3_f16(uint32_t w16, uint32_t x2, float acc) {
-    const __half2_raw wh = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w16 & 0xffffu), __NV_E4M3);
-    const uint32_t w2 = (uint32_t)wh.x | ((uint32_t)wh.y << 16);
-    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
-        "mov.b32 {a0, a1}, %1;\n\t"
-        "mov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
-        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(w2), "r"(x2));
-    return acc;
+// D += A . B for one m16n8k32 tile: A 16 x 32 E4M3 (row-major fragments
+// a0..a3), B 32 x 8 E4M3 (column fragments b0, b1), D 16 x 8 fp32.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// FP8: 16 weights x f16 activations held as two planes of 8 f16; two chains.
-__device__ __forceinline__ void dot_fp8(const uint4 w, const uint4 a, const uint4 b, float& e, float& o) {
-    e = fma2_e4m3_f16(w.x, a.x, e);
-    o = fma2_e4m3_f16(w.x >> 16, a.y, o);
-    e = fma2_e4m3_f16(w.y, a.z, e);
-    o = fma2_e4m3_f16(w.y >> 16, a.w, o);
-    e = fma2_e4m3_f16(w.z, b.x, e);
-    o = fma2_e4m3_f16(w.z >> 16, b.y, o);
-    e = fma2_e4m3_f16(w.w, b.z, e);
-    o = fma2_e4m3_f16(w.w >> 16, b.w, o);
+// fp32 -> E4M3 byte (round to nearest even, saturating to +-448).
+__device__ __forceinline__ uint32_t e4m3_byte(float x) {
+    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
@@ -251,7 +248,8 @@ __device__ __forceinline__ void drain(const Ring& ring, int it) {
 //   x (fp32, global, written by other CTAs: read through L2) -> optional
 //   RMSNorm with gain gamma -> shared memory, fp32 planes (bf16 weights) or,
 //   with FP8 weights, per-token E4M3 quantisation with scale amax/448 stored
-//   as f16 planes.  Returns the activation scale (1 for bf16).  Consumers only.
+//   as E4M3 bytes in order.  Returns the activation scale (1 for bf16).
+//   Consumers only.
 template <bool FP8, bool RMS>
 __device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* gamma, int K, float eps,
                                          unsigned char* xs, float* red) {
@@ -294,16 +292,11 @@ __device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* ga
         }
         amax = consumer_max(amax, red);
         sa = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
-        uint2* xs2 = reinterpret_cast<uint2*>(xs);  // 4 f16 per uint2
+        uint32_t* xs4 = reinterpret_cast<uint32_t*>(xs);  // E4M3 bytes, in order
         for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
             const float4 v = load(i);
-            const __half2 h01 = __floats2half2_rn(quant_e4m3(__fdiv_rn(v.x, sa)), quant_e4m3(__fdiv_rn(v.y, sa)));
-            const __half2 h23 = __floats2half2_rn(quant_e4m3(__fdiv_rn(v.z, sa)), quant_e4m3(__fdiv_rn(v.w, sa)));
-            const int e = 4 * i;  // chunk e/16, plane (e%16)/8, half (e%8)/4
-            uint2 packed;
-            packed.x = *reinterpret_cast<const uint32_t*>(&h01);
-            packed.y = *reinterpret_cast<const uint32_t*>(&h23);
-            xs2[(((e & 15) >> 3) * cpr + (e >> 4)) * 2 + ((e & 7) >> 2)] = packed;
+            xs4[i] = e4m3_byte(__fdiv_rn(v.x, sa)) | (e4m3_byte(__fdiv_rn(v.y, sa)) << 8) |
+                     (e4m3_byte(__fdiv_rn(v.z, sa)) << 16) | (e4m3_byte(__fdiv_rn(v.w, sa)) << 24);
         }
     }
     consumer_sync();
@@ -312,18 +305,18 @@ __device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* ga
 
 // ---- activation segments in registers -----------------------------------------
 // A consumer warp's column segment [c0, c1) of a projection is the same in
-// every stage, so each lane keeps the activations of its chunks c0 + lane +
-// 32 i (at most kMaxLaneChunks) in registers: two planes per chunk, fp32
-// (bf16 weights) or f16 (FP8 weights).
+// every stage, so with bf16 weights each lane keeps the activations of its
+// chunks c0 + lane + 32 i (at most kMaxLaneChunks) in registers, two fp32
+// planes per chunk.  E4M3 weights (tensor cores) read their activation chunks
+// from the staged bytes in shared memory instead.
 template <bool FP8>
 struct XSeg {
-    static constexpr int kChunks = lane_chunk_limit(0);
+    static constexpr int kChunks = kMaxLaneChunks;
     float4 a[kChunks], b[kChunks];  // elements 0-3 and 4-7 of each 8-weight chunk
 };
 template <>
 struct XSeg<true> {
-    static constexpr int kChunks = lane_chunk_limit(1);
-    uint4 a[kChunks], b[kChunks];   // f16 activations (exact E4M3 values) 0-7 and 8-15 of each chunk
+    const unsigned char* xs;  // E4M3 activation bytes in shared memory (read per MMA pair)
 };
 
 // This warp's segment of projection j.
@@ -335,21 +328,20 @@ __device__ __forceinline__ void proj_segment(const Proj& j, int warp, int& rslot
     c1 = (int)((long long)(sg + 1) * CPR / WPR);
 }
 
-// Segment from the shared-memory planes written by stage_x: fp32 planes for
-// bf16 weights, f16 planes (exact E4M3 values) for FP8.
+// Segment from the shared memory written by stage_x: fp32 planes for bf16
+// weights, E4M3 bytes for FP8 (in the order the lane's MMAs consume them).
 template <bool FP8>
 __device__ __forceinline__ void load_xseg_smem(const unsigned char* xs, int CPR, int c0, int c1, XSeg<FP8>& x) {
     const int lane = threadIdx.x & 31;
+    if constexpr (!FP8) {
 #pragma unroll
-    for (int i = 0; i < XSeg<FP8>::kChunks; ++i) {
-        const int c = c0 + lane + 32 * i;
-        if constexpr (!FP8) {
+        for (int i = 0; i < XSeg<FP8>::kChunks; ++i) {
+            const int c = c0 + lane + 32 * i;
             x.a[i] = c < c1 ? reinterpret_cast<const float4*>(xs)[c] : float4{};
             x.b[i] = c < c1 ? reinterpret_cast<const float4*>(xs)[CPR + c] : float4{};
-        } else {
-            x.a[i] = c < c1 ? reinterpret_cast<const uint4*>(xs)[c] : uint4{};
-            x.b[i] = c < c1 ? reinterpret_cast<const uint4*>(xs)[CPR + c] : uint4{};
         }
+    } else {
+        x.xs = xs;
     }
 }
 
@@ -381,10 +373,10 @@ struct XStats {
 };
 
 // Stage an activation vector whose statistics the producing phase published,
-// into the shared planes of stage_x, with no block-wide reduction.
+// into the shared layout of stage_x, with no block-wide reduction.
 //   RMS:   x = h * r * gamma, r = 1/sqrt(sum(h^2)/K + eps)   (K <= kMaxRmsK)
 //   FP8:   sa = max(amax, 1e-12)/448, amax = r * max|h*gamma| (RMS) or max|x|;
-//          x8 = e4m3(x/sa) stored as f16
+//          x8 = e4m3(x/sa) stored as bytes
 //   plain bf16: a permuted copy, issued as asynchronous 16-byte copies.
 // x is read through L2 (other CTAs wrote it).  The first batch of x is loaded
 // together with the statistics (one memory round trip); every warp reduces the
@@ -419,6 +411,8 @@ __device__ __forceinline__ float stage_x_stats(const float* x, const __nv_bfloat
             }
         }
     };
+    // FP8: the site's static activation scale is pulled into L1 while x loads
+    if (FP8 && st.sa_static) prefetch_l1(st.sa_static);
     load(0);
     float r = 1.0f, sa = 1.0f;
     {
@@ -448,7 +442,7 @@ __device__ __forceinline__ float stage_x_stats(const float* x, const __nv_bfloat
             // non-negative floats order like their bit patterns
             if (st.calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(st.calib), __float_as_int(am));
             if (st.sa_static) {
-                const float ss_ = __ldcg(st.sa_static);
+                const float ss_ = *st.sa_static;
                 if (ss_ > 0.f) sa = ss_;  // static: values beyond 448 * sa saturate
             }
         }
@@ -470,14 +464,9 @@ __device__ __forceinline__ float stage_x_stats(const float* x, const __nv_bfloat
                 if constexpr (!FP8) {
                     reinterpret_cast<float4*>(xs)[((e & 7) >> 2) * cpr + (e >> 3)] = u;
                 } else {
-                    const __half2 h01 =
-                        __floats2half2_rn(quant_e4m3(__fdiv_rn(u.x, sa)), quant_e4m3(__fdiv_rn(u.y, sa)));
-                    const __half2 h23 =
-                        __floats2half2_rn(quant_e4m3(__fdiv_rn(u.z, sa)), quant_e4m3(__fdiv_rn(u.w, sa)));
-                    uint2 packed;
-                    packed.x = *reinterpret_cast<const uint32_t*>(&h01);
-                    packed.y = *reinterpret_cast<const uint32_t*>(&h23);
-                    reinterpret_cast<uint2*>(xs)[(((e & 15) >> 3) * cpr + (e >> 4)) * 2 + ((e & 7) >> 2)] = packed;
+                    reinterpret_cast<uint32_t*>(xs)[i] =
+                        e4m3_byte(__fdiv_rn(u.x, sa)) | (e4m3_byte(__fdiv_rn(u.y, sa)) << 8) |
+                        (e4m3_byte(__fdiv_rn(u.z, sa)) << 16) | (e4m3_byte(__fdiv_rn(u.w, sa)) << 24);
                 }
             }
         }
@@ -494,6 +483,96 @@ struct StatsOut {
     float* rows;                   // kEpiResid: shared-memory copy of this CTA's rows of y (read and
                                    //   updated instead of global memory), or null
 };
+
+// The tensor-core FP8 stage loop's per-lane constants for one projection (the
+// same in every stage: worked out once, outside the stage loop).  A stage
+// holds `rs` rows (a power of two, 2..16; SwiGLU: rs / 2 gate rows, then their
+// rs / 2 up rows) of cpr 16-byte chunks; P = 16 / rs subranges of cpr / P
+// chunks per row.  Lane (g, q) of warp w works on subrange kap = g / (8 / P)
+// and on rows ra = g mod (8 / P) and rb = ra + rs / 2, which it feeds as MMA
+// rows g and g + 8; subrange kap's piece of warp w is its units
+// [w u / 8, (w + 1) u / 8) of u = cpr / (4 P) units of 4 chunks.
+struct Fp8Lane {
+    int a_off, b_off;   // byte offset, within a stage, of this lane's first chunk of rows ra and rb
+    int x_off;          // byte offset of its first activation chunk
+    int a_out, b_out;   // output rows of ra and rb within a stage (an up row maps to its gate row)
+    int a_part, b_part; // their partial-sum slots: r * wpr + w P + kap
+    int nu;             // 4-chunk units of this warp's piece
+    int odd;            // g & 1
+};
+__device__ __forceinline__ Fp8Lane fp8_lane(int cpr, size_t rowb, int rs, int opst, int wpr) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int P = kFp8MmaRows / rs, gpr = 8 / P;  // subranges per row, lane groups per subrange
+    const int kap = g / gpr, ra = g % gpr, rb = ra + rs / 2;
+    const int ls = cpr / P, units = ls / 4;       // chunks and 4-chunk units per subrange
+    const int u0 = warp * units / kConsumerWarps;
+    const int c0 = kap * ls + 4 * u0 + q;         // this lane's first chunk
+    Fp8Lane L;
+    L.a_off = (int)(ra * rowb) + 16 * c0;
+    L.b_off = (int)(rb * rowb) + 16 * c0;
+    L.x_off = 16 * c0;
+    L.a_out = ra < opst ? ra : ra - opst;
+    L.b_out = rb < opst ? rb : rb - opst;
+    L.a_part = ra * wpr + warp * P + kap;
+    L.b_part = rb * wpr + warp * P + kap;
+    L.nu = (warp + 1) * units / kConsumerWarps - u0;
+    L.odd = g & 1;
+    return L;
+}
+
+// One ring stage of E4M3 rows on the tensor cores (lane constants from
+// fp8_lane).  Per 128-byte group (8 chunks) of a lane's piece, lanes of even g
+// take chunks q and 4 + q in that order, lanes of odd g the other way round
+// (conflict-free 16-byte loads); a trailing unit of 4 chunks takes chunk q.
+// Each lane's activation chunk is the one matching its row chunk, so
+// D[m][m mod 8] is MMA row m's partial sum.  The four MMAs of a group go to
+// four accumulators, added in a fixed order.  A row is fed as zeros unless its
+// output row is below `nv`.  Writes the partial sums of the valid rows into
+// part (this stage's slots).
+__device__ __forceinline__ void fp8_stage(const unsigned char* sbuf, const Fp8Lane& L, int nv,
+                                          const unsigned char* xs, float* part) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const bool va = L.a_out < nv, vb = L.b_out < nv;
+    const unsigned char* pa = sbuf + L.a_off;
+    const unsigned char* pb = sbuf + L.b_off;
+    const unsigned char* px = xs + L.x_off;
+    const int off0 = 64 * L.odd, off1 = 64 * (L.odd ^ 1);  // the two halves of a group, odd rows swapped
+    const int groups = L.nu >> 1;
+    float d[4][4] = {};
+#pragma unroll 2
+    for (int t = 0; t < groups; ++t) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int off = 128 * t + (h ? off1 : off0);
+            const uint4 wa = va ? *reinterpret_cast<const uint4*>(pa + off) : uint4{};
+            const uint4 wb = vb ? *reinterpret_cast<const uint4*>(pb + off) : uint4{};
+            const uint4 x = *reinterpret_cast<const uint4*>(px + off);
+            mma_e4m3(d[2 * h], wa.x, wb.x, wa.y, wb.y, x.x, x.y);
+            mma_e4m3(d[2 * h + 1], wa.z, wb.z, wa.w, wb.w, x.z, x.w);
+        }
+    }
+    if (L.nu & 1) {  // trailing unit: chunk q of every lane's 4
+        const int off = 128 * groups;
+        const uint4 wa = va ? *reinterpret_cast<const uint4*>(pa + off) : uint4{};
+        const uint4 wb = vb ? *reinterpret_cast<const uint4*>(pb + off) : uint4{};
+        const uint4 x = *reinterpret_cast<const uint4*>(px + off);
+        mma_e4m3(d[0], wa.x, wb.x, wa.y, wb.y, x.x, x.y);
+        mma_e4m3(d[1], wa.z, wb.z, wa.w, wb.w, x.z, x.w);
+    }
+    // D[g][g] sits in lane (g, g / 2) as element g & 1, D[g + 8][g] as element
+    // 2 + (g & 1) (selects, not an index: a lane-dependent index would put d
+    // in local memory)
+    if (q == (g >> 1)) {
+        float sa_[4], sb_[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            sa_[k] = L.odd ? d[k][1] : d[k][0];
+            sb_[k] = L.odd ? d[k][3] : d[k][2];
+        }
+        if (va) part[L.a_part] = (sa_[0] + sa_[1]) + (sa_[2] + sa_[3]);
+        if (vb) part[L.b_part] = (sb_[0] + sb_[1]) + (sb_[2] + sb_[3]);
+    }
+}
 
 // Consumers: reduce projection j's stages from the ring against the lane's
 // activation registers, then apply the epilogue to this CTA's outputs (and
@@ -515,14 +594,30 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
     const int nst = (nrows + opst - 1) / opst;
     int rslot, sg, c0, c1;
     proj_segment(j, warp, rslot, sg, c0, c1);
+    Fp8Lane fl{};
+    if constexpr (FP8) fl = fp8_lane(CPR, rowb, RS, opst, WPR);
+    // the epilogue's operands in global memory (per-row weight scales, the
+    // next RMSNorm's gain) are pulled into L1 now, so that the epilogue's loads
+    // hit L1 instead of waiting for L2 behind the weight stream; a prefetch
+    // holds no register, so nothing waits for it
+    if (threadIdx.x < nrows) {
+        const int n = r0 + threadIdx.x;
+        if constexpr (FP8) {
+            prefetch_l1(j.wscale + n);
+            if (EPI == kEpiSwiglu) prefetch_l1(j.wscale + j.N + n);
+        }
+        if (EPI == kEpiResid && so && so->h && so->gamma) prefetch_l1(so->gamma + n);
+    }
 
     bool ok = true;
     unsigned long long waited = 0;  // ns spent waiting for data (traced runs; stored once at the end)
+    int slot = it % ring.ns;        // ring slot and phase of stage `it`, advanced per stage
+    uint32_t phase = (it / ring.ns) & 1;
     for (int s = 0; s < nst; ++s, ++it) {
-        const int slot = it % ring.ns;
-        const uint64_t tw = wait_ns ? globaltimer_ns() : 0;
-        const bool got = mbar_wait_or_abort(&ring.full[slot], (it / ring.ns) & 1, abort);
-        if (wait_ns) waited += globaltimer_ns() - tw;
+        const bool timed = wait_ns && threadIdx.x == 0;  // traced runs: thread 0 times its data waits
+        const uint64_t tw = timed ? globaltimer_ns() : 0;
+        const bool got = mbar_wait_or_abort(&ring.full[slot], phase, abort);
+        if (timed) waited += globaltimer_ns() - tw;
         if (!got) {
             if (lane == 0 && err) atomicOr(err, kErrTimeout);
             *abort = 1;
@@ -535,23 +630,23 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
             str = stage_tr + (warp == 0 ? 0 : stage_tr_n * 4) + 4 * it;
         if (str) str[1] = globaltimer_ns();
         const unsigned char* sbuf = ring.buf + (size_t)slot * ring.slot_bytes;
-        for (int ps = 0; ps < NP; ++ps) {
-            const int r = ps * SLOTS + rslot;          // row of the stage
-            const int orow = j.swiglu ? r % opst : r;  // its output row within the stage
-            if (s * opst + orow < nrows) {
-                const uint4* wrow = reinterpret_cast<const uint4*>(sbuf + r * rowb);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (FP8) {
+            fp8_stage(sbuf, fl, nrows - s * opst, xr.xs, part + (size_t)s * RS * WPR);
+        } else {
+            for (int ps = 0; ps < NP; ++ps) {
+                const int r = ps * SLOTS + rslot;          // row of the stage
+                const int orow = j.swiglu ? r % opst : r;  // its output row within the stage
+                if (s * opst + orow < nrows) {
+                    const uint4* wrow = reinterpret_cast<const uint4*>(sbuf + r * rowb);
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < XSeg<FP8>::kChunks; ++i) {
-                    const int c = c0 + lane + 32 * i;
-                    if (c < c1) {
-                        const uint4 w = wrow[c];
-                        if constexpr (!FP8) dot_bf16(w, xr.a[i], xr.b[i], acc[2 * (i & 1)], acc[2 * (i & 1) + 1]);
-                        else dot_fp8(w, xr.a[i], xr.b[i], acc[2 * (i & 1)], acc[2 * (i & 1) + 1]);
+                    for (int i = 0; i < XSeg<FP8>::kChunks; ++i) {
+                        const int c = c0 + lane + 32 * i;
+                        if (c < c1) dot_bf16(wrow[c], xr.a[i], xr.b[i], acc[2 * (i & 1)], acc[2 * (i & 1) + 1]);
                     }
+                    const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+                    if (lane == 0) part[(s * RS + r) * WPR + sg] = v;
                 }
-                const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-                if (lane == 0) part[(s * RS + r) * WPR + sg] = v;
             }
         }
         __syncwarp();
@@ -560,8 +655,12 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
             str[2] = globaltimer_ns();
             str[3] = (unsigned long long)(clock64() - clk0);  // SM cycles of this stage
         }
+        if (++slot == ring.ns) {
+            slot = 0;
+            phase ^= 1;
+        }
     }
-    if (wait_ns) *wait_ns += waited;
+    if (wait_ns && threadIdx.x == 0) *wait_ns += waited;
     consumer_sync();
     if (!ok || *abort) return false;
 

@@ -23,10 +23,12 @@ enum Epi { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiLogits = 3 };
 #endif
 constexpr int kConsumerWarps = TTS_CONSUMER_WARPS;
 constexpr int kMaxLaneChunks = TTS_MAX_LANE_CHUNKS;
-// FP8 chunks carry 16 weights (twice the FMAs per chunk): half as many per
-// lane keep the FP8 stage loop's registers (activations as f16 pairs plus the
-// conversion temporaries) within the budget.
-constexpr int lane_chunk_limit(int prec) { return prec == 1 ? kMaxLaneChunks / 2 : kMaxLaneChunks; }
+// FP8 projections run their stage loop on the tensor cores (E4M3 mma.sync,
+// fp32 accumulation).  A stage holds R rows (R = 16, 8, 4 or 2, R x K bytes
+// at most kStageTarget); each row is cut into P = 16 / R K-subranges and each
+// subrange into kConsumerWarps pieces of whole 64-byte units, so that the 16
+// MMA rows of a warp's tile are all (row, subrange) pairs of the stage.
+constexpr int kFp8MmaRows = 16;
 constexpr int kStageTarget = 40 * 1024;  // bytes per ring stage, at most (unless one row is longer)
 constexpr int kMaxRmsK = 4096;            // persistent step: longest normalised activation (hidden)
 constexpr int kMaxPlainK = 12288;         // longest plain activation (attention output, MLP activation)
@@ -42,11 +44,21 @@ struct StageGeom {
     bool ok;  // segments fit the lane registers and every warp has a chunk
 };
 inline __host__ __device__ StageGeom stage_geom(int prec, int epi, int K) {
-    const int cpr = K / (prec == kBF16 ? 8 : 16);
+    if (prec != kBF16) {
+        // tensor-core FP8: R rows per stage (a power of two, 2..16, R x K <=
+        // kStageTarget), P = 16 / R subranges per row; a row's partial sums
+        // are kept per (warp, subrange): wpr = kConsumerWarps x P.  SwiGLU
+        // stages hold R / 2 gate and R / 2 up rows.
+        int rs = kFp8MmaRows;
+        while (rs > 2 && (long long)rs * K > kStageTarget) rs >>= 1;
+        const int P = kFp8MmaRows / rs;
+        return StageGeom{rs, kConsumerWarps * P, K % 512 == 0 && (long long)rs * K <= kStageTarget};
+    }
+    const int cpr = K / 8;
     const long long rowb = (long long)cpr * 16;
     auto lane_chunks = [&](int w) { return ((cpr + w - 1) / w + 31) / 32; };
     int wpr = 1;
-    const int limit = lane_chunk_limit(prec);
+    const int limit = kMaxLaneChunks;
     while (wpr < kConsumerWarps && lane_chunks(wpr) > limit) wpr *= 2;
     while (wpr < kConsumerWarps && (long long)(kConsumerWarps / wpr) * rowb > kStageTarget) wpr *= 2;
     const int slots = kConsumerWarps / wpr;

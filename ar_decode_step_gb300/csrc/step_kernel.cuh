@@ -387,13 +387,17 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
 
     // the stage loop and epilogue in a function of their own (consume_call):
     // allocated apart from the staging code above, it keeps the activation
-    // segment and the loop state in registers
+    // segment and the loop state in registers.  Traced launches also record
+    // the consumers' data waits and CTA 0's per-stage times.
+    unsigned long long* cw = TRACE && cs.cwait && KIND < 4 ? cs.cwait + 4 * l + KIND : nullptr;
+    unsigned long long* str = TRACE ? cs.cstr : nullptr;
+    const int str_n = TRACE ? cs.cstr_n : 0;
     if constexpr (KIND == 1 || KIND == 3) {
         // residual add; publish h's statistics for the next RMSNorm (FP8: max |h * gamma_next|)
         const __nv_bfloat16* gnext = KIND == 1 ? m.sl[l].ln_post : (l + 1 < p.n_layers ? m.sl[l + 1].ln_in : p.final_norm);
         const StatsOut so{p.h_stats, FP8 ? gnext : nullptr, nullptr, s_hrows};
-        it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, &so, red,
-                                          nullptr, 0, FP8 ? nullptr : (KIND == 1 ? p.attn : p.act));
+        it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, red,
+                                          str, str_n, FP8 ? nullptr : (KIND == 1 ? p.attn : p.act));
         if constexpr (TRACE && KIND == 3) {
             // layer-level checks: this CTA's rows of the residual stream after the layer
             if (p.hsnap && it >= 0)
@@ -402,11 +406,11 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
         }
     } else if constexpr (KIND == 2) {
         const StatsOut so{nullptr, nullptr, FP8 ? p.act_mx : nullptr, nullptr};
-        it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, &so, red,
-                                           nullptr, 0);
+        it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, red,
+                                           str, str_n);
     } else {
-        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, nullptr, nullptr,
-                                          nullptr, nullptr, 0);
+        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, nullptr,
+                                          nullptr, str, str_n);
     }
     const bool ok = it >= 0;
     if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 1);

@@ -131,6 +131,11 @@ int validate(const tts_config* c, const tts_weights* w) {
         return TTS_ERR_ARG;
     const bool fp8 = c->precision == TTS_FP8;
     if (fp8 && (!w->sqkv || !w->so || !w->sgu || !w->sd)) return TTS_ERR_ARG;
+    // FP8 projections reduce whole 64-byte units of each row on the tensor
+    // cores, in stages of at least 2 rows: K a multiple of 512, at most 20480
+    if (fp8)
+        for (const long long K : {(long long)c->hidden, (long long)c->inter, (long long)c->n_q_heads * kHeadDim})
+            if (!stage_geom(kFP8, kEpiStore, (int)K).ok) return TTS_ERR_ARG;
     for (int l = 0; l < c->n_layers; ++l) {
         if (!aligned16(w->wqkv[l]) || !aligned16(w->wo[l]) || !aligned16(w->wgu[l]) || !aligned16(w->wd[l]))
             return TTS_ERR_ARG;

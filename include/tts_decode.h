@@ -68,7 +68,8 @@ typedef struct tts_ctx tts_ctx;
 
 /* Model and run configuration.  Supported shapes: head_dim 128; n_q_heads a
  * multiple of n_kv_heads with 1, 2, 4 or 8 query heads per key-value head;
- * hidden, inter and n_q_heads*128 multiples of 256 and at most 12288;
+ * hidden, inter and n_q_heads*128 multiples of 256 and at most 12288 (for
+ * TTS_FP8: multiples of 512);
  * n_codebooks 1..8; cb_vocab >= 2 (codes
  * cb_vocab-2 and cb_vocab-1 are BOS-pad and EOC, i.e. 1024 and 1025 for the
  * 1026-entry codebooks); 1 <= max_pos <= 65536. */
