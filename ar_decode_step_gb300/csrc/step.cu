@@ -14,8 +14,10 @@ cudaError_t step_prepare(int prec, int G, int smem) {
 }
 
 int step_attn_scratch_bytes(int G) {
+    // AttnSmem<G> (step_kernel.cuh): queries, the new key and value rows, per
+    // warp softmax state, partial outputs and the weights of 8 positions
     return (int)(sizeof(float) * (G * kHeadDim + 2 * kHeadDim + 2 * kConsumerWarps * G +
-                                  kConsumerWarps * G * kHeadDim));
+                                  kConsumerWarps * G * kHeadDim + kConsumerWarps * 8 * G));
 }
 
 int step_threads() { return (kConsumerWarps + 1) * 32; }

@@ -67,13 +67,36 @@ __device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned target, De
     return !*abort;
 }
 
+constexpr int kAttnStep = 8;  // positions a warp scores at once
+
 template <int G>
 struct AttnSmem {
     float qs[G][kHeadDim];  // normalised, rotated, pre-scaled queries
     float knew[kHeadDim], vnew[kHeadDim];
     float wm[kConsumerWarps][G], wl[kConsumerWarps][G];
     float wo[kConsumerWarps][G][kHeadDim];
+    float pw[kConsumerWarps][kAttnStep][G];  // a warp's softmax weights of its current positions
 };
+
+// Sum each of the kAttnStep entries of v over the 32 lanes of the warp (a
+// reduce-scatter: each halving step exchanges half of the entries with one
+// partner lane, then the lanes holding the same entry add up).  Lane l ends
+// with the total of entry l mod kAttnStep in v[0].
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[kAttnStep]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = kAttnStep / 2; o >= 1; o >>= 1) {
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float keep = up ? v[i + o] : v[i];
+            const float send = up ? v[i] : v[i + o];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+#pragma unroll
+    for (int o = kAttnStep; o < 32; o <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+}
 
 // One (kv head g, split) unit of the decode attention of one layer, run by the
 // consumer warps of this CTA (no waits inside).
@@ -108,22 +131,24 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
             dst[4 * lane + jj] = (lane < 16 ? a[jj] * cs.x - partner * cs.y : a[jj] * cs.x + partner * cs.y) * post;
         }
     };
-    // The cached rows do not depend on this step: issue their loads first so
-    // they overlap the q/k loads (one memory round trip for both).
+    // The cached rows do not depend on this step: issue the loads of the
+    // warp's first positions before the q/k loads (one memory round trip).
+    // Warp w scores positions in steps of kAttnStep: step i covers
+    // [t0 + kAttnStep (w + 8 i), +kAttnStep); lane l holds dims 4 (l mod 32)
+    // .. +3 of each key and value row (whole rows are one coalesced load per
+    // position).  The new position's row (t1 - 1 when has_new) comes from
+    // shared memory.
     const int tcache_end = has_new ? t1 - 1 : t1;  // cached rows; the new row comes from smem
-    constexpr int kBatch = 4;                       // rows per warp per round trip
-    uint2 ka[kBatch], va[kBatch];
-    auto load_rows = [&](int tb) {
+    uint2 ka[kAttnStep];
+    auto load_k = [&](int tb) {
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int t = tb + b * kConsumerWarps;
-            if (t < tcache_end) {
-                ka[b] = *reinterpret_cast<const uint2*>(kc + (size_t)t * kHeadDim + 4 * lane);
-                va[b] = *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane);
-            }
+        for (int b = 0; b < kAttnStep; ++b) {
+            const int t = tb + b;
+            ka[b] = t < tcache_end ? *reinterpret_cast<const uint2*>(kc + (size_t)t * kHeadDim + 4 * lane)
+                                   : make_uint2(0u, 0u);
         }
     };
-    load_rows(t0 + warp);
+    load_k(t0 + kAttnStep * warp);
     if (warp < G) norm_rope(p.qkv + (size_t)(g * G + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
     if (has_new && warp == G) {
         norm_rope(p.qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
@@ -146,43 +171,75 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
 #pragma unroll
     for (int jj = 0; jj < G; ++jj) {
         m[jj] = -INFINITY;
-        l[jj] = 0.f;
+        l[jj] = 0.f;  // this lane's share of the softmax denominator (summed over the warp at the end)
 #pragma unroll
         for (int i = 0; i < 4; ++i) { o[jj][i] = 0.f; qr[jj][i] = sm.qs[jj][4 * lane + i]; }
     }
-    auto consume_pos = [&](const float* k4, const float* v4) {
-        float s[G];
+    const int new_t = has_new ? t1 - 1 : -1;
+    float (*pw)[G] = sm.pw[warp];
+    for (int tb = t0 + kAttnStep * warp; tb < t1; tb += kAttnStep * kConsumerWarps) {
+        if (tb != t0 + kAttnStep * warp) load_k(tb);
+        // partial scores of the lane's 4 dims, reduced over the warp: lane l
+        // ends with the full score of position tb + l mod kAttnStep for every head
+        float sc[G][kAttnStep];
 #pragma unroll
-        for (int jj = 0; jj < G; ++jj)
-            s[jj] = warp_sum(qr[jj][0] * k4[0] + qr[jj][1] * k4[1] + qr[jj][2] * k4[2] + qr[jj][3] * k4[3]);
+        for (int b = 0; b < kAttnStep; ++b) {
+            float k4[4];
+            if (tb + b == new_t) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) k4[i] = sm.knew[4 * lane + i];
+            } else {
+                k4[0] = bf16lo(ka[b].x); k4[1] = bf16hi(ka[b].x); k4[2] = bf16lo(ka[b].y); k4[3] = bf16hi(ka[b].y);
+            }
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj)
+                sc[jj][b] = qr[jj][0] * k4[0] + qr[jj][1] * k4[1] + qr[jj][2] * k4[2] + qr[jj][3] * k4[3];
+        }
+        // the value rows of these positions, in flight during the reduction
+        uint2 va[kAttnStep];
+#pragma unroll
+        for (int b = 0; b < kAttnStep; ++b) {
+            const int t = tb + b;
+            va[b] = t < tcache_end ? *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane)
+                                   : make_uint2(0u, 0u);
+        }
+        const int tl = tb + (lane & (kAttnStep - 1));  // the position this lane's scores belong to
+        const bool live = tl < t1;
 #pragma unroll
         for (int jj = 0; jj < G; ++jj) {
-            const float mn = fmaxf(m[jj], s[jj]);
+            warp_reduce_scatter(sc[jj]);
+            const float sj = live ? sc[jj][0] : -INFINITY;
+            const float mn = fmaxf(m[jj], warp_max(sj));
             const float corr = __expf(m[jj] - mn);
-            const float pj = __expf(s[jj] - mn);
-            l[jj] = l[jj] * corr + pj;
+            const float pj = live ? __expf(sj - mn) : 0.f;
+            l[jj] = l[jj] * corr + (lane < kAttnStep ? pj : 0.f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[jj][i] = o[jj][i] * corr + pj * v4[i];
+            for (int i = 0; i < 4; ++i) o[jj][i] *= corr;
             m[jj] = mn;
+            if (lane < kAttnStep) pw[lane][jj] = pj;
         }
-    };
-    for (int tb = t0 + warp; tb < tcache_end; tb += kBatch * kConsumerWarps) {
-        if (tb != t0 + warp) load_rows(tb);
+        __syncwarp();
+        // o[h] += sum_b p[h][b] V[tb + b] over the lane's dims
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            if (tb + b * kConsumerWarps < tcache_end) {
-                const float k4[4] = {bf16lo(ka[b].x), bf16hi(ka[b].x), bf16lo(ka[b].y), bf16hi(ka[b].y)};
-                const float v4[4] = {bf16lo(va[b].x), bf16hi(va[b].x), bf16lo(va[b].y), bf16hi(va[b].y)};
-                consume_pos(k4, v4);
+        for (int b = 0; b < kAttnStep; ++b) {
+            float v4[4];
+            if (tb + b == new_t) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v4[i] = sm.vnew[4 * lane + i];
+            } else {
+                v4[0] = bf16lo(va[b].x); v4[1] = bf16hi(va[b].x); v4[2] = bf16lo(va[b].y); v4[3] = bf16hi(va[b].y);
+            }
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj) {
+                const float pj = pw[b][jj];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[jj][i] += pj * v4[i];
             }
         }
+        __syncwarp();
     }
-    if (has_new && warp == (t1 - 1 - t0) % kConsumerWarps) {
-        float k4[4], v4[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) { k4[i] = sm.knew[4 * lane + i]; v4[i] = sm.vnew[4 * lane + i]; }
-        consume_pos(k4, v4);
-    }
+    for (int jj = 0; jj < G; ++jj) l[jj] = warp_sum(l[jj]);
 #pragma unroll
     for (int jj = 0; jj < G; ++jj) {
         if (lane == 0) { sm.wm[warp][jj] = m[jj]; sm.wl[warp][jj] = l[jj]; }
