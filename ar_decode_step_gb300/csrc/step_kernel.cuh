@@ -178,7 +178,14 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     const int new_t = has_new ? t1 - 1 : -1;
     float (*pw)[G] = sm.pw[warp];
     for (int tb = t0 + kAttnStep * warp; tb < t1; tb += kAttnStep * kConsumerWarps) {
-        if (tb != t0 + kAttnStep * warp) load_k(tb);
+        // the value rows of these positions: in flight while the scores are formed
+        uint2 va[kAttnStep];
+#pragma unroll
+        for (int b = 0; b < kAttnStep; ++b) {
+            const int t = tb + b;
+            va[b] = t < tcache_end ? *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane)
+                                   : make_uint2(0u, 0u);
+        }
         // partial scores of the lane's 4 dims, reduced over the warp: lane l
         // ends with the full score of position tb + l mod kAttnStep for every head
         float sc[G][kAttnStep];
@@ -195,14 +202,8 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
             for (int jj = 0; jj < G; ++jj)
                 sc[jj][b] = qr[jj][0] * k4[0] + qr[jj][1] * k4[1] + qr[jj][2] * k4[2] + qr[jj][3] * k4[3];
         }
-        // the value rows of these positions, in flight during the reduction
-        uint2 va[kAttnStep];
-#pragma unroll
-        for (int b = 0; b < kAttnStep; ++b) {
-            const int t = tb + b;
-            va[b] = t < tcache_end ? *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane)
-                                   : make_uint2(0u, 0u);
-        }
+        // the next step's key rows: in flight during the reduction and P.V
+        load_k(tb + kAttnStep * kConsumerWarps);
         const int tl = tb + (lane & (kAttnStep - 1));  // the position this lane's scores belong to
         const bool live = tl < t1;
 #pragma unroll
