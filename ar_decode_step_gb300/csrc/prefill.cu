@@ -282,14 +282,15 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_reg_kernel(const T* X,
 // Rows [row0, row0 + 16) of the prompt against the G query heads of kv head g:
 // warp w takes query head g*G + w for the 16 rows.  Per 64-key tile,
 //   S = Q K^T      mma.sync m16n8k16, bf16 operands, fp32 accumulation
-//                  (Q rounded to bf16 once; K straight from the bf16 cache)
+//                  (Q rounded to bf16 once, or carried as two bf16 terms for
+//                  FP8 contexts; K straight from the bf16 cache)
 //   online softmax in fp32 on the accumulator fragments (row max and the
-//                  rescale of O); P rounded to bf16 and reused in registers as
-//                  the A operand of
+//                  rescale of O); P rounded to bf16 (or two bf16 terms) and
+//                  reused in registers as the A operand of
 //   O += P V       mma.sync, V read transposed from shared memory.
 // Row p attends positions [0, pos0 + p].  K/V tiles are double-buffered in
-// shared memory (cp.async); the row sums are taken over the rounded P, the
-// weights O is built from.
+// shared memory (cp.async); the row sums are taken over the weights O is
+// built from (the rounded P, or the fp32 P when split).
 constexpr int kMmaRows = 16;
 constexpr int kMmaKeys = 64;
 constexpr int kMmaPad = kHeadDim + 8;  // bf16 per shared row: 272 B, the 8 rows of an ldmatrix on distinct banks
@@ -300,6 +301,7 @@ constexpr int attention_mma_smem() {
     return 2 * 2 * kMmaKeys * kMmaPad * (int)sizeof(__nv_bfloat16);
 }
 
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
@@ -327,7 +329,12 @@ __device__ __forceinline__ void cp_async_wait_group() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int G>
+// SPLIT (FP8 contexts): Q and the softmax weights P are each carried as two
+// bf16 terms, hi = bf16(x) and lo = bf16(x - hi), so Q K^T and P V keep about
+// 16 significant bits of the fp32 values (the K/V cache is bf16 exactly); the
+// row sums are taken over the fp32 weights.  Without SPLIT, Q and P are
+// rounded to bf16 once (the W16A16 prefill of BF16 contexts).
+template <int G, bool SPLIT>
 __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, const __nv_bfloat16* kc,
                                                                const __nv_bfloat16* vc, __nv_bfloat16* out,
                                                                float* out_f32, int pos0, int P, int n_q,
@@ -365,7 +372,9 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
     load_tile(0, 0);
 
     // this warp's Q (16 rows x 128 dims) as A fragments, one per 16-dim k-step
+    // (SPLIT: qa = bf16(Q), ql = bf16(Q - qa))
     uint32_t qa[kHeadDim / 16][4];
+    uint32_t ql[SPLIT ? kHeadDim / 16 : 1][4];
     {
         const bool v0 = gi < nrows, v1 = gi + 8 < nrows;
         const float* q0 = Q + ((size_t)(row0 + gi) * n_q + h) * kHeadDim;
@@ -382,6 +391,12 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
             qa[ks][1] = pack_bf16x2(a10.x, a10.y);
             qa[ks][2] = pack_bf16x2(a01.x, a01.y);
             qa[ks][3] = pack_bf16x2(a11.x, a11.y);
+            if constexpr (SPLIT) {
+                ql[ks][0] = pack_bf16x2(a00.x - bf16_round(a00.x), a00.y - bf16_round(a00.y));
+                ql[ks][1] = pack_bf16x2(a10.x - bf16_round(a10.x), a10.y - bf16_round(a10.y));
+                ql[ks][2] = pack_bf16x2(a01.x - bf16_round(a01.x), a01.y - bf16_round(a01.y));
+                ql[ks][3] = pack_bf16x2(a11.x - bf16_round(a11.x), a11.y - bf16_round(a11.y));
+            }
         }
     }
     float o[kHeadDim / 8][4];
@@ -414,6 +429,10 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
                 ldmatrix_x4(b, Ks + (np * 16 + (mat >> 1) * 8 + mrow) * kMmaPad + ks * 16 + (mat & 1) * 8);
                 mma_bf16_16816(s[2 * np], qa[ks], b[0], b[1]);
                 mma_bf16_16816(s[2 * np + 1], qa[ks], b[2], b[3]);
+                if constexpr (SPLIT) {
+                    mma_bf16_16816(s[2 * np], ql[ks], b[0], b[1]);
+                    mma_bf16_16816(s[2 * np + 1], ql[ks], b[2], b[3]);
+                }
             }
         }
         // causal mask: key > position of the row
@@ -456,14 +475,26 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
             o[d][3] *= c1;
         }
         uint32_t pa[kMmaKeys / 16][4];  // P as A fragments, one per 16-key k-step
+        uint32_t pl[SPLIT ? kMmaKeys / 16 : 1][4];  // SPLIT: bf16(P - pa)
 #pragma unroll
         for (int j = 0; j < kMmaKeys / 8; ++j) {
-            const __nv_bfloat162 p01 =
-                __floats2bfloat162_rn(exp2f(s[j][0] * kLog2e - e0), exp2f(s[j][1] * kLog2e - e0));
-            const __nv_bfloat162 p23 =
-                __floats2bfloat162_rn(exp2f(s[j][2] * kLog2e - e1), exp2f(s[j][3] * kLog2e - e1));
-            l0 += __low2float(p01) + __high2float(p01);
-            l1 += __low2float(p23) + __high2float(p23);
+            const float q0 = exp2f(s[j][0] * kLog2e - e0), q1 = exp2f(s[j][1] * kLog2e - e0);
+            const float q2 = exp2f(s[j][2] * kLog2e - e1), q3 = exp2f(s[j][3] * kLog2e - e1);
+            const __nv_bfloat162 p01 = __floats2bfloat162_rn(q0, q1);
+            const __nv_bfloat162 p23 = __floats2bfloat162_rn(q2, q3);
+            if constexpr (SPLIT) {
+                l0 += q0 + q1;
+                l1 += q2 + q3;
+                const __nv_bfloat162 r01 =
+                    __floats2bfloat162_rn(q0 - __low2float(p01), q1 - __high2float(p01));
+                const __nv_bfloat162 r23 =
+                    __floats2bfloat162_rn(q2 - __low2float(p23), q3 - __high2float(p23));
+                pl[j >> 1][(j & 1) * 2] = *reinterpret_cast<const uint32_t*>(&r01);
+                pl[j >> 1][(j & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&r23);
+            } else {
+                l0 += __low2float(p01) + __high2float(p01);
+                l1 += __low2float(p23) + __high2float(p23);
+            }
             pa[j >> 1][(j & 1) * 2] = *reinterpret_cast<const uint32_t*>(&p01);
             pa[j >> 1][(j & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&p23);
         }
@@ -476,6 +507,10 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
                 ldmatrix_x4_trans(b, Vs + (kk * 16 + (mat & 1) * 8 + mrow) * kMmaPad + dp * 16 + (mat >> 1) * 8);
                 mma_bf16_16816(o[2 * dp], pa[kk], b[0], b[1]);
                 mma_bf16_16816(o[2 * dp + 1], pa[kk], b[2], b[3]);
+                if constexpr (SPLIT) {
+                    mma_bf16_16816(o[2 * dp], pl[kk], b[0], b[1]);
+                    mma_bf16_16816(o[2 * dp + 1], pl[kk], b[2], b[3]);
+                }
             }
         }
         __syncthreads();  // this buffer is refilled two tiles on
@@ -502,21 +537,31 @@ __global__ void __launch_bounds__(32 * G) attention_mma_kernel(const float* Q, c
     }
 }
 
-template <int G>
-cudaError_t launch_attention_rows_t(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
-                                    __nv_bfloat16* out, float* out_f32, int pos0, int P, int n_q, int n_kv,
-                                    int max_pos, cudaStream_t s) {
+template <int G, bool SPLIT>
+cudaError_t launch_attention_rows_split(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
+                                        __nv_bfloat16* out, float* out_f32, int pos0, int P, int n_q, int n_kv,
+                                        int max_pos, cudaStream_t s) {
     constexpr int smem = attention_mma_smem<G>();
-    static bool attr = false;
+    static bool attr = false;  // set once, on the first (uncaptured) run of a chunk shape
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem);
+        cudaError_t e = cudaFuncSetAttribute(attention_mma_kernel<G, SPLIT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const dim3 grid((P + kMmaRows - 1) / kMmaRows, n_kv);
-    attention_mma_kernel<G><<<grid, 32 * G, smem, s>>>(Q, kc, vc, out, out_f32, pos0, P, n_q, max_pos);
+    attention_mma_kernel<G, SPLIT><<<grid, 32 * G, smem, s>>>(Q, kc, vc, out, out_f32, pos0, P, n_q, max_pos);
     return cudaGetLastError();
+}
+
+// FP8 contexts (fp32 output, quantised per row next) take the split-bf16
+// operands; BF16 contexts the single bf16 rounding of their W16A16 prefill.
+template <int G>
+cudaError_t launch_attention_rows_t(const float* Q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
+                                    __nv_bfloat16* out, float* out_f32, int pos0, int P, int n_q, int n_kv,
+                                    int max_pos, cudaStream_t s) {
+    return out_f32 ? launch_attention_rows_split<G, true>(Q, kc, vc, out, out_f32, pos0, P, n_q, n_kv, max_pos, s)
+                   : launch_attention_rows_split<G, false>(Q, kc, vc, out, out_f32, pos0, P, n_q, n_kv, max_pos, s);
 }
 
 }  // namespace

@@ -125,15 +125,17 @@ class Fp8Fp32Step:
         x1, x2 = x[..., :h], x[..., h:]
         return torch.cat([x1 * c - x2 * s, x2 * c + x1 * s], dim=-1)
 
-    def step(self, codes):
-        """One frame at self.pos with input `codes`; returns (codes, logits
-        float64 [n_cb][cb_vocab])."""
+    def layer_states(self, codes):
+        """The embedding and every layer at self.pos for input `codes` (K/V
+        rows written at self.pos; the position is not advanced).  Returns the
+        residual stream after the embedding and after each layer."""
         d = self.d
         D, NQ, NKV, I, eps = d.head_dim, d.n_q, d.n_kv, d.inter, d.rms_eps
         pos = self.pos
         h = torch.zeros(d.hidden, dtype=torch.float32)
         for k in range(d.n_cb):
             h = h + self.E[k, int(codes[k])]
+        hs = [h]
         for l, P in enumerate(self.L):
             qkv = self._proj(P["wqkv"], rms_norm(h, P["ln_in"], eps))
             q = self._rope(rms_norm(qkv[:NQ * D].view(NQ, D), P["q_norm"], eps), pos)
@@ -151,7 +153,15 @@ class Fp8Fp32Step:
             g, u = gu[:I], gu[I:]
             m = _round_bf16(g / (1.0 + torch.exp(-g)) * u)
             h = h + self._proj(P["wd"], m)
-        f = rms_norm(h, self.fn, eps)
+            hs.append(h)
+        return hs
+
+    def step(self, codes):
+        """One frame at self.pos with input `codes`; returns (codes, logits
+        float64 [n_cb][cb_vocab])."""
+        d = self.d
+        h = self.layer_states(codes)[-1]
+        f = rms_norm(h, self.fn, d.rms_eps)
         logits = torch.mv(self.head, f).view(d.n_cb, d.cb_vocab).to(torch.float64).numpy()
         out = []
         for k in range(d.n_cb):
@@ -177,3 +187,22 @@ def frame_stats(logits, or_logits, codes, or_codes, or_gaps, gap: float = 1e-2):
     cos = float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
     live = np.asarray(or_gaps) > gap
     return cos, int(live.sum()), int((np.asarray(codes)[live] != np.asarray(or_codes)[live]).sum())
+
+
+def layerwise_spread(orc, hs_of_row, pos0: int, n_layers: int):
+    """Per-row, per-layer contribution cosines of a run against the oracle's
+    layer applied to the run's own input to that layer: hs_of_row(p) gives
+    the run's residual stream [n_layers + 1] of prompt row p (position pos0 +
+    p).  Layers outer, rows inner, so the oracle's cache for layer l holds the
+    rows before p when row p is computed.  Returns the cosines, [n_layers][P]."""
+    out = []
+    P = len(hs_of_row)
+    for l in range(n_layers):
+        row = []
+        for p in range(P):
+            hin = np.asarray(hs_of_row[p][l], np.float64)
+            ho = orc.layer(l, pos0 + p, hin)
+            a, b = np.asarray(hs_of_row[p][l + 1], np.float64) - hin, ho - hin
+            row.append(float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b))))
+        out.append(row)
+    return np.array(out)

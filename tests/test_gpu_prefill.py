@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import synth
+from fp8_restatement import Fp8Fp32Step, layerwise_spread
 from helpers import adopt_gpu_cache, bf16_f64, check_frame, check_kv_rows, cosine, reduced_dims, to_binding_dims, upload_kv
 
 pytestmark = pytest.mark.gpu
@@ -58,19 +59,42 @@ def run_case(ads, d, P, prefix, seed_stream, gamma_variant=False):
     return kv_stat, stat
 
 
+def restatement_prefill_spread(w, d, P, prefix, prompt, max_pos):
+    """The float32 restatement of the FP8 step (exact projection sums) run
+    over the prompt rows and checked by the same layer-by-layer protocol as
+    the GPU: the spread of per-row layer-contribution cosines that fp32
+    arithmetic alone leaves against the oracle.  [n_layers][P]."""
+    r = Fp8Fp32Step(w, max_pos, "exact")
+    orc = oracle.Oracle(w, max_pos, precision=1)
+    if prefix:
+        k, v = synth.make_kv_prefix(d, prefix, max_pos)
+        r.set_kv(k, v, prefix)
+        orc.set_kv(k, v, prefix)
+    else:
+        r.pos = 0
+    rows = []
+    for p in range(P):
+        rows.append([h.numpy() for h in r.layer_states(prompt[p])])
+        r.pos += 1
+    return layerwise_spread(orc, rows, prefix, d.n_layers)
+
+
 def run_case_fp8(ads, d, P, prefix, seed_stream):
     """The batched FP8 W8A8 prefill (tcgen05 kind::f8f6f4 GEMMs, per-token
     activation scales) against the oracle's FP8 layers, layer by layer from
     the GPU's own residual stream (as the FP8 decode step is checked: every
-    layer re-quantises per token, so e4m3 rounding flips from fp32-versus-fp64
-    sums compound across layers).  The layer's K/V rows reach the FP8 bar
-    (cos >= 0.999).  Each row's layer contribution must reach 0.998 and their
-    mean 0.9995: the prefill's attention runs on the tensor cores with bf16 Q
-    and P, so single e4m3 codes of its output (steps of 6-12 %) flip where the
-    oracle's exact attention lands near a rounding boundary, and at this
-    reduced width (1024-wide attention output) one flip moves a row's
-    contribution by up to ~1e-3 of cosine.  The first frame after the
-    prefill, run from the GPU's cache, meets the FP8 frame bar."""
+    layer re-quantises per token).  The attention of FP8 prefills carries Q
+    and P as two bf16 terms each on the tensor cores (about 2^-16 of the
+    oracle's exact attention).  The layer's K/V rows reach the FP8 bar (cos
+    >= 0.999).  Each row's layer contribution is held to the spread that
+    fp32 arithmetic alone leaves under this protocol, measured on the same
+    rows by the float32 restatement with exact projection sums
+    (fp8_restatement.py; the cache each side attends is its own, so rare
+    E4M3 flips of the quantised inputs move single rows by ~1e-3 at this
+    width): no row below the restatement's worst by more than 5e-4, at most
+    3 more rows below 0.999, and a mean no lower by more than 1e-4.  The
+    first frame after the prefill, run from the GPU's cache, meets the FP8
+    frame bar."""
     max_pos = prefix + P + 4
     w = synth.make_weights(d, gamma_variant=True)
     dw = ads.DeviceWeights(w, precision=1)
@@ -85,25 +109,25 @@ def run_case_fp8(ads, d, P, prefix, seed_stream):
     hs = dec.prefill_states(prompt).astype(np.float64)
     assert dec.state()[0] == prefix + P
     gk, gv = dec.get_kv(prefix, prefix + P)
-    worst, coss = 1.0, []
+    G = layerwise_spread(orc, [hs[:, p] for p in range(P)], prefix, d.n_layers)
     for l in range(d.n_layers):
-        for p in range(P):
-            out = orc.layer(l, prefix + p, hs[l, p])
-            c = cosine(hs[l + 1, p] - hs[l, p], out - hs[l, p])
-            worst = min(worst, c)
-            coss.append(c)
-            assert c >= 0.998, f"FP8 prefill P={P} layer {l} row {p}: contribution cos {c}"
         for name, g_, o_ in (("K", gk[l], orc.k[l, :, prefix:prefix + P]), ("V", gv[l], orc.v[l, :, prefix:prefix + P])):
             c = cosine(bf16_f64(g_).ravel(), bf16_f64(o_).ravel())
             assert c >= 0.999, f"FP8 prefill P={P} {name} layer {l}: cos {c}"
-    assert float(np.mean(coss)) >= 0.9995, f"FP8 prefill P={P}: mean contribution cos {np.mean(coss)}"
+    R = restatement_prefill_spread(w, d, P, prefix, prompt, max_pos)
+    stats = dict(gpu_min=float(G.min()), gpu_mean=float(G.mean()), gpu_below=int((G < 0.999).sum()),
+                 fp32_min=float(R.min()), fp32_mean=float(R.mean()), fp32_below=int((R < 0.999).sum()))
+    print(f"FP8 prefill P={P} layer contributions:", stats)
+    assert G.min() >= min(0.999, R.min() - 5e-4), stats
+    assert stats["gpu_below"] <= stats["fp32_below"] + 3, stats
+    assert G.mean() >= R.mean() - 1e-4, stats
     adopt_gpu_cache(dec, orc, prefix + P)
     orc.st.pos = prefix + P
     g = dec.decode_step()
     o, ol, og = orc.decode_step(np.full(8, 1024, np.int32))
     stat = check_frame(g, dec.get_logits(), o, ol, og, True, 0, -1, f"FP8 frame after prefill P={P}")
     dec.close()
-    return worst, float(np.mean(coss)), stat
+    return stats, stat
 
 
 def test_prefill_fp8_batched(ads):
