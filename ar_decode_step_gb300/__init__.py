@@ -391,7 +391,7 @@ class Decoder:
     def trace_step(self, n_sms_max: int = 1024):
         """One decode step with the persistent kernel's phase trace: uint64 ns
         stamps shaped [n_cta][stride]."""
-        cap = n_sms_max * (8 + 27 * self.dims.n_layers) + 2 * 4 * 2048
+        cap = n_sms_max * (8 + 31 * self.dims.n_layers) + 2 * 4 * 2048
         buf = np.zeros(cap, np.uint64)
         st, nc = ctypes.c_int(), ctypes.c_int()
         _call("tts_trace_step", self._ctx, _ptr(buf), cap, ctypes.byref(st), ctypes.byref(nc))

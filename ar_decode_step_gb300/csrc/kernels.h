@@ -232,8 +232,10 @@ struct StepParams {
 //   (k = 4: head), [4 + 19 L + 1] producer done; [8 + 19 L + 4 l + k] ns the
 //   consumers waited for ring data in layer l's projection k; [8 + 23 L +
 //   4 l + k] ns the producer waited for free slots (the head adds to the last
-//   layer's down-proj slot).
-inline int step_trace_stride(int n_layers) { return 8 + 27 * n_layers; }
+//   layer's down-proj slot); [8 + 27 L + 4 l + k] the attention unit of layer
+//   l: k = 0 inputs loaded (queries and the new key/value row ready), 1
+//   positions done, 2 warps merged, 3 splits merged (CTAs without a unit: 0).
+inline int step_trace_stride(int n_layers) { return 8 + 31 * n_layers; }
 
 cudaError_t step_prepare(int prec, int G, int smem);
 int step_attn_scratch_bytes(int G);

@@ -34,7 +34,7 @@ namespace {
 using namespace core;
 
 constexpr int kMaxHRows = 256;     // rows of h one CTA owns, at most
-constexpr int kAttnMinChunk = 32;   // positions per attention split, at least (no merge below)
+constexpr int kAttnMinChunk = 64;   // positions per attention split, at least (no merge below)
 
 // Grid barrier among the consumer warps of all CTAs.  `gbar` counts arrivals
 // over the launch (zeroed before it); barrier k (1-based) waits for
@@ -100,10 +100,15 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[kAttnStep]) {
 
 // One (kv head g, split) unit of the decode attention of one layer, run by the
 // consumer warps of this CTA (no waits inside).
-template <int G, bool FP8>
+template <int G, bool FP8, bool TRACE>
 __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLayer& L, int layer, int pos, int g,
                                                int split, int nsplit, int chunk, unsigned char* scratch, int* s_last,
                                                float* red) {
+    auto mark = [&](int k) {  // traced launches: the unit's progress
+        if constexpr (TRACE)
+            if (threadIdx.x == 0)
+                p.trace[(size_t)blockIdx.x * p.trace_stride + 8 + 27 * p.n_layers + 4 * layer + k] = globaltimer_ns();
+    };
     AttnSmem<G>& sm = *reinterpret_cast<AttnSmem<G>*>(scratch);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int len = pos + 1;
@@ -139,7 +144,7 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     // position).  The new position's row (t1 - 1 when has_new) comes from
     // shared memory.
     const int tcache_end = has_new ? t1 - 1 : t1;  // cached rows; the new row comes from smem
-    uint2 ka[kAttnStep];
+    uint2 ka[kAttnStep];  // the key rows of the warp's next step
     auto load_k = [&](int tb) {
 #pragma unroll
         for (int b = 0; b < kAttnStep; ++b) {
@@ -166,6 +171,7 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
         }
     }
     consumer_sync();
+    mark(0);
 
     float m[G], l[G], o[G][4], qr[G][4];
 #pragma unroll
@@ -241,6 +247,7 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     }
 #pragma unroll
     for (int jj = 0; jj < G; ++jj) l[jj] = warp_sum(l[jj]);
+    mark(1);
 #pragma unroll
     for (int jj = 0; jj < G; ++jj) {
         if (lane == 0) { sm.wm[warp][jj] = m[jj]; sm.wl[warp][jj] = l[jj]; }
@@ -278,8 +285,11 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
             if (threadIdx.x == 0) p.attn_mx[g] = mx;
         }
         consumer_sync();
+        mark(2);
+        mark(3);
         return;
     }
+    mark(2);
     // the last split of this kv head merges all splits
     __threadfence();
     consumer_sync();
@@ -287,10 +297,27 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     consumer_sync();
     if (*s_last) {
         __threadfence();
-        // all splits' (max, sum) pairs into shared memory first: one parallel round trip
+        // every split's (max, sum) pairs and partial outputs in one round trip:
+        // the pairs into shared memory, the outputs of this thread's entries
+        // (idx = threadIdx.x + 256 e) into registers, kMergeBatch splits at a time
+        constexpr int kMergeBatch = 20;
+        constexpr int kEntries = (G * kHeadDim + kConsumers - 1) / kConsumers;
         const float* po0 = p.part_o + ((size_t)g * p.S * G) * kHeadDim;
         const float* pml0 = p.part_ml + ((size_t)g * p.S * G) * 2;
         float* mlw = &sm.wo[0][0][0];  // reuse: [nsplit][G][2] pairs, then [nsplit][G] weights
+        float pv[kEntries][kMergeBatch];
+        auto load_po = [&](int s0) {
+#pragma unroll
+            for (int e = 0; e < kEntries; ++e) {
+                const int idx = threadIdx.x + kConsumers * e;
+                const int jj = idx / kHeadDim, d = idx % kHeadDim;
+#pragma unroll
+                for (int b = 0; b < kMergeBatch; ++b)
+                    pv[e][b] = (idx < G * kHeadDim && s0 + b < nsplit)
+                                   ? __ldcg(po0 + ((size_t)(s0 + b) * G + jj) * kHeadDim + d) : 0.f;
+            }
+        };
+        load_po(0);
         for (int i = threadIdx.x; i < nsplit * G * 2; i += kConsumers) mlw[i] = __ldcg(pml0 + i);
         consumer_sync();
         float* wgt = mlw + nsplit * G * 2;
@@ -308,14 +335,26 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
             lsum[jj] = Ls;
         }
         consumer_sync();
-        for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kConsumers) {
-            const int jj = idx / kHeadDim, d = idx % kHeadDim;
-            float O = 0.f;
-#pragma unroll 8
-            for (int s = 0; s < nsplit; ++s) O += __ldcg(po0 + ((size_t)s * G + jj) * kHeadDim + d) * wgt[s * G + jj];
-            const float a = O / lsum[jj];
-            p.attn[(size_t)(g * G + jj) * kHeadDim + d] = a;
-            mx = fmaxf(mx, fabsf(a));
+        float acc[kEntries] = {};
+        for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+            if (s0 > 0) load_po(s0);
+#pragma unroll
+            for (int e = 0; e < kEntries; ++e) {
+                const int jj = (threadIdx.x + kConsumers * e) / kHeadDim;
+#pragma unroll
+                for (int b = 0; b < kMergeBatch; ++b)
+                    if (s0 + b < nsplit) acc[e] += pv[e][b] * wgt[(s0 + b) * G + jj];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kEntries; ++e) {
+            const int idx = threadIdx.x + kConsumers * e;
+            if (idx < G * kHeadDim) {
+                const int jj = idx / kHeadDim, d = idx % kHeadDim;
+                const float a = acc[e] / lsum[jj];
+                p.attn[(size_t)(g * G + jj) * kHeadDim + d] = a;
+                mx = fmaxf(mx, fabsf(a));
+            }
         }
         if constexpr (FP8) {
             mx = consumer_max(mx, red);
@@ -324,6 +363,7 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
         if (threadIdx.x == 0) p.att_counter[g] = 0u;
     }
     consumer_sync();
+    mark(3);
 }
 
 // Per-CTA constants of one launch, worked out once at kernel start and kept
@@ -477,13 +517,13 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
 }
 
 // This CTA's attention unit of layer l (no-op for CTAs without one).  Not inlined.
-template <int G, bool FP8>
+template <int G, bool FP8, bool TRACE>
 __device__ __noinline__ void attn_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l,
                                         int* s_last, float* red) {
     if ((int)blockIdx.x >= cs.nunits) return;
     const StepSmem m = step_smem(smem, p);
-    attention_unit<G, FP8>(p, m.sl[l], l, cs.pos, blockIdx.x / cs.nsplit, blockIdx.x % cs.nsplit, cs.nsplit,
-                           cs.chunk, m.xs, s_last, red);
+    attention_unit<G, FP8, TRACE>(p, m.sl[l], l, cs.pos, blockIdx.x / cs.nsplit, blockIdx.x % cs.nsplit, cs.nsplit,
+                                  cs.chunk, m.xs, s_last, red);
 }
 
 template <int PREC, int G, bool TRACE>
@@ -738,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if ((it = proj_phase<FP8, 0, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
         if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 2);
-        attn_phase<G, FP8>(s_p, s_cs, smem, l, &s_last, red);
+        attn_phase<G, FP8, TRACE>(s_p, s_cs, smem, l, &s_last, red);
         trace_mark<TRACE>(p, ev + 3);
         if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 4);
