@@ -145,6 +145,7 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     // shared memory.
     const int tcache_end = has_new ? t1 - 1 : t1;  // cached rows; the new row comes from smem
     uint2 ka[kAttnStep];  // the key rows of the warp's next step
+    uint2 va[kAttnStep];  // the value rows of its current step
     auto load_k = [&](int tb) {
 #pragma unroll
         for (int b = 0; b < kAttnStep; ++b) {
@@ -153,7 +154,16 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
                                    : make_uint2(0u, 0u);
         }
     };
+    auto load_v = [&](int tb) {
+#pragma unroll
+        for (int b = 0; b < kAttnStep; ++b) {
+            const int t = tb + b;
+            va[b] = t < tcache_end ? *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane)
+                                   : make_uint2(0u, 0u);
+        }
+    };
     load_k(t0 + kAttnStep * warp);
+    load_v(t0 + kAttnStep * warp);
     if (warp < G) norm_rope(p.qkv + (size_t)(g * G + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
     if (has_new && warp == G) {
         norm_rope(p.qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
@@ -184,14 +194,9 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     const int new_t = has_new ? t1 - 1 : -1;
     float (*pw)[G] = sm.pw[warp];
     for (int tb = t0 + kAttnStep * warp; tb < t1; tb += kAttnStep * kConsumerWarps) {
-        // the value rows of these positions: in flight while the scores are formed
-        uint2 va[kAttnStep];
-#pragma unroll
-        for (int b = 0; b < kAttnStep; ++b) {
-            const int t = tb + b;
-            va[b] = t < tcache_end ? *reinterpret_cast<const uint2*>(vc + (size_t)t * kHeadDim + 4 * lane)
-                                   : make_uint2(0u, 0u);
-        }
+        // the value rows of these positions (the first step's came with its
+        // key rows): in flight while the scores are formed
+        if (tb != t0 + kAttnStep * warp) load_v(tb);
         // partial scores of the lane's 4 dims, reduced over the warp: lane l
         // ends with the full score of position tb + l mod kAttnStep for every head
         float sc[G][kAttnStep];
