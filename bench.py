@@ -395,7 +395,7 @@ def time_one_layer(ads, host_w, args, clocks):
         dec.set_input(codes)
         if i == args.warmup:
             w0 = time.time()
-        flush.sum(dtype=torch.int32)  # read 512 MB: the step starts from a cold L2
+        flush.sum()  # read 512 MB (one reduction kernel): the step starts from a cold L2
         dec.decode_steps(1)
         if i >= args.warmup:
             times.append(dec.last_steps_ms())
