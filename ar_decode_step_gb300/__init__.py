@@ -421,9 +421,10 @@ class Decoder:
         return buf.reshape(self.dims.n_layers + 1, P, self.dims.hidden)
 
     def debug_expire_wait(self) -> int:
-        """tts_debug_expire_wait: one step launch whose first grid barrier
-        cannot complete and whose waits give up after 1 ms; returns the
-        status code (TTS_ERR_DEVICE, -5, when the timeout was detected)."""
+        """tts_debug_expire_wait: one step launch whose first wait (for the
+        embedding, never stored) cannot complete and whose waits give up
+        after 1 ms; returns the status code (TTS_ERR_DEVICE, -5, when the
+        timeout was detected)."""
         return int(load().tts_debug_expire_wait(self._ctx))
 
     def last_steps_ms(self) -> float:

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     constexpr int CEPI = EPI == kEpiLogits ? kEpiStore : EPI;
     if (!consume<FP8, CEPI>(j, ring, it, xr, sa, part, &s_abort, p.err)) return;
     if constexpr (EPI == kEpiLogits)
-        head_tail(p.y, p.n_cb, p.cb_vocab, p.st, p.counter, p.hist, p.hist_cap, &s_last, s_codes);
+        head_tail(p.y, p.n_cb, p.cb_vocab, p.st, p.counter, 0u, p.hist, p.hist_cap, &s_last, s_codes);
 }
 
 template <int PREC, int PRO, int EPI>

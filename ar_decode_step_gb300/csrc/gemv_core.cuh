@@ -85,6 +85,20 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Barrier among the consumer warps only (the producer warp does not take part).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+// The same barrier, returning whether v was true in any consumer thread: a
+// decision every consumer thread takes alike (to stop after a failed wait).
+__device__ __forceinline__ bool consumer_sync_or(bool v) {
+    unsigned r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((unsigned)v), "n"(kConsumers)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ float consumer_sum(float v, float* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -109,6 +123,115 @@ __device__ __forceinline__ float consumer_max(float v, float* red) {
     for (int i = 1; i < kConsumerWarps; ++i) s = fmaxf(s, red[i]);
     consumer_sync();
     return s;
+}
+
+// ---- data exchange between the phases of the persistent step -----------------
+// Each vector a phase of the persistent step hands to the next (qkv, the
+// attention output, the residual stream after the attention and after the
+// MLP, the MLP activation) has a buffer of its own per layer, set to kUnset
+// before every launch, and an arrival counter, also kUnset at launch.
+// Producers store their elements once, then each producing CTA adds 1 to the
+// counter, with no fence in between.  A consumer CTA waits (one thread
+// polling) until the counter shows every producer, then loads the vector and
+// re-reads any element still kUnset: the data is the signal, the counter
+// only says when to start reading (it keeps thousands of threads from
+// polling the data lines while the producers work).  So no CTA waits for a
+// fence, and there is no grid barrier.  Arithmetic never makes the bit
+// pattern kUnset (a negative NaN with every payload bit set; NaNs from
+// arithmetic are the canonical 0x7fffffff).
+constexpr uint32_t kUnset = 0xffffffffu;
+
+__device__ __forceinline__ bool unset4(const float4& v) {
+    return __float_as_uint(v.x) == kUnset || __float_as_uint(v.y) == kUnset || __float_as_uint(v.z) == kUnset ||
+           __float_as_uint(v.w) == kUnset;
+}
+__device__ __forceinline__ float4 ld_relaxed4(const float4* p) {
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed(float* p, float v) {
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// What a polling wait needs: where to record a timeout, the CTA's abort flag
+// (set by any of its threads that gave up) and the wait's limit in ns.
+struct Poll {
+    int* err;
+    volatile int* abort;
+    uint64_t limit_ns;
+};
+
+// Re-read the float4 at p until none of its elements is kUnset and return
+// it.  If the wait ran out (the timeout is recorded) or the launch is
+// aborting, *w.abort is set and the value returned is still unset.  (Values
+// go in and out by value: a reference would move the caller's registers to
+// local memory.)
+static __device__ __noinline__ float4 poll4_wait(const float4* p, const Poll& w) {
+    const uint64_t t0 = globaltimer_ns();
+    for (unsigned n = 1;; ++n) {
+        __nanosleep(64);
+        const float4 v = ld_relaxed4(p);
+        if (!unset4(v)) return v;
+        if ((n & 15) == 0) {
+            if (*w.abort || (w.err && (*reinterpret_cast<volatile int*>(w.err) & kErrTimeout))) {
+                *w.abort = 1;
+                return v;
+            }
+            if (globaltimer_ns() - t0 > w.limit_ns) {
+                if (w.err) atomicOr(w.err, kErrTimeout);
+                *w.abort = 1;
+                return v;
+            }
+        }
+    }
+}
+// One float4 of an exchanged vector, waiting until it is written (still
+// unset only if the wait failed).
+__device__ __forceinline__ float4 poll4(const float4* p, const Poll& w) {
+    const float4 v = ld_relaxed4(p);
+    return unset4(v) ? poll4_wait(p, w) : v;
+}
+
+// Announce this CTA's stores of an exchanged vector: after every consumer
+// thread issued its stores, one relaxed add to the vector's counter.
+__device__ __forceinline__ void xch_publish(unsigned* ctr) {
+    consumer_sync();
+    if (threadIdx.x == 0) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+// Thread 0's half of xch_wait.
+static __device__ __noinline__ void xch_wait_thread(const unsigned* ctr, unsigned n, const Poll& w) {
+    uint64_t t0 = 0;
+    for (unsigned k = 0;; ++k) {
+        unsigned v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v - kUnset >= n) return;  // the counter started at kUnset
+        __nanosleep(32);
+        if ((k & 15) == 15) {
+            if (*w.abort || (w.err && (*reinterpret_cast<volatile int*>(w.err) & kErrTimeout))) {
+                *w.abort = 1;
+                return;
+            }
+            const uint64_t t = globaltimer_ns();
+            if (!t0) t0 = t;
+            else if (t - t0 > w.limit_ns) {
+                if (w.err) atomicOr(w.err, kErrTimeout);
+                *w.abort = 1;
+                return;
+            }
+        }
+    }
+}
+// Wait until n producer CTAs have announced their stores to the vector of
+// counter ctr (thread 0 polls; the other consumer threads wait at the
+// barrier).  False, for every consumer thread alike, if the wait ran out or
+// the launch is aborting.
+__device__ __forceinline__ bool xch_wait(const unsigned* ctr, unsigned n, const Poll& w) {
+    if (threadIdx.x == 0) xch_wait_thread(ctr, n, w);
+    return !consumer_sync_or(*w.abort);
 }
 
 // ---- one projection as seen by one CTA ---------------------------------------
@@ -349,139 +472,144 @@ __device__ __forceinline__ void load_xseg_smem(const unsigned char* xs, int CPR,
 // segment straight from global memory (through L2: other CTAs wrote it) into
 // registers, all loads in flight at once.  Needs no shared staging and no
 // block barrier.  Same values and layout as load_xseg_smem after stage_x.
-__device__ __forceinline__ void load_xseg_plain(const float* x, int c0, int c1, XSeg<false>& xr) {
+// With a Poll, x is an exchanged vector: elements still kUnset are re-read
+// until written (all loads are first issued together); a failed wait sets
+// *w->abort.
+__device__ __forceinline__ void load_xseg_plain(const float* x, int c0, int c1, XSeg<false>& xr,
+                                                const Poll* w = nullptr) {
     const int lane = threadIdx.x & 31;
     const float4* x4 = reinterpret_cast<const float4*>(x);
 #pragma unroll
     for (int i = 0; i < kMaxLaneChunks; ++i) {
         const int c = c0 + lane + 32 * i;
-        xr.a[i] = c < c1 ? __ldcg(x4 + 2 * c) : float4{};
-        xr.b[i] = c < c1 ? __ldcg(x4 + 2 * c + 1) : float4{};
+        xr.a[i] = c < c1 ? ld_relaxed4(x4 + 2 * c) : float4{};
+        xr.b[i] = c < c1 ? ld_relaxed4(x4 + 2 * c + 1) : float4{};
+    }
+    if (!w) return;
+#pragma unroll
+    for (int i = 0; i < kMaxLaneChunks; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < c1) {
+            if (unset4(xr.a[i])) xr.a[i] = poll4_wait(x4 + 2 * c, *w);
+            if (unset4(xr.b[i])) xr.b[i] = poll4_wait(x4 + 2 * c + 1, *w);
+        }
     }
 }
 
-// Statistics a phase publishes for the next phase's activation staging.
-struct XStats {
-    const float2* h;   // per producing CTA: {sum of squares, max |h * gamma_next|} (RMSNorm inputs)
-    const float* mx;   // per producing unit: max |x| (plain FP8 inputs)
-    int n;             // entries
-    // FP8 only, both optional: this site's static activation scale (used when
-    // > 0 instead of the per-token amax / 448), and an amax accumulator that
-    // calibration runs raise to the largest amax seen
-    const float* sa_static = nullptr;
-    float* calib = nullptr;
-};
-
-// Stage an activation vector whose statistics the producing phase published,
-// into the shared layout of stage_x, with no block-wide reduction.
+// Stage an exchanged activation vector (see "data exchange" above) for a
+// projection with inner dimension K into the shared layout of stage_x,
+// waiting for its elements:
 //   RMS:   x = h * r * gamma, r = 1/sqrt(sum(h^2)/K + eps)   (K <= kMaxRmsK)
-//   FP8:   sa = max(amax, 1e-12)/448, amax = r * max|h*gamma| (RMS) or max|x|;
-//          x8 = e4m3(x/sa) stored as bytes
-//   plain bf16: a permuted copy, issued as asynchronous 16-byte copies.
-// x is read through L2 (other CTAs wrote it).  The first batch of x is loaded
-// together with the statistics (one memory round trip); every warp reduces the
-// statistics itself (fixed order), so the only synchronisation is the final
-// barrier.  Returns sa (1 for bf16).
+//   FP8:   sa = max(amax, 1e-12)/448, amax over the (normalised) values, or
+//          the site's static scale when one is set; x8 = e4m3(x/sa) as bytes
+// (plain bf16 inputs are not staged: the stage loop reads them itself).
+// Every thread waits for its own elements, then the CTA reduces the
+// statistics in a fixed order.  Plain FP8 inputs go through xf, an fp32
+// scratch of K floats in shared memory, filled by asynchronous copies.
+// Returns sa (1 for bf16), or -1 if a wait ran out (every consumer thread
+// returns, having passed the same barriers).
 template <bool FP8, bool RMS>
-__device__ __forceinline__ float stage_x_stats(const float* x, const __nv_bfloat16* gamma, int K, float eps,
-                                               const XStats& st, unsigned char* xs) {
-    const int lane = threadIdx.x & 31;
+__device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, float eps, const float* sa_static,
+                             float* calib, unsigned char* xs, float* xf, float* red, const Poll& w) {
     const int cpr = K / (FP8 ? 16 : 8);
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int n4 = K / 4;
-    if constexpr (!FP8 && !RMS) {
-        // plain bf16 input: float4 i goes to plane i % 2, chunk i / 2
-        for (int i = threadIdx.x; i < n4; i += kConsumers)
-            cp_async16(xs + 16 * ((i & 1) * cpr + (i >> 1)), x4 + i);
-        cp_async_wait_all();
-        consumer_sync();
-        return 1.0f;
-    }
-    // a batch: kB float4 per thread; RMS inputs fit one batch
-    constexpr int kB = kMaxRmsK / 4 / kConsumers;
-    float4 v[kB];
-    uint2 g[kB];
-    auto load = [&](int base) {
+    if (FP8 && sa_static) prefetch_l1(sa_static);
+    float sa = 1.0f;
+    if constexpr (RMS) {
+        constexpr int kB = kMaxRmsK / 4 / kConsumers;
+        float4 v[kB];
+        uint2 g[kB];
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
-            const int i = base + threadIdx.x + k * kConsumers;
+            const int i = threadIdx.x + k * kConsumers;
             if (i < n4) {
-                v[k] = __ldcg(x4 + i);
-                if constexpr (RMS) g[k] = *reinterpret_cast<const uint2*>(gamma + 4 * i);
+                v[k] = ld_relaxed4(x4 + i);
+                g[k] = *reinterpret_cast<const uint2*>(gamma + 4 * i);
             }
         }
-    };
-    // FP8: the site's static activation scale is pulled into L1 while x loads
-    if (FP8 && st.sa_static) prefetch_l1(st.sa_static);
-    load(0);
-    float r = 1.0f, sa = 1.0f;
-    {
-        constexpr int kMaxStatLoads = 8;  // 256 entries
-        float ss = 0.f, am = 0.f;
+        float ss = 0.f;
 #pragma unroll
-        for (int k = 0; k < kMaxStatLoads; ++k) {
-            const int i = lane + 32 * k;
-            if (i < st.n) {
-                if constexpr (RMS) {
-                    const float2 w = __ldcg(st.h + i);
-                    ss += w.x;
-                    am = fmaxf(am, w.y);
-                } else {
-                    am = fmaxf(am, __ldcg(st.mx + i));
-                }
+        for (int k = 0; k < kB; ++k) {
+            const int i = threadIdx.x + k * kConsumers;
+            if (i < n4) {
+                if (unset4(v[k])) v[k] = poll4_wait(x4 + i, w);
+                ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
             }
         }
-        if constexpr (RMS) {
-            ss = warp_sum(ss);
-            r = 1.0f / sqrtf(ss / (float)K + eps);
+        const float r = 1.0f / sqrtf(consumer_sum(ss, red) / (float)K + eps);
+        float am = 0.f;
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+            v[k].x *= r * bf16lo(g[k].x);
+            v[k].y *= r * bf16hi(g[k].x);
+            v[k].z *= r * bf16lo(g[k].y);
+            v[k].w *= r * bf16hi(g[k].y);
+            if (FP8 && threadIdx.x + k * kConsumers < n4)
+                am = fmaxf(am, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
         }
         if constexpr (FP8) {
-            am = warp_max(am);
-            if constexpr (RMS) am *= r;
+            am = consumer_max(am, red);
             sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
             // non-negative floats order like their bit patterns
-            if (st.calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(st.calib), __float_as_int(am));
-            if (st.sa_static) {
-                const float ss_ = *st.sa_static;
+            if (calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(calib), __float_as_int(am));
+            if (sa_static) {
+                const float ss_ = *sa_static;
                 if (ss_ > 0.f) sa = ss_;  // static: values beyond 448 * sa saturate
             }
         }
-    }
-    for (int base = 0; base < n4; base += kB * kConsumers) {
-        if (base > 0) load(base);
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
-            const int i = base + threadIdx.x + k * kConsumers;
+            const int i = threadIdx.x + k * kConsumers;
             if (i < n4) {
-                float4 u = v[k];
-                if constexpr (RMS) {
-                    u.x = u.x * r * bf16lo(g[k].x);
-                    u.y = u.y * r * bf16hi(g[k].x);
-                    u.z = u.z * r * bf16lo(g[k].y);
-                    u.w = u.w * r * bf16hi(g[k].y);
-                }
                 const int e = 4 * i;
                 if constexpr (!FP8) {
-                    reinterpret_cast<float4*>(xs)[((e & 7) >> 2) * cpr + (e >> 3)] = u;
+                    reinterpret_cast<float4*>(xs)[((e & 7) >> 2) * cpr + (e >> 3)] = v[k];
                 } else {
                     reinterpret_cast<uint32_t*>(xs)[i] =
-                        e4m3_byte(__fdiv_rn(u.x, sa)) | (e4m3_byte(__fdiv_rn(u.y, sa)) << 8) |
-                        (e4m3_byte(__fdiv_rn(u.z, sa)) << 16) | (e4m3_byte(__fdiv_rn(u.w, sa)) << 24);
+                        e4m3_byte(__fdiv_rn(v[k].x, sa)) | (e4m3_byte(__fdiv_rn(v[k].y, sa)) << 8) |
+                        (e4m3_byte(__fdiv_rn(v[k].z, sa)) << 16) | (e4m3_byte(__fdiv_rn(v[k].w, sa)) << 24);
                 }
             }
         }
+    } else {
+        static_assert(FP8, "plain bf16 inputs are read by the stage loop");
+        // the whole vector into xf at once, then the elements still unset re-read
+        for (int i = threadIdx.x; i < n4; i += kConsumers) cp_async16(xf + 4 * i, x4 + i);
+        cp_async_wait_all();
+        float am = 0.f;
+        for (int i = threadIdx.x; i < n4; i += kConsumers) {
+            float4 v = reinterpret_cast<const float4*>(xf)[i];
+            if (unset4(v)) {
+                v = poll4_wait(x4 + i, w);
+                reinterpret_cast<float4*>(xf)[i] = v;
+            }
+            am = fmaxf(am, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        am = consumer_max(am, red);
+        sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+        if (calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(calib), __float_as_int(am));
+        if (sa_static) {
+            const float ss_ = *sa_static;
+            if (ss_ > 0.f) sa = ss_;
+        }
+        for (int i = threadIdx.x; i < n4; i += kConsumers) {
+            const float4 v = reinterpret_cast<const float4*>(xf)[i];
+            reinterpret_cast<uint32_t*>(xs)[i] =
+                e4m3_byte(__fdiv_rn(v.x, sa)) | (e4m3_byte(__fdiv_rn(v.y, sa)) << 8) |
+                (e4m3_byte(__fdiv_rn(v.z, sa)) << 16) | (e4m3_byte(__fdiv_rn(v.w, sa)) << 24);
+        }
     }
-    consumer_sync();
-    return sa;
+    return consumer_sync_or(*w.abort) ? -1.0f : sa;
 }
 
-// What the epilogue publishes for the next phase (all optional).
-struct StatsOut {
-    float2* h;                     // kEpiResid: this CTA's {sum y^2, max |y * gamma|} at [blockIdx.x]
-    const __nv_bfloat16* gamma;    //   gain of the next RMSNorm (for the max)
-    float* mx;                     // kEpiSwiglu: this CTA's max |y| at [blockIdx.x]
-    float* rows;                   // kEpiResid: shared-memory copy of this CTA's rows of y (read and
-                                   //   updated instead of global memory), or null
+// Where the persistent step's epilogue puts its outputs (both optional).
+struct EpiOut {
+    float* rows;  // kEpiResid: shared-memory copy of this CTA's rows of y (read and updated
+                  //   instead of global memory), or null
+    float* xout;  // the exchange buffer of y: every output stored there for the next phase
+                  //   (y itself is then written only by kEpiResid, the residual stream kept
+                  //   for the host)
 };
 
 // The tensor-core FP8 stage loop's per-lane constants for one projection (the
@@ -575,15 +703,14 @@ __device__ __forceinline__ void fp8_stage(const unsigned char* sbuf, const Fp8La
 }
 
 // Consumers: reduce projection j's stages from the ring against the lane's
-// activation registers, then apply the epilogue to this CTA's outputs (and
-// publish statistics).  `part` holds proj_stages(j) * rs * wpr floats.  `red` is
-// shared scratch for the statistics reduction.  Returns false if a wait ran out.
+// activation registers, then apply the epilogue to this CTA's outputs.
+// `part` holds proj_stages(j) * rs * wpr floats.  Returns false if a wait ran
+// out or the launch is aborting (every consumer thread alike).
 template <bool FP8, int EPI>
 __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it, const XSeg<FP8>& xr, float sa,
                                         float* part, volatile int* abort, int* err,
-                                        unsigned long long* wait_ns = nullptr, const StatsOut* so = nullptr,
-                                        float* red = nullptr, unsigned long long* stage_tr = nullptr,
-                                        int stage_tr_n = 0) {
+                                        unsigned long long* wait_ns = nullptr, const EpiOut* so = nullptr,
+                                        unsigned long long* stage_tr = nullptr, int stage_tr_n = 0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int r0, r1;
     proj_rows(j, r0, r1);
@@ -596,17 +723,14 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
     proj_segment(j, warp, rslot, sg, c0, c1);
     Fp8Lane fl{};
     if constexpr (FP8) fl = fp8_lane(CPR, rowb, RS, opst, WPR);
-    // the epilogue's operands in global memory (per-row weight scales, the
-    // next RMSNorm's gain) are pulled into L1 now, so that the epilogue's loads
-    // hit L1 instead of waiting for L2 behind the weight stream; a prefetch
-    // holds no register, so nothing waits for it
-    if (threadIdx.x < nrows) {
-        const int n = r0 + threadIdx.x;
-        if constexpr (FP8) {
-            prefetch_l1(j.wscale + n);
-            if (EPI == kEpiSwiglu) prefetch_l1(j.wscale + j.N + n);
+    // FP8: the epilogue's per-row weight scales are pulled into L1 now, so
+    // that its loads hit L1 instead of waiting for L2 behind the weight
+    // stream; a prefetch holds no register, so nothing waits for it
+    if constexpr (FP8) {
+        if (threadIdx.x < nrows) {
+            prefetch_l1(j.wscale + r0 + threadIdx.x);
+            if (EPI == kEpiSwiglu) prefetch_l1(j.wscale + j.N + r0 + threadIdx.x);
         }
-        if (EPI == kEpiResid && so && so->h && so->gamma) prefetch_l1(so->gamma + n);
     }
 
     bool ok = true;
@@ -616,7 +740,8 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
     for (int s = 0; s < nst; ++s, ++it) {
         const bool timed = wait_ns && threadIdx.x == 0;  // traced runs: thread 0 times its data waits
         const uint64_t tw = timed ? globaltimer_ns() : 0;
-        const bool got = mbar_wait_or_abort(&ring.full[slot], phase, abort);
+        // the warp stops as one: a lane that gave up stops its neighbours too
+        const bool got = __all_sync(0xffffffffu, mbar_wait_or_abort(&ring.full[slot], phase, abort));
         if (timed) waited += globaltimer_ns() - tw;
         if (!got) {
             if (lane == 0 && err) atomicOr(err, kErrTimeout);
@@ -661,11 +786,9 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
         }
     }
     if (wait_ns && threadIdx.x == 0) *wait_ns += waited;
-    consumer_sync();
-    if (!ok || *abort) return false;
+    if (consumer_sync_or(!ok || *abort)) return false;
 
     // per-row sums over segments (in segment order) and the epilogue
-    float st_ss = 0.f, st_mx = 0.f;
     for (int r = threadIdx.x; r < nrows; r += kConsumers) {
         const int n = r0 + r;
         const int s = r / opst, jj = r % opst;
@@ -685,8 +808,8 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
             } else {
                 m = silu(g) * u;
             }
-            j.y[n] = m;
-            st_mx = fmaxf(st_mx, fabsf(m));
+            if (so && so->xout) st_relaxed(so->xout + n, m);
+            else j.y[n] = m;
         } else {
             float o = row_sum(jj);
             if constexpr (FP8) o = round_bf16(o * (sa * j.wscale[n]));
@@ -697,22 +820,13 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
                 } else {
                     o = __ldcg(j.y + n) + o;
                 }
-                if (so && so->h) {
-                    st_ss += o * o;
-                    if (so->gamma) st_mx = fmaxf(st_mx, fabsf(o * __bfloat162float(so->gamma[n])));
-                }
             }
-            j.y[n] = o;
-        }
-    }
-    if (so && red) {
-        if (so->h) {
-            const float ss = consumer_sum(st_ss, red);
-            const float mx = consumer_max(st_mx, red);
-            if (threadIdx.x == 0) so->h[blockIdx.x] = make_float2(ss, mx);
-        } else if (so->mx) {
-            const float mx = consumer_max(st_mx, red);
-            if (threadIdx.x == 0) so->mx[blockIdx.x] = mx;
+            if (so && so->xout) {
+                st_relaxed(so->xout + n, o);
+                if constexpr (EPI == kEpiResid) j.y[n] = o;
+            } else {
+                j.y[n] = o;
+            }
         }
     }
     return true;
@@ -727,19 +841,19 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
 template <bool FP8, int EPI>
 __device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, const unsigned char* xs, float sa,
                                         float* part, volatile int* abort, int* err, unsigned long long* wait_ns,
-                                        const StatsOut* so, float* red, unsigned long long* stage_tr,
-                                        int stage_tr_n, const float* xplain = nullptr) {
+                                        const EpiOut* so, unsigned long long* stage_tr, int stage_tr_n,
+                                        const float* xplain = nullptr, const Poll* poll = nullptr) {
     int rslot, sg, c0, c1;
     proj_segment(j, threadIdx.x >> 5, rslot, sg, c0, c1);
     XSeg<FP8> xr;
     if constexpr (!FP8) {
-        if (xplain) load_xseg_plain(xplain, c0, c1, xr);
+        // a failed wait sets *abort: the stage loop then stops, all threads alike
+        if (xplain) load_xseg_plain(xplain, c0, c1, xr, poll);
         else load_xseg_smem<false>(xs, proj_cpr(j), c0, c1, xr);
     } else {
         load_xseg_smem<true>(xs, proj_cpr(j), c0, c1, xr);
     }
-    return consume<FP8, EPI>(j, ring, it, xr, sa, part, abort, err, wait_ns, so, red, stage_tr, stage_tr_n) ? it
-                                                                                                             : -1;
+    return consume<FP8, EPI>(j, ring, it, xr, sa, part, abort, err, wait_ns, so, stage_tr, stage_tr_n) ? it : -1;
 }
 
 // Philox4x32-10 counter-based generator (Salmon, Moraes, Dror and Shaw,
@@ -818,13 +932,14 @@ __device__ __forceinline__ int sample_codebook(const float* row, int V, float T,
 // mask (codebook k is BOS-pad before frame k and EOC from frame eoc + k on;
 // "Higgs Audio v3 TTS-4B on FlashRT", section 4 sampling policy and section 5),
 // records the codes (next step's input and the history ring) and advances the
-// position and frame.  Consumers only.
+// position and frame.  `counter` holds `base` before the first arrival and is
+// put back to it.  Consumers only.
 __device__ __forceinline__ void head_tail(const float* logits, int n_cb, int V, DevState* st, unsigned* counter,
-                                          int* hist, int hist_cap, int* s_last, int* s_codes) {
+                                          unsigned base, int* hist, int hist_cap, int* s_last, int* s_codes) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __threadfence();
     consumer_sync();
-    if (threadIdx.x == 0) *s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
+    if (threadIdx.x == 0) *s_last = (atomicAdd(counter, 1u) - base == gridDim.x - 1);
     consumer_sync();
     if (!*s_last) return;
     __threadfence();
@@ -867,7 +982,7 @@ __device__ __forceinline__ void head_tail(const float* logits, int n_cb, int V, 
         st->hist_idx += 1;
         st->t = t + 1;
         st->pos += 1;
-        *counter = 0u;
+        *counter = base;
     }
 }
 

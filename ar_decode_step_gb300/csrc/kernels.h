@@ -183,11 +183,10 @@ struct StepParams {
     int decode;         // 1: head + argmax + advance; 0: prefill position advance
     float *h, *qkv, *attn, *act, *logits;
     float *part_o, *part_ml;                  // attention split partials
-    unsigned *att_counter, *head_counter;     // last-arriver tickets
-    unsigned* gbar;                           // grid-barrier arrivals, zero at launch
-    float2* h_stats;                          // [grid]: per CTA {sum h^2, max |h * gamma_next|}
-    float* attn_mx;                           // [n_kv]: max |attn| of each kv head's outputs (FP8)
-    float* act_mx;                            // [grid]: per CTA max |act| (FP8)
+    // the vectors the phases hand to each other, one buffer per layer and
+    // kind, and the last-arriver tickets, every word 0xffffffff at launch
+    // (the data exchange in gemv_core.cuh; layout: step_xch_words)
+    float* xch;
     int* hist;
     int hist_cap;
     int hidden, n_q, n_kv, inter, n_cb, cb_vocab, max_pos;
@@ -196,6 +195,7 @@ struct StepParams {
     int rs[5];   // rows per ring stage: QKV, O, gate/up, down, head
     int wpr[5];  // column segments (warps) per row, same order
     int ns, slot_bytes, xs_bytes, part_bytes;
+    int xf_off;  // FP8: byte offset in the activation scratch of the fp32 copy of a plain input
     int pf_stages;  // how many stages the L2 prefetch runs ahead of the ring copies
     int pf_max;     // ... and how far it may run ahead while the ring is full
     // FP8: static activation scales [n_layers][4] (QKV, O, gate/up, down
@@ -215,19 +215,34 @@ struct StepParams {
     // optional (traced launches): the residual stream after the embedding and
     // after every layer, [n_layers + 1][hidden] fp32
     float* hsnap;
-    // bound on each grid-barrier wait in ns (0: kWaitLimitNs), and a count
-    // added to every grid barrier's arrival target (0 on the product path; a
-    // test hook sets 1 so that the first barrier cannot complete and the
-    // bounded wait runs out)
+    // bound on each wait for exchanged data in ns (0: kWaitLimitNs), and a
+    // test hook: non-zero makes the embedding store nothing, so the first
+    // layer's wait for it cannot complete and runs out (0 on the product path)
     unsigned long long wait_limit_ns;
-    unsigned bar_target_extra;
+    int fault_skip_embed;
 };
+
+// Layout of StepParams::xch in 4-byte words: [0, hidden) h after the
+// embedding; then per layer l, from hidden + l * step_xch_layer_words: qkv
+// [qkv_rows], attention output [attn_dim], h after the attention [hidden],
+// MLP activation [inter], h after the MLP [hidden]; then the counters
+// (unsigned): last-arriver tickets of the attention [n_layers][n_kv] and of
+// the head [1], then the arrival counters of the vectors: the embedding [1],
+// then per layer the five vectors in the order above [n_layers][5].
+__host__ __device__ inline size_t step_xch_layer_words(int hidden, int qkv_rows, int attn_dim, int inter) {
+    return (size_t)qkv_rows + attn_dim + 2 * (size_t)hidden + inter;
+}
+inline size_t step_xch_words(int n_layers, int hidden, int qkv_rows, int attn_dim, int inter, int n_kv) {
+    return (size_t)hidden + (size_t)n_layers * step_xch_layer_words(hidden, qkv_rows, attn_dim, inter) +
+           (size_t)n_layers * n_kv + 1 + 1 + 5 * (size_t)n_layers;
+}
 
 // Phase-trace layout of the persistent kernel, per CTA (see step.cu):
 //   [0] consumer start; [1 + 14 l + k] layer l, event k (after: 0 QKV norm,
-//   1 QKV reduce, 2 barrier, 3 attention, 4 barrier, 5 O stage, 6 O reduce,
-//   7 barrier, 8 gate/up norm, 9 gate/up reduce, 10 barrier, 11 down stage,
-//   12 down reduce, 13 barrier); [1 + 14 L + 0..2] head norm, reduce, tail;
+//   1 QKV reduce, 3 attention, 5 O stage, 6 O reduce, 8 gate/up norm, 9
+//   gate/up reduce, 11 down stage, 12 down reduce; 2, 4, 7, 10 and 13 repeat
+//   the event before them: each staging includes its wait for the exchanged
+//   input); [1 + 14 L + 0..2] head norm, reduce, tail;
 //   [4 + 14 L + 5 l + k] producer: last copy of layer l's projection k issued
 //   (k = 4: head), [4 + 19 L + 1] producer done; [8 + 19 L + 4 l + k] ns the
 //   consumers waited for ring data in layer l's projection k; [8 + 23 L +

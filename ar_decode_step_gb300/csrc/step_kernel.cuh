@@ -7,22 +7,29 @@
 // waiting on anything but free ring slots.  The eight consumer warps walk
 // the phases of the step ("Higgs Audio v3 TTS-4B on FlashRT", section 5):
 //
-//   embed:   h = sum_k E_k[c_k] (this CTA's slice)               -> grid barrier
+//   embed:   h = sum_k E_k[c_k] (this CTA's slice)
 //   per layer l:
-//     QKV:   x = RMSNorm(h) (+FP8 quant); qkv rows                 -> grid barrier
+//     QKV:   x = RMSNorm(h) (+FP8 quant); qkv rows
 //     attn:  per (kv head, split) unit: q/k RMSNorm + RoPE, bf16 KV write,
-//            online-softmax attention over the split, last unit merges -> barrier
-//     O:     x = attn (+quant); h += W_o x                         -> grid barrier
-//     GU:    x = RMSNorm(h) (+quant); act = silu(gate) * up        -> grid barrier
-//     down:  x = act (+quant); h += W_d x                          -> grid barrier
+//            online-softmax attention over the split, last unit merges
+//     O:     x = attn (+quant); h += W_o x
+//     GU:    x = RMSNorm(h) (+quant); act = silu(gate) * up
+//     down:  x = act (+quant); h += W_d x
 //   head:    x = RMSNorm(h); logits; last CTA: greedy argmax under the delay
 //            mask, codes, position and frame advance (prefill: advance only)
 //
-// A grid barrier only stops the consumers: the producer keeps the ring full
-// with the next phase's weights, so HBM streams through barriers, norms and
-// attention.  Barrier waits are bounded (kWaitLimitNs) and stop early once any
-// CTA has recorded an error; on expiry the kernel records kErrTimeout, lets
-// its in-flight copies land and returns.
+// There is no grid barrier: every vector a phase hands on (h, qkv, the
+// attention output, the MLP activation) is stored into an exchange buffer of
+// its own (one per layer and kind, all 0xffffffff at launch), each producing
+// CTA then bumps the vector's arrival counter without a fence, and the next
+// phase starts reading once the counter is complete, re-reading any element
+// still unset (the data exchange in gemv_core.cuh).  No CTA waits for a
+// fence or for the CTAs that do not feed it.  The producer never waits for the
+// consumers of other CTAs: it
+// keeps its ring full with the next phase's weights, so HBM streams through
+// norms, attention and the waits.  Every wait is bounded (kWaitLimitNs) and
+// stops early once any CTA has recorded a timeout; then the kernel records
+// kErrTimeout, lets its in-flight copies land and returns.
 #pragma once
 
 #include "gemv_core.cuh"
@@ -36,35 +43,33 @@ using namespace core;
 constexpr int kMaxHRows = 256;     // rows of h one CTA owns, at most
 constexpr int kAttnMinChunk = 64;   // positions per attention split, at least (no merge below)
 
-// Grid barrier among the consumer warps of all CTAs.  `gbar` counts arrivals
-// over the launch (zeroed before it); barrier k (1-based) waits for
-// k * gridDim.x.  Returns false if the wait ran out (after limit_ns) or
-// another CTA failed.
-__device__ __forceinline__ bool grid_barrier(unsigned* gbar, unsigned target, DevState* st, volatile int* abort,
-                                             uint64_t limit_ns) {
-    consumer_sync();  // every consumer thread's writes of this phase precede the release below
-    if (threadIdx.x == 0) {
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gbar) : "memory");
-        uint64_t t0 = 0;
-        unsigned spins = 0;
-        while (ld_acquire_u32(gbar) < target) {
-            if ((++spins & 63) == 0) {
-                if (*reinterpret_cast<volatile int*>(&st->err) & kErrTimeout) {
-                    *abort = 1;
-                    break;
-                }
-                const uint64_t t = globaltimer_ns();
-                if (!t0) t0 = t;
-                else if (t - t0 > limit_ns) {
-                    atomicOr(&st->err, kErrTimeout);
-                    *abort = 1;
-                    break;
-                }
-            }
-        }
+// The exchange buffers of StepParams::xch (layout: step_xch_words).
+enum XchKind { kXQkv = 0, kXAttn, kXHo, kXAct, kXHd };  // qkv, attention output, h after attention / MLP, act
+
+// Vector `kind` of layer l; l = -1: h after the embedding (any kind).
+__device__ __forceinline__ float* xch_vec(const StepParams& p, int l, int kind) {
+    if (l < 0) return p.xch;
+    const int QKVR = (p.n_q + 2 * p.n_kv) * kHeadDim, A = p.n_q * kHeadDim;
+    float* b = p.xch + p.hidden + (size_t)l * step_xch_layer_words(p.hidden, QKVR, A, p.inter);
+    switch (kind) {
+        case kXQkv: return b;
+        case kXAttn: return b + QKVR;
+        case kXHo: return b + QKVR + A;
+        case kXAct: return b + QKVR + A + p.hidden;
+        default: return b + QKVR + A + p.hidden + p.inter;
     }
-    consumer_sync();  // the acquire above precedes every consumer thread's reads of the next phase
-    return !*abort;
+}
+// The last-arriver tickets: attention of (layer l, kv head g) at l * n_kv + g,
+// the head at n_layers * n_kv.  Each starts the launch at kUnset.
+__device__ __forceinline__ unsigned* xch_tickets(const StepParams& p) {
+    return reinterpret_cast<unsigned*>(xch_vec(p, p.n_layers, kXQkv));
+}
+// The arrival counter of vector `kind` of layer l (l = -1: the embedding).
+__device__ __forceinline__ unsigned* xch_counter(const StepParams& p, int l, int kind) {
+    return xch_tickets(p) + p.n_layers * p.n_kv + 1 + (l < 0 ? 0 : 1 + 5 * l + kind);
+}
+__device__ __forceinline__ Poll step_poll(const StepParams& p, volatile int* abort) {
+    return Poll{&p.st->err, abort, p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs};
 }
 
 constexpr int kAttnStep = 8;  // positions a warp scores at once
@@ -99,11 +104,17 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[kAttnStep]) {
 }
 
 // One (kv head g, split) unit of the decode attention of one layer, run by the
-// consumer warps of this CTA (no waits inside).
-template <int G, bool FP8, bool TRACE>
-__device__ __forceinline__ void attention_unit(const StepParams& p, const StepLayer& L, int layer, int pos, int g,
+// consumer warps of this CTA.  The cached K and V rows of the unit's positions
+// are read from global memory, a step ahead of their use (an L2 prefetch of
+// them measured slower: it competes with the weight stream).  The new
+// position's row comes from the QKV output: the
+// unit waits for its q/k/v rows in the exchange buffer (a failed wait sets the
+// abort flag; the unit then writes no cache row).  Returns false (every
+// consumer thread alike) if a wait ran out or the launch is aborting.
+template <int G, bool TRACE>
+__device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLayer& L, int layer, int pos, int g,
                                                int split, int nsplit, int chunk, unsigned char* scratch, int* s_last,
-                                               float* red) {
+                                               const Poll& w) {
     auto mark = [&](int k) {  // traced launches: the unit's progress
         if constexpr (TRACE)
             if (threadIdx.x == 0)
@@ -119,11 +130,15 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     const size_t cache_off = ((size_t)layer * p.n_kv + g) * p.max_pos * kHeadDim;
     __nv_bfloat16* kc = p.kc + cache_off;
     __nv_bfloat16* vc = p.vc + cache_off;
+    const float* qkv = xch_vec(p, layer, kXQkv);
+    float* out = xch_vec(p, layer, kXAttn);
 
     // q/k RMSNorm over head_dim then rotate-half RoPE: lane l holds dims
-    // 4l..4l+3; its rotation partner dims (+-64) sit in lane l^16.
+    // 4l..4l+3; its rotation partner dims (+-64) sit in lane l^16.  Returns
+    // whether the lane's row elements arrived.
     auto norm_rope = [&](const float* src, const __nv_bfloat16* gamma, float* dst, float post) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src) + lane);
+        const float4 v = poll4(reinterpret_cast<const float4*>(src) + lane, w);
+        const bool ok = !unset4(v);
         const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
         const float r = 1.0f / sqrtf(ss / (float)kHeadDim + p.eps);
         const uint2 gb = *reinterpret_cast<const uint2*>(gamma + 4 * lane);
@@ -135,6 +150,7 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
             const float2 cs = rope[(4 * lane + jj) & 63];
             dst[4 * lane + jj] = (lane < 16 ? a[jj] * cs.x - partner * cs.y : a[jj] * cs.x + partner * cs.y) * post;
         }
+        return ok;
     };
     // The cached rows do not depend on this step: issue the loads of the
     // warp's first positions before the q/k loads (one memory round trip).
@@ -164,18 +180,23 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
     };
     load_k(t0 + kAttnStep * warp);
     load_v(t0 + kAttnStep * warp);
-    if (warp < G) norm_rope(p.qkv + (size_t)(g * G + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
+    if (warp < G) norm_rope(qkv + (size_t)(g * G + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
     if (has_new && warp == G) {
-        norm_rope(p.qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
+        const bool okk = norm_rope(qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
+        const float4 v4 = poll4(reinterpret_cast<const float4*>(qkv + (size_t)(p.n_q + p.n_kv + g) * kHeadDim) + lane, w);
+        const bool okv = !unset4(v4);
+        const bool store = __all_sync(0xffffffffu, okk && okv);  // a row that never arrived is not cached
         __syncwarp();
-        const float* vsrc = p.qkv + (size_t)(p.n_q + p.n_kv + g) * kHeadDim;
+        const float vf[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int d = 4 * lane + jj;
             const __nv_bfloat16 kb = __float2bfloat16_rn(sm.knew[d]);
-            const __nv_bfloat16 vb = __float2bfloat16_rn(__ldcg(vsrc + d));
-            kc[(size_t)pos * kHeadDim + d] = kb;
-            vc[(size_t)pos * kHeadDim + d] = vb;
+            const __nv_bfloat16 vb = __float2bfloat16_rn(vf[jj]);
+            if (store) {
+                kc[(size_t)pos * kHeadDim + d] = kb;
+                vc[(size_t)pos * kHeadDim + d] = vb;
+            }
             sm.knew[d] = __bfloat162float(kb);
             sm.vnew[d] = __bfloat162float(vb);
         }
@@ -259,46 +280,41 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
 #pragma unroll
         for (int i = 0; i < 4; ++i) sm.wo[warp][jj][4 * lane + i] = o[jj][i];
     }
-    consumer_sync();
+    if (consumer_sync_or(*w.abort)) return false;
 
     // merge the warps; a single split writes the output directly
-    float mx = 0.f;  // max |output| (FP8 scale of the O-proj input)
     float* po = p.part_o + (((size_t)g * p.S + split) * G) * kHeadDim;
     float* pml = p.part_ml + (((size_t)g * p.S + split) * G) * 2;
     for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kConsumers) {
         const int jj = idx / kHeadDim, d = idx % kHeadDim;
         float M = -INFINITY;
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.wm[w][jj]);
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, sm.wm[w2][jj]);
         float Ls = 0.f, O = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float c = sm.wm[w][jj] == -INFINITY ? 0.f : __expf(sm.wm[w][jj] - M);
-            Ls += sm.wl[w][jj] * c;
-            O += sm.wo[w][jj][d] * c;
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+            const float c = sm.wm[w2][jj] == -INFINITY ? 0.f : __expf(sm.wm[w2][jj] - M);
+            Ls += sm.wl[w2][jj] * c;
+            O += sm.wo[w2][jj][d] * c;
         }
         if (nsplit == 1) {
-            const float a = O / Ls;
-            p.attn[(size_t)(g * G + jj) * kHeadDim + d] = a;
-            mx = fmaxf(mx, fabsf(a));
+            st_relaxed(out + (size_t)(g * G + jj) * kHeadDim + d, O / Ls);
         } else {
             po[idx] = O;
             if (d == 0) { pml[2 * jj] = M; pml[2 * jj + 1] = Ls; }
         }
     }
     if (nsplit == 1) {
-        if constexpr (FP8) {
-            mx = consumer_max(mx, red);
-            if (threadIdx.x == 0) p.attn_mx[g] = mx;
-        }
         consumer_sync();
         mark(2);
         mark(3);
-        return;
+        return true;
     }
     mark(2);
-    // the last split of this kv head merges all splits
+    // the last split of this kv head merges all splits (the ticket starts at
+    // kUnset: arrival k, from 0, reads kUnset + k)
     __threadfence();
     consumer_sync();
-    if (threadIdx.x == 0) *s_last = atomicAdd(&p.att_counter[g], 1u) == (unsigned)(nsplit - 1);
+    if (threadIdx.x == 0)
+        *s_last = atomicAdd(xch_tickets(p) + layer * p.n_kv + g, 1u) + 1u == (unsigned)(nsplit - 1);
     consumer_sync();
     if (*s_last) {
         __threadfence();
@@ -356,19 +372,13 @@ __device__ __forceinline__ void attention_unit(const StepParams& p, const StepLa
             const int idx = threadIdx.x + kConsumers * e;
             if (idx < G * kHeadDim) {
                 const int jj = idx / kHeadDim, d = idx % kHeadDim;
-                const float a = acc[e] / lsum[jj];
-                p.attn[(size_t)(g * G + jj) * kHeadDim + d] = a;
-                mx = fmaxf(mx, fabsf(a));
+                st_relaxed(out + (size_t)(g * G + jj) * kHeadDim + d, acc[e] / lsum[jj]);
             }
         }
-        if constexpr (FP8) {
-            mx = consumer_max(mx, red);
-            if (threadIdx.x == 0) p.attn_mx[g] = mx;
-        }
-        if (threadIdx.x == 0) p.att_counter[g] = 0u;
     }
     consumer_sync();
     mark(3);
+    return true;
 }
 
 // Per-CTA constants of one launch, worked out once at kernel start and kept
@@ -438,11 +448,13 @@ __device__ __forceinline__ void trace_mark(const StepParams& p, int ev) {
         if (threadIdx.x == 0) p.trace[(size_t)blockIdx.x * p.trace_stride + ev] = globaltimer_ns();
 }
 
-// One projection phase of the consumers: stage the activation vector (with
-// the norm / quantisation its kind needs), reduce this CTA's stages from the
-// ring, apply the epilogue.  Not inlined: its registers are allocated on their
-// own, free of the state the step keeps across phases.  Returns the advanced
-// stage counter, or -1 if a wait ran out.
+// One projection phase of the consumers: stage the activation vector from its
+// exchange buffer (waiting for it, with the norm / quantisation its kind
+// needs), reduce this CTA's stages from the ring, apply the epilogue (storing
+// the outputs into their exchange buffer).  Not inlined: its registers are
+// allocated on their own, free of the state the step keeps across phases.
+// Returns the advanced stage counter, or -1 if a wait ran out or the launch is
+// aborting (every consumer thread alike).
 template <bool FP8_, int KIND, bool TRACE>
 __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l, int it,
                                        float* red, volatile int* abort, float* s_hrows) {
@@ -454,37 +466,29 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
     // FP8 activation site of this projection: static scale and calibration
     const float* site_sa = FP8 && p.fp8_sa ? p.fp8_sa + 4 * l + KIND : nullptr;
     float* site_cal = FP8 && p.fp8_calib ? p.fp8_calib + 4 * l + KIND : nullptr;
-    float sa;
+    const Poll w = step_poll(p, abort);
+    // this projection's input: h after the previous layer (the embedding for
+    // layer 0), the attention output, h after the attention, the MLP
+    // activation, h after the last layer
+    const int xl = KIND == 0 ? l - 1 : KIND == 4 ? p.n_layers - 1 : l;
+    const int xk = KIND == 1 ? kXAttn : KIND == 2 ? kXHo : KIND == 3 ? kXAct : kXHd;
+    const float* x = xch_vec(p, xl, xk);
+    float sa = 1.0f;
+    // every CTA produces a slice of every exchanged vector
+    if (!xch_wait(xch_counter(p, xl, xk), gridDim.x, w)) return -1;
     if constexpr (KIND == 0) {
-        // warm L2 with the cache rows this CTA's attention unit of this layer will read
-        if (threadIdx.x == 0 && (int)blockIdx.x < cs.nunits) {
-            const int g = blockIdx.x / cs.nsplit, sp = blockIdx.x % cs.nsplit;
-            const int a0 = sp * cs.chunk, a1 = min(cs.pos, a0 + cs.chunk);  // rows before pos are cached
-            if (a1 > a0) {
-                const size_t off = (((size_t)l * p.n_kv + g) * p.max_pos + a0) * kHeadDim;
-                prefetch_l2_bulk(p.kc + off, (uint32_t)((a1 - a0) * kHeadDim * 2));
-                prefetch_l2_bulk(p.vc + off, (uint32_t)((a1 - a0) * kHeadDim * 2));
-            }
-        }
-        sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_in, p.hidden, p.eps,
-                                      XStats{p.h_stats, nullptr, (int)gridDim.x, site_sa, site_cal}, m.xs);
-    } else if constexpr (KIND == 1) {
-        // bf16: the attention output goes straight from L2 into the lanes' registers
-        sa = FP8 ? stage_x_stats<FP8, false>(p.attn, nullptr, A, p.eps,
-                                             XStats{nullptr, p.attn_mx, p.n_kv, site_sa, site_cal}, m.xs)
-                 : 1.0f;
+        sa = stage_x_xch<FP8, true>(x, m.sl[l].ln_in, p.hidden, p.eps, site_sa, site_cal, m.xs, nullptr, red, w);
     } else if constexpr (KIND == 2) {
-        sa = stage_x_stats<FP8, true>(p.h, m.sl[l].ln_post, p.hidden, p.eps,
-                                      XStats{p.h_stats, nullptr, (int)gridDim.x, site_sa, site_cal}, m.xs);
-    } else if constexpr (KIND == 3) {
-        // bf16: the MLP activation goes straight from L2 into the lanes' registers
-        sa = FP8 ? stage_x_stats<FP8, false>(p.act, nullptr, p.inter, p.eps,
-                                             XStats{nullptr, p.act_mx, (int)gridDim.x, site_sa, site_cal}, m.xs)
-                 : 1.0f;
-    } else {
-        sa = stage_x_stats<false, true>(p.h, p.final_norm, p.hidden, p.eps, XStats{p.h_stats, nullptr, (int)gridDim.x},
-                                        m.xs);
+        sa = stage_x_xch<FP8, true>(x, m.sl[l].ln_post, p.hidden, p.eps, site_sa, site_cal, m.xs, nullptr, red, w);
+    } else if constexpr (KIND == 4) {
+        sa = stage_x_xch<false, true>(x, p.final_norm, p.hidden, p.eps, nullptr, nullptr, m.xs, nullptr, red, w);
+    } else if constexpr (FP8) {
+        sa = stage_x_xch<true, false>(x, nullptr, KIND == 1 ? A : p.inter, p.eps, site_sa, site_cal, m.xs,
+                                      reinterpret_cast<float*>(m.xs + p.xf_off), red, w);
     }
+    // (bf16 O and down inputs are not staged: the stage loop's lanes load their
+    // segments of the exchanged vector straight into registers, waiting there)
+    if (sa < 0.f) return -1;
     if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers);
     else trace_mark<TRACE>(p, ev);
 
@@ -496,11 +500,10 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
     unsigned long long* str = TRACE ? cs.cstr : nullptr;
     const int str_n = TRACE ? cs.cstr_n : 0;
     if constexpr (KIND == 1 || KIND == 3) {
-        // residual add; publish h's statistics for the next RMSNorm (FP8: max |h * gamma_next|)
-        const __nv_bfloat16* gnext = KIND == 1 ? m.sl[l].ln_post : (l + 1 < p.n_layers ? m.sl[l + 1].ln_in : p.final_norm);
-        const StatsOut so{p.h_stats, FP8 ? gnext : nullptr, nullptr, s_hrows};
-        it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, red,
-                                          str, str_n, FP8 ? nullptr : (KIND == 1 ? p.attn : p.act));
+        // residual add on this CTA's rows of h (kept in shared memory)
+        const EpiOut so{s_hrows, xch_vec(p, l, KIND == 1 ? kXHo : kXHd)};
+        it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n,
+                                          FP8 ? nullptr : x, &w);
         if constexpr (TRACE && KIND == 3) {
             // layer-level checks: this CTA's rows of the residual stream after the layer
             if (p.hsnap && it >= 0)
@@ -508,27 +511,41 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
                     p.hsnap[(size_t)(l + 1) * p.hidden + j.r0 + r] = s_hrows[r];
         }
     } else if constexpr (KIND == 2) {
-        const StatsOut so{nullptr, nullptr, FP8 ? p.act_mx : nullptr, nullptr};
-        it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, red,
-                                           str, str_n);
+        const EpiOut so{nullptr, xch_vec(p, l, kXAct)};
+        it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n);
+    } else if constexpr (KIND == 0) {
+        const EpiOut so{nullptr, xch_vec(p, l, kXQkv)};
+        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n);
     } else {
-        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, nullptr,
-                                          nullptr, str, str_n);
+        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, nullptr, str,
+                                          str_n);
     }
     const bool ok = it >= 0;
+    if constexpr (KIND < 4)
+        if (ok) xch_publish(xch_counter(p, l, KIND == 0 ? kXQkv : KIND == 1 ? kXHo : KIND == 2 ? kXAct : kXHd));
     if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 1);
     else trace_mark<TRACE>(p, ev + 1);
     return ok ? it : -1;
 }
 
-// This CTA's attention unit of layer l (no-op for CTAs without one).  Not inlined.
-template <int G, bool FP8, bool TRACE>
-__device__ __noinline__ void attn_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l,
-                                        int* s_last, float* red) {
-    if ((int)blockIdx.x >= cs.nunits) return;
-    const StepSmem m = step_smem(smem, p);
-    attention_unit<G, FP8, TRACE>(p, m.sl[l], l, cs.pos, blockIdx.x / cs.nsplit, blockIdx.x % cs.nsplit, cs.nsplit,
-                                  cs.chunk, m.xs, s_last, red);
+// This CTA's attention unit of layer l (CTAs without one only announce that
+// they are done).  Not inlined.  Returns the advanced stage counter, or -1 if
+// a wait ran out or the launch is aborting (every consumer thread alike).
+template <int G, bool TRACE>
+__device__ __noinline__ int attn_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l, int it,
+                                       int* s_last, volatile int* abort) {
+    if ((int)blockIdx.x < cs.nunits) {
+        const Poll w = step_poll(p, abort);
+        if (!xch_wait(xch_counter(p, l, kXQkv), gridDim.x, w)) return -1;
+        const StepSmem m = step_smem(smem, p);
+        if (!attention_unit<G, TRACE>(p, m.sl[l], l, cs.pos, blockIdx.x / cs.nsplit, blockIdx.x % cs.nsplit,
+                                      cs.nsplit, cs.chunk, m.xs, s_last, w))
+            return -1;
+    }
+    // after its merge, if this unit merged: every CTA counts, so the count is
+    // complete only once every kv head's output is stored
+    xch_publish(xch_counter(p, l, kXAttn));
+    return it;
 }
 
 template <int PREC, int G, bool TRACE>
@@ -589,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
     // ---- warm L2 with every layer's small parameters ---------------------------
     // Norm gains, FP8 scales and this position's RoPE row are read on the
-    // consumers' critical path right after a barrier; a first touch would queue
+    // consumers' critical path right after a wait; a first touch would queue
     // behind the saturated weight stream.  The idle lanes of the producer warp
     // spread L2 prefetches of all of them over the CTAs at kernel start.
     if (warp == kConsumerWarps && lane > 0) {
@@ -665,15 +682,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
             int pq = 0, ps = 0, pidx = 0;
             Seg psg = seg_of(0);
             auto prefetch_upto = [&](int limit) {
+                // pidx counts real stages only (it is compared with the copy
+                // cursor): segments without stages are stepped over
                 while (pq < nkinds && pidx < limit) {
-                    if (psg.nst > 0) {
+                    if (ps < psg.nst) {
                         const uint32_t bytes = ps + 1 < psg.nst ? psg.stage_bytes : psg.last_bytes;
                         const size_t off = (size_t)ps * psg.stage_bytes;
                         prefetch_l2_bulk(psg.a + off, bytes);
                         if (psg.b) prefetch_l2_bulk(psg.b + off, bytes);
+                        ++pidx;
+                        ++ps;
                     }
-                    ++pidx;
-                    if (++ps >= psg.nst) {
+                    if (ps >= psg.nst) {
                         ps = 0;
                         if (++pq < nkinds) psg = seg_of(pq);
                     }
@@ -693,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                     prefetch_upto(it + p.pf_stages);
                     const uint64_t tw = pw ? globaltimer_ns() : 0;
                     // While the slot is still busy (the consumers are in a norm, a
-                    // barrier or attention) keep HBM streaming: run the L2 prefetch
+                    // wait or attention) keep HBM streaming: run the L2 prefetch
                     // further ahead, up to p.pf_max stages past the copy cursor.
                     bool got = mbar_try_wait(&ring.empty[slot], parity);
                     while (!got && pq < nkinds && pidx < it + p.pf_max) {
@@ -733,16 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     trace_mark<TRACE>(p, 0);
     if (pos < 0 || pos >= p.max_pos) {
         if (threadIdx.x == 0) {
-            atomicOr(&p.st->err, kErrPos | kErrTimeout);  // kErrTimeout stops the others' barriers early
+            atomicOr(&p.st->err, kErrPos | kErrTimeout);  // kErrTimeout stops the others' waits early
             s_abort = 1;
         }
         return;
     }
-    unsigned nbar = 0;
-    const uint64_t bar_limit = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
-    auto barrier = [&]() {
-        return grid_barrier(p.gbar, ++nbar * gridDim.x + p.bar_target_extra, p.st, &s_abort, bar_limit);
-    };
 
     // embed: this CTA's slice of h = sum_k E_k[c_k]
     {
@@ -757,49 +772,42 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         consumer_sync();
         const int i0 = (int)((long long)blockIdx.x * p.hidden / gridDim.x);
         const int i1 = (int)((long long)(blockIdx.x + 1) * p.hidden / gridDim.x);
-        float ss = 0.f, mxg = 0.f;
-        const __nv_bfloat16* g0 = m.sl[0].ln_in;
+        float* h0 = xch_vec(p, -1, kXHd);
         for (int i = i0 + threadIdx.x; i < i1; i += kConsumers) {
             float acc = 0.f;
             for (int k = 0; k < p.n_cb; ++k)
                 acc += __bfloat162float(p.embed[((size_t)k * p.cb_vocab + s_codes[k]) * p.hidden + i]);
             p.h[i] = acc;
             s_hrows[i - i0] = acc;
+            if (!p.fault_skip_embed) st_relaxed(h0 + i, acc);
             if constexpr (TRACE)
                 if (p.hsnap) p.hsnap[i] = acc;
-            ss += acc * acc;
-            mxg = fmaxf(mxg, fabsf(acc * __bfloat162float(g0[i])));
         }
-        ss = consumer_sum(ss, red);
-        mxg = consumer_max(mxg, red);
-        if (threadIdx.x == 0) p.h_stats[blockIdx.x] = make_float2(ss, mxg);
+        if (!p.fault_skip_embed) xch_publish(xch_counter(p, -1, 0));
     }
-    if (!barrier()) return;
 
-    // per layer: QKV | attention | O-proj | gate/up | down, a grid barrier after each
+    // per layer: QKV | attention | O-proj | gate/up | down, each phase waiting
+    // only for the exchanged elements it reads (no barrier between phases:
+    // trace events 2, 4, 7, 10 and 13 repeat the event before them)
     int it = 0;
     for (int l = 0; l < p.n_layers; ++l) {
         const int ev = 1 + 14 * l;
         if ((it = proj_phase<FP8, 0, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
-        if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 2);
-        attn_phase<G, FP8, TRACE>(s_p, s_cs, smem, l, &s_last, red);
+        if ((it = attn_phase<G, TRACE>(s_p, s_cs, smem, l, it, &s_last, &s_abort)) < 0) return;
         trace_mark<TRACE>(p, ev + 3);
-        if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 4);
         if ((it = proj_phase<FP8, 1, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
-        if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 7);
         if ((it = proj_phase<FP8, 2, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
-        if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 10);
         if ((it = proj_phase<FP8, 3, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
-        if (!barrier()) return;
         trace_mark<TRACE>(p, ev + 13);
     }
     if (p.decode) {
         if ((it = proj_phase<FP8, 4, TRACE>(s_p, s_cs, smem, 0, it, red, &s_abort, s_hrows)) < 0) return;
-        head_tail(p.logits, p.n_cb, p.cb_vocab, p.st, p.head_counter, p.hist, p.hist_cap, &s_last, s_codes);
+        head_tail(p.logits, p.n_cb, p.cb_vocab, p.st, xch_tickets(p) + p.n_layers * p.n_kv, kUnset, p.hist,
+                  p.hist_cap, &s_last, s_codes);
         trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 2);
     }
     if (!p.decode && blockIdx.x == 0 && threadIdx.x == 0) {

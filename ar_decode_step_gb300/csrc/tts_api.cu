@@ -73,7 +73,8 @@ struct tts_ctx {
     // persistent step kernel
     bool persistent = true;
     StepLayer* d_layers = nullptr;
-    unsigned* gbar = nullptr;
+    float* xch = nullptr;  // the persistent step's exchange buffers (StepParams::xch)
+    size_t xch_bytes = 0;
     StepParams sp{};
     int step_smem = 0;
 
@@ -211,11 +212,15 @@ constexpr size_t kGemvPrefetchAttnBytes = 160 * 1024;
 constexpr int kStepPrefetchStages = 4;
 constexpr int kStepPrefetchMax = 12;
 
-// Persistent form: zero the grid-barrier counter, then one cooperative launch.
+// Every exchange word of the persistent step back to 0xffffffff (the unset
+// sentinel, and the tickets' starting value): before every launch.
+cudaError_t xch_reset(tts_ctx* c, cudaStream_t s) { return cudaMemsetAsync(c->xch, 0xFF, c->xch_bytes, s); }
+
+// Persistent form: reset the exchange buffers, then one cooperative launch.
 int record_step_persistent(tts_ctx* c, cudaStream_t s, bool decode) {
     StepParams p = c->sp;
     p.decode = decode ? 1 : 0;
-    TTS_CK(cudaMemsetAsync(c->gbar, 0, sizeof(unsigned), s));
+    TTS_CK(xch_reset(c, s));
     const int prec = c->cfg.precision == TTS_FP8 ? kFP8 : kBF16;
     TTS_CK(launch_step(p, prec, c->G, c->num_sms, c->step_smem, s));
     return TTS_OK;
@@ -348,9 +353,12 @@ int setup_persistent(tts_ctx* c) {
     }
     // shared scratch: the staged activation vector, or the attention unit's state
     // bf16: plain inputs (attention output, MLP activation) are read into
-    // registers directly, only RMSNorm inputs are staged; FP8 stages all (quantised)
+    // registers directly, only RMSNorm inputs are staged (fp32, as is the
+    // head's input in both precisions); FP8 stages all as E4M3 bytes, plain
+    // inputs through an fp32 copy at xf_off
+    const int xf_off = round128i(std::max({H, A, I}));
     int xs = prec == kBF16 ? std::max(H * 4, step_attn_scratch_bytes(c->G))
-                           : std::max({H * 2, A * 2, I * 2, H * 4, step_attn_scratch_bytes(c->G)});
+                           : std::max({H * 4, xf_off + 4 * std::max(A, I), step_attn_scratch_bytes(c->G)});
     xs = round128i(xs);
     part = round128i(part);
     const int budget = 225 * 1024;
@@ -367,6 +375,7 @@ int setup_persistent(tts_ctx* c) {
     p.slot_bytes = slot;
     p.xs_bytes = xs;
     p.part_bytes = part;
+    p.xf_off = xf_off;
 
     std::vector<StepLayer> layers(k.n_layers);
     for (int l = 0; l < k.n_layers; ++l) {
@@ -375,10 +384,8 @@ int setup_persistent(tts_ctx* c) {
     }
     TTS_TRY(dalloc(c, &c->d_layers, (size_t)k.n_layers));
     TTS_CK(cudaMemcpy(c->d_layers, layers.data(), layers.size() * sizeof(StepLayer), cudaMemcpyHostToDevice));
-    TTS_TRY(dalloc(c, &c->gbar, 1));
-    TTS_TRY(dalloc(c, &p.h_stats, (size_t)grid));
-    TTS_TRY(dalloc(c, &p.attn_mx, (size_t)k.n_kv_heads));
-    TTS_TRY(dalloc(c, &p.act_mx, (size_t)grid));
+    c->xch_bytes = 4 * step_xch_words(k.n_layers, H, c->qkv_rows, A, I, k.n_kv_heads);
+    TTS_TRY(dalloc(c, &c->xch, c->xch_bytes / 4));
     p.fp8_sa = nullptr;
     p.fp8_calib = nullptr;
     if (prec == kFP8) {  // static activation scales, all dynamic until set
@@ -401,9 +408,7 @@ int setup_persistent(tts_ctx* c) {
     p.prompt = c->prompt;
     p.h = c->h; p.qkv = c->qkv; p.attn = c->attn; p.act = c->act; p.logits = c->logits;
     p.part_o = c->part_o; p.part_ml = c->part_ml;
-    p.att_counter = c->counters;
-    p.head_counter = c->counters + k.n_kv_heads;
-    p.gbar = c->gbar;
+    p.xch = c->xch;
     p.hist = c->hist;
     p.hist_cap = k.max_pos;
     p.hidden = H; p.n_q = k.n_q_heads; p.n_kv = k.n_kv_heads; p.inter = I;
@@ -922,7 +927,7 @@ int tts_fp8_calibrate(tts_ctx* ctx, int n_frames, float* amax_out) {
     p.decode = 1;
     p.fp8_calib = cal;
     for (int f = 0; f < n_frames && e == cudaSuccess; ++f) {
-        e = cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream);
+        e = xch_reset(ctx, ctx->stream);
         if (e == cudaSuccess) e = launch_step(p, kFP8, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream);
     }
     if (e == cudaSuccess) e = cudaMemcpyAsync(amax_out, cal, n * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream);
@@ -1065,7 +1070,7 @@ int tts_trace_step(tts_ctx* ctx, uint64_t* host_out, int capacity, int* stride, 
     p.stage_trace = d + n;
     p.stage_trace_stride = sstride;
     const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
-    cudaError_t e = cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream);
+    cudaError_t e = xch_reset(ctx, ctx->stream);
     if (e == cudaSuccess) e = launch_step(p, prec, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, d, ntot * sizeof(unsigned long long), cudaMemcpyDeviceToHost, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
@@ -1106,7 +1111,7 @@ int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes
     p.stage_trace_stride = 0;
     p.hsnap = hs;
     const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
-    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream);
+    if (e == cudaSuccess) e = xch_reset(ctx, ctx->stream);
     if (e == cudaSuccess) e = launch_step(p, prec, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync(host_h, hs, nh * sizeof(float), cudaMemcpyDeviceToHost, ctx->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
@@ -1158,9 +1163,9 @@ int tts_debug_expire_wait(tts_ctx* ctx) {
     StepParams p = ctx->sp;
     p.decode = 1;
     p.wait_limit_ns = 1000ull * 1000ull;  // 1 ms
-    p.bar_target_extra = 1;               // the first grid barrier waits for one arrival too many
+    p.fault_skip_embed = 1;               // the first layer waits for an embedding never stored
     const int prec = k.precision == TTS_FP8 ? kFP8 : kBF16;
-    TTS_CK(cudaMemsetAsync(ctx->gbar, 0, sizeof(unsigned), ctx->stream));
+    TTS_CK(xch_reset(ctx, ctx->stream));
     TTS_CK(launch_step(p, prec, ctx->G, ctx->num_sms, ctx->step_smem, ctx->stream));
     return pull_state(ctx);
 }

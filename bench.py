@@ -340,9 +340,9 @@ def time_frames(dec, ctx0: int, seg: int, warmup: int, steps: int, barrier=None)
 
 def roofline_line(d, precision: int, ctxs, ms_per_launch: float, wl_name: str, persistent: bool = True) -> dict:
     """Roofline of the dominant kernel: the step kernel, one launch per frame
-    (the timed region / frames; each frame also carries a 4-byte memset of the
-    grid-barrier counter and the graph-launch gap, both counted against the
-    kernel).  Algorithmic bytes per launch: the mean over the timed contexts."""
+    (the timed region / frames; each frame also carries the memset that
+    resets the kernel's exchange buffers and the graph-launch gap, both
+    counted against the kernel).  Algorithmic bytes per launch: the mean over the timed contexts."""
     mean_bytes = float(np.mean([step_bytes(d, precision, c) for c in ctxs]))
     peak, peak_kind = read_peaks()
     achieved = mean_bytes / (ms_per_launch * 1e-3) / 1e9

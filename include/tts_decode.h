@@ -301,12 +301,12 @@ int tts_debug_layer_states(tts_ctx* ctx, const int32_t* codes_in, int32_t* codes
 int tts_debug_prefill_states(tts_ctx* ctx, const int32_t* codes, int P, float* host_h, long long capacity);
 
 /* Test hook for failure detection (not part of the product path): one launch
- * of the persistent step kernel, outside the graph, whose first grid barrier
- * waits for one arrival more than the grid has and whose barrier waits give
- * up after 1 ms instead of 1 s.  The wait runs out, the kernel records the
- * timeout in the device error word, every CTA leaves at its next barrier or
- * ring wait, the copies in flight land, and the launch ends; no spin is left
- * running.  Returns TTS_ERR_DEVICE (the error word is cleared again);
+ * of the persistent step kernel, outside the graph, whose embedding phase
+ * stores nothing into its exchange buffer and whose waits give up after 1 ms
+ * instead of 1 s.  The first layer's wait for the embedding runs out, the
+ * kernel records the timeout in the device error word, every CTA leaves at
+ * its next wait, the copies in flight land, and the launch ends; no spin is
+ * left running.  Returns TTS_ERR_DEVICE (the error word is cleared again);
  * position, frame and cache are left as they were, so the next step runs
  * normally.  TTS_ERR_UNSUPPORTED when the step runs as separate kernels.
  * Synchronises the stream. */

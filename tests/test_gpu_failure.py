@@ -1,10 +1,10 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
-Every spin-wait of the step kernel (its grid barriers, the ring's mbarrier
-waits) gives up after a time limit, records the timeout in the device error
-word and winds the launch down.  tts_debug_expire_wait launches the step with
-a first grid barrier that cannot complete (one arrival short) and a 1 ms
-limit.  The host must see TTS_ERR_DEVICE, the context must stay usable with
+Every spin-wait of the step kernel (its waits for data other CTAs exchange,
+the ring's mbarrier waits) gives up after a time limit, records the timeout
+in the device error word and winds the launch down.  tts_debug_expire_wait
+launches the step with an embedding that is never stored, so the first
+layer's wait for it cannot complete, and a 1 ms limit.  The host must see TTS_ERR_DEVICE, the context must stay usable with
 its state unchanged, and the next steps -- also after tts_reset -- must meet
 the oracle's parity bar."""
 import numpy as np
