@@ -172,6 +172,21 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
+// x / d in fp32, rounded to nearest even, given rd = the correctly rounded
+// 1 / d: the quotient-correction step of Markstein's FMA division
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  q0 = RN(x rd) is
+// within an ulp of x / d, so the residual x - d q0 is exact in one FMA, and
+// RN(q0 + residual rd) is the correctly rounded quotient.  Used with one
+// divisor for many dividends (quantisation scales), where it replaces a full
+// division per element.  The quotients here stay far from overflow; one below
+// the normal range may differ in its last bit from a true division, which no
+// E4M3 code can show (their smallest magnitude is 2^-9).
+__device__ __forceinline__ float div_rn_by(float x, float d, float rd) {
+    const float q0 = x * rd;
+    return fmaf(fmaf(-q0, d, x), rd, q0);
+}
+
 // Round an fp32 value to bf16 (nearest even) and return it widened again.
 __device__ __forceinline__ float round_bf16(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));

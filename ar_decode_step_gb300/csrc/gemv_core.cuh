@@ -415,11 +415,12 @@ __device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* ga
         }
         amax = consumer_max(amax, red);
         sa = __fdiv_rn(fmaxf(amax, 1e-12f), 448.0f);
+        const float rsa = __frcp_rn(sa);
         uint32_t* xs4 = reinterpret_cast<uint32_t*>(xs);  // E4M3 bytes, in order
         for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
             const float4 v = load(i);
-            xs4[i] = e4m3_byte(__fdiv_rn(v.x, sa)) | (e4m3_byte(__fdiv_rn(v.y, sa)) << 8) |
-                     (e4m3_byte(__fdiv_rn(v.z, sa)) << 16) | (e4m3_byte(__fdiv_rn(v.w, sa)) << 24);
+            xs4[i] = e4m3_byte(div_rn_by(v.x, sa, rsa)) | (e4m3_byte(div_rn_by(v.y, sa, rsa)) << 8) |
+                     (e4m3_byte(div_rn_by(v.z, sa, rsa)) << 16) | (e4m3_byte(div_rn_by(v.w, sa, rsa)) << 24);
         }
     }
     consumer_sync();
@@ -558,6 +559,7 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
                 if (ss_ > 0.f) sa = ss_;  // static: values beyond 448 * sa saturate
             }
         }
+        const float rsa = __frcp_rn(sa);  // x / sa by div_rn_by: one division per CTA, not per element
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
             const int i = threadIdx.x + k * kConsumers;
@@ -567,8 +569,8 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
                     reinterpret_cast<float4*>(xs)[((e & 7) >> 2) * cpr + (e >> 3)] = v[k];
                 } else {
                     reinterpret_cast<uint32_t*>(xs)[i] =
-                        e4m3_byte(__fdiv_rn(v[k].x, sa)) | (e4m3_byte(__fdiv_rn(v[k].y, sa)) << 8) |
-                        (e4m3_byte(__fdiv_rn(v[k].z, sa)) << 16) | (e4m3_byte(__fdiv_rn(v[k].w, sa)) << 24);
+                        e4m3_byte(div_rn_by(v[k].x, sa, rsa)) | (e4m3_byte(div_rn_by(v[k].y, sa, rsa)) << 8) |
+                        (e4m3_byte(div_rn_by(v[k].z, sa, rsa)) << 16) | (e4m3_byte(div_rn_by(v[k].w, sa, rsa)) << 24);
                 }
             }
         }
@@ -593,11 +595,12 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
             const float ss_ = *sa_static;
             if (ss_ > 0.f) sa = ss_;
         }
+        const float rsa = __frcp_rn(sa);
         for (int i = threadIdx.x; i < n4; i += kConsumers) {
             const float4 v = reinterpret_cast<const float4*>(xf)[i];
             reinterpret_cast<uint32_t*>(xs)[i] =
-                e4m3_byte(__fdiv_rn(v.x, sa)) | (e4m3_byte(__fdiv_rn(v.y, sa)) << 8) |
-                (e4m3_byte(__fdiv_rn(v.z, sa)) << 16) | (e4m3_byte(__fdiv_rn(v.w, sa)) << 24);
+                e4m3_byte(div_rn_by(v.x, sa, rsa)) | (e4m3_byte(div_rn_by(v.y, sa, rsa)) << 8) |
+                (e4m3_byte(div_rn_by(v.z, sa, rsa)) << 16) | (e4m3_byte(div_rn_by(v.w, sa, rsa)) << 24);
         }
     }
     return consumer_sync_or(*w.abort) ? -1.0f : sa;

@@ -47,7 +47,8 @@ __global__ void advance_kernel(DevState* st) {
 }
 
 // s[n] = max_k |W[n][k]| / 448 (1 for a zero row); W8 = E4M3(W / s[n]) with
-// an IEEE fp32 division, nearest-even rounding, saturation.  One CTA per row.
+// the quotient rounded as an IEEE fp32 division (div_rn_by), nearest-even
+// rounding, saturation.  One CTA per row.
 __global__ void quantize_weight_kernel(const __nv_bfloat16* W, int K, uint8_t* W8, float* s) {
     __shared__ float red[32];
     const size_t row = blockIdx.x;
@@ -56,8 +57,9 @@ __global__ void quantize_weight_kernel(const __nv_bfloat16* W, int K, uint8_t* W
     for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(__bfloat162float(w[k])));
     amax = block_max(amax, red);
     const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float rsc = __frcp_rn(sc);
     for (int k = threadIdx.x; k < K; k += blockDim.x)
-        W8[row * K + k] = __nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(w[k]), sc), __NV_SATFINITE, __NV_E4M3);
+        W8[row * K + k] = __nv_cvt_float_to_fp8(div_rn_by(__bfloat162float(w[k]), sc, rsc), __NV_SATFINITE, __NV_E4M3);
     if (threadIdx.x == 0) s[row] = sc;
 }
 

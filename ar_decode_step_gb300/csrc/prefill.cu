@@ -163,9 +163,9 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_rows_kernel(const f
     for (int i = threadIdx.x; i < hidden; i += blockDim.x)
         am = fmaxf(am, fabsf(h[i] * r * __bfloat162float(gamma[i])));
     am = block_max(am, red);
-    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f), rsa = __frcp_rn(sa);
     for (int i = threadIdx.x; i < hidden; i += blockDim.x)
-        out[(size_t)p * hidden + i] = e4m3_sat(__fdiv_rn(h[i] * r * __bfloat162float(gamma[i]), sa));
+        out[(size_t)p * hidden + i] = e4m3_sat(div_rn_by(h[i] * r * __bfloat162float(gamma[i]), sa, rsa));
     if (threadIdx.x == 0) scale[p] = sa;
 }
 
@@ -181,8 +181,9 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(const T* X, uin
     float am = 0.f;
     for (int i = threadIdx.x; i < n; i += blockDim.x) am = fmaxf(am, fabsf(as_f32(x[i])));
     am = block_max(am, red);
-    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) out[(size_t)p * n + i] = e4m3_sat(__fdiv_rn(as_f32(x[i]), sa));
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f), rsa = __frcp_rn(sa);
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        out[(size_t)p * n + i] = e4m3_sat(div_rn_by(as_f32(x[i]), sa, rsa));
     if (threadIdx.x == 0) scale[p] = sa;
 }
 
@@ -198,12 +199,12 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* x, float (&v)[8]) {
     v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
     v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
 }
-__device__ __forceinline__ uint2 quant8(const float (&v)[8], float sa) {
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], float sa, float rsa) {
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        lo |= (uint32_t)e4m3_sat(__fdiv_rn(v[e], sa)) << (8 * e);
-        hi |= (uint32_t)e4m3_sat(__fdiv_rn(v[e + 4], sa)) << (8 * e);
+        lo |= (uint32_t)e4m3_sat(div_rn_by(v[e], sa, rsa)) << (8 * e);
+        hi |= (uint32_t)e4m3_sat(div_rn_by(v[e + 4], sa, rsa)) << (8 * e);
     }
     return make_uint2(lo, hi);
 }
@@ -243,11 +244,11 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_quant_rows_reg_kernel(con
         }
     }
     am = block_max(am, red);
-    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f), rsa = __frcp_rn(sa);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int j = threadIdx.x + i * kRowThreads;
-        if (j < n8) *reinterpret_cast<uint2*>(out + (size_t)p * hidden + 8 * j) = quant8(v[i], sa);
+        if (j < n8) *reinterpret_cast<uint2*>(out + (size_t)p * hidden + 8 * j) = quant8(v[i], sa, rsa);
     }
     if (threadIdx.x == 0) scale[p] = sa;
 }
@@ -269,11 +270,11 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_reg_kernel(const T* X,
         }
     }
     am = block_max(am, red);
-    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
+    const float sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f), rsa = __frcp_rn(sa);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int j = threadIdx.x + i * kRowThreads;
-        if (j < n8) *reinterpret_cast<uint2*>(out + (size_t)p * n + 8 * j) = quant8(v[i], sa);
+        if (j < n8) *reinterpret_cast<uint2*>(out + (size_t)p * n + 8 * j) = quant8(v[i], sa, rsa);
     }
     if (threadIdx.x == 0) scale[p] = sa;
 }
