@@ -940,12 +940,14 @@ __device__ __forceinline__ int sample_codebook(const float* row, int V, float T,
 __device__ __forceinline__ void head_tail(const float* logits, int n_cb, int V, DevState* st, unsigned* counter,
                                           unsigned base, int* hist, int hist_cap, int* s_last, int* s_codes) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __threadfence();
-    consumer_sync();
-    if (threadIdx.x == 0) *s_last = (atomicAdd(counter, 1u) - base == gridDim.x - 1);
+    consumer_sync();  // every thread's logits stores precede thread 0's release below
+    if (threadIdx.x == 0) {
+        unsigned old;  // acquire-release: the last CTA then sees every CTA's logits
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+        *s_last = old - base == gridDim.x - 1;
+    }
     consumer_sync();
     if (!*s_last) return;
-    __threadfence();
     const int t = st->t, eoc = st->eoc;
     const float T = st->temperature;
     for (int k = warp; k < n_cb; k += kConsumerWarps) {
