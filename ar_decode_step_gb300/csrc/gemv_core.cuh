@@ -264,6 +264,13 @@ __device__ __forceinline__ unsigned char* opaque_ptr(unsigned char* v) {
     return v;
 }
 
+// log2 of a power of two.  The stage geometry's row counts (rs, and so the
+// output rows per stage) and segments per row (wpr) are powers of two, so
+// the per-phase set-up divides by shifting: a run-time integer division
+// costs tens of instructions (64-bit ones a subroutine call), paid by every
+// consumer thread at the start of every phase.
+__device__ __forceinline__ int ilog2(int x) { return 31 - __clz(x); }
+
 __device__ __forceinline__ int proj_cpr(const Proj& j) { return j.K / (j.fp8 ? 16 : 8); }
 __device__ __forceinline__ int proj_opst(const Proj& j) { return j.swiglu ? j.rs / 2 : j.rs; }
 __device__ __forceinline__ void proj_rows(const Proj& j, int& r0, int& r1) {
@@ -274,7 +281,7 @@ __device__ __forceinline__ int proj_stages(const Proj& j) {
     int r0, r1;
     proj_rows(j, r0, r1);
     const int opst = proj_opst(j);
-    return (r1 - r0 + opst - 1) / opst;
+    return (r1 - r0 + opst - 1) >> ilog2(opst);
 }
 
 // Ring of shared-memory stages; `it` counts stages since the ring was set up
@@ -338,7 +345,7 @@ __device__ __forceinline__ bool produce(const Proj& j, const Ring& ring, int& it
     proj_rows(j, r0, r1);
     const size_t rowb = (size_t)proj_cpr(j) * 16;
     const int opst = proj_opst(j);
-    const int nst = (r1 - r0 + opst - 1) / opst;
+    const int nst = (r1 - r0 + opst - 1) >> ilog2(opst);
     for (int s = 0; s < nst; ++s, ++it) {
         const int slot = it % ring.ns;
         if (!mbar_wait_or_abort(&ring.empty[slot], ((it / ring.ns) & 1) ^ 1, abort)) {
@@ -445,11 +452,11 @@ struct XSeg<true> {
 
 // This warp's segment of projection j.
 __device__ __forceinline__ void proj_segment(const Proj& j, int warp, int& rslot, int& sg, int& c0, int& c1) {
-    const int CPR = proj_cpr(j), WPR = j.wpr;
-    rslot = warp / WPR;
-    sg = warp % WPR;
-    c0 = (int)((long long)sg * CPR / WPR);
-    c1 = (int)((long long)(sg + 1) * CPR / WPR);
+    const int CPR = proj_cpr(j), lw = ilog2(j.wpr);
+    rslot = warp >> lw;
+    sg = warp & (j.wpr - 1);
+    c0 = (sg * CPR) >> lw;
+    c1 = ((sg + 1) * CPR) >> lw;
 }
 
 // Segment from the shared memory written by stage_x: fp32 planes for bf16
@@ -633,9 +640,10 @@ struct Fp8Lane {
 };
 __device__ __forceinline__ Fp8Lane fp8_lane(int cpr, size_t rowb, int rs, int opst, int wpr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    const int P = kFp8MmaRows / rs, gpr = 8 / P;  // subranges per row, lane groups per subrange
-    const int kap = g / gpr, ra = g % gpr, rb = ra + rs / 2;
-    const int ls = cpr / P, units = ls / 4;       // chunks and 4-chunk units per subrange
+    const int lr = ilog2(rs);                         // rs = 2^lr, 2 <= rs <= kFp8MmaRows = 16
+    const int P = kFp8MmaRows >> lr, gpr = rs >> 1;   // subranges per row, lane groups per subrange
+    const int kap = g >> (lr - 1), ra = g & (gpr - 1), rb = ra + gpr;
+    const int ls = cpr >> (4 - lr), units = ls / 4;   // chunks and 4-chunk units per subrange
     const int u0 = warp * units / kConsumerWarps;
     const int c0 = kap * ls + 4 * u0 + q;         // this lane's first chunk
     Fp8Lane L;
@@ -718,10 +726,11 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
     int r0, r1;
     proj_rows(j, r0, r1);
     const int nrows = r1 - r0;
-    const int CPR = proj_cpr(j), RS = j.rs, WPR = j.wpr, SLOTS = kConsumerWarps / WPR, NP = RS / SLOTS;
+    const int CPR = proj_cpr(j), RS = j.rs, WPR = j.wpr, SLOTS = kConsumerWarps >> ilog2(WPR),
+              NP = RS >> ilog2(SLOTS);
     const size_t rowb = (size_t)CPR * 16;
-    const int opst = proj_opst(j);
-    const int nst = (nrows + opst - 1) / opst;
+    const int opst = proj_opst(j), lo = ilog2(opst);
+    const int nst = (nrows + opst - 1) >> lo;
     int rslot, sg, c0, c1;
     proj_segment(j, warp, rslot, sg, c0, c1);
     Fp8Lane fl{};
@@ -763,7 +772,7 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
         } else {
             for (int ps = 0; ps < NP; ++ps) {
                 const int r = ps * SLOTS + rslot;          // row of the stage
-                const int orow = j.swiglu ? r % opst : r;  // its output row within the stage
+                const int orow = r & (opst - 1);           // its output row within the stage (gate row for up)
                 if (s * opst + orow < nrows) {
                     const uint4* wrow = reinterpret_cast<const uint4*>(sbuf + r * rowb);
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -794,7 +803,7 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
     // per-row sums over segments (in segment order) and the epilogue
     for (int r = threadIdx.x; r < nrows; r += kConsumers) {
         const int n = r0 + r;
-        const int s = r / opst, jj = r % opst;
+        const int s = r >> lo, jj = r & (opst - 1);
         auto row_sum = [&](int rs_) {
             const float* pr = part + (s * RS + rs_) * WPR;
             float acc = 0.f;

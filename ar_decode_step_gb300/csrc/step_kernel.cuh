@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
                 Seg sg;
                 sg.a = j.W + (size_t)j.r0 * rowb;
                 sg.b = j.swiglu ? j.W + ((size_t)j.N + j.r0) * rowb : nullptr;
-                sg.nst = (nrows + opst - 1) / opst;
+                sg.nst = (nrows + opst - 1) >> ilog2(opst);
                 sg.stage_bytes = (uint32_t)opst * rowb;
                 sg.last_bytes = (uint32_t)(nrows - (sg.nst - 1) * opst) * rowb;
                 sg.b_off = (uint32_t)opst * rowb;

@@ -343,6 +343,7 @@ int setup_persistent(tts_ctx* c) {
         const KindShape& ks = kinds[i];
         const StageGeom g = stage_geom(ks.prec, ks.epi, ks.K);
         if (!g.ok) return TTS_ERR_ARG;  // segments must fit the lane registers
+        if ((g.rs & (g.rs - 1)) || (g.wpr & (g.wpr - 1))) return TTS_ERR_ARG;  // the kernels shift, not divide
         const int rowb = ks.K / (ks.prec == kBF16 ? 8 : 16) * 16;
         p.rs[i] = g.rs;
         p.wpr[i] = g.wpr;
