@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
            EPI == kEpiSwiglu ? 1 : 0, 0, 0};
     proj_split_rows(j);
     Ring ring{reinterpret_cast<uint64_t*>(smem), reinterpret_cast<uint64_t*>(smem) + p.nstages,
-              smem + kBarrierBytes + xbytes + p.part_bytes, (uint32_t)(p.rs * cpr * 16), p.nstages};
+              smem + kBarrierBytes + xbytes + p.part_bytes, (uint32_t)(p.rs * cpr * 16), p.nstages,
+              ring_magic(p.nstages)};
     unsigned char* xs = smem + kBarrierBytes;
     float* part = reinterpret_cast<float*>(xs + xbytes);
 

@@ -292,7 +292,19 @@ struct Ring {
     unsigned char* buf;
     uint32_t slot_bytes;
     int ns;
+    uint32_t ns_magic;  // ring_magic(ns)
 };
+
+// floor(2^32 / ns) + 1: it / ns = __umulhi(it, ring_magic(ns)) exactly for
+// every it < 2^32 / ns (the error term stays below 1 / ns), which saves the
+// consumers a run-time division at every phase start.
+__host__ __device__ inline uint32_t ring_magic(int ns) { return 0xffffffffu / (uint32_t)ns + 1u; }
+// Slot and phase parity of ring stage `it`.
+__device__ __forceinline__ void ring_pos(const Ring& r, int it, int& slot, uint32_t& phase) {
+    const uint32_t q = __umulhi((uint32_t)it, r.ns_magic);
+    slot = it - (int)q * r.ns;
+    phase = q & 1u;
+}
 
 __device__ __forceinline__ void ring_init(const Ring& r) {
     for (int s = 0; s < r.ns; ++s) {
@@ -311,9 +323,11 @@ __device__ __forceinline__ bool produce_stage(const Proj& j, int s, const Ring& 
     proj_rows(j, r0, r1);
     const size_t rowb = (size_t)proj_cpr(j) * 16;
     const int opst = proj_opst(j);
-    const int slot = it % ring.ns;
+    int slot;
+    uint32_t ph;
+    ring_pos(ring, it, slot, ph);
     const uint64_t tw = wait_ns ? globaltimer_ns() : 0;
-    const bool got = mbar_wait_or_abort(&ring.empty[slot], ((it / ring.ns) & 1) ^ 1, abort);
+    const bool got = mbar_wait_or_abort(&ring.empty[slot], ph ^ 1, abort);
     if (wait_ns) *wait_ns += globaltimer_ns() - tw;
     if (!got) {
         if (err) atomicOr(err, kErrTimeout);
@@ -347,8 +361,10 @@ __device__ __forceinline__ bool produce(const Proj& j, const Ring& ring, int& it
     const int opst = proj_opst(j);
     const int nst = (r1 - r0 + opst - 1) >> ilog2(opst);
     for (int s = 0; s < nst; ++s, ++it) {
-        const int slot = it % ring.ns;
-        if (!mbar_wait_or_abort(&ring.empty[slot], ((it / ring.ns) & 1) ^ 1, abort)) {
+        int slot;
+        uint32_t ph;
+        ring_pos(ring, it, slot, ph);
+        if (!mbar_wait_or_abort(&ring.empty[slot], ph ^ 1, abort)) {
             if (err) atomicOr(err, kErrTimeout);
             *abort = 1;
             return false;
@@ -371,7 +387,12 @@ __device__ __forceinline__ bool produce(const Proj& j, const Ring& ring, int& it
 
 // Producer after an abort: wait (bounded) for the copies still in flight.
 __device__ __forceinline__ void drain(const Ring& ring, int it) {
-    for (int i = it > ring.ns ? it - ring.ns : 0; i < it; ++i) mbar_wait(&ring.full[i % ring.ns], (i / ring.ns) & 1);
+    for (int i = it > ring.ns ? it - ring.ns : 0; i < it; ++i) {
+        int slot;
+        uint32_t ph;
+        ring_pos(ring, i, slot, ph);
+        mbar_wait(&ring.full[slot], ph);
+    }
 }
 
 // Stage the activation vector for a projection with inner dimension K:
@@ -747,8 +768,9 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
 
     bool ok = true;
     unsigned long long waited = 0;  // ns spent waiting for data (traced runs; stored once at the end)
-    int slot = it % ring.ns;        // ring slot and phase of stage `it`, advanced per stage
-    uint32_t phase = (it / ring.ns) & 1;
+    int slot;                       // ring slot and phase of stage `it`, advanced per stage
+    uint32_t phase;
+    ring_pos(ring, it, slot, phase);
     for (int s = 0; s < nst; ++s, ++it) {
         const bool timed = wait_ns && threadIdx.x == 0;  // traced runs: thread 0 times its data waits
         const uint64_t tw = timed ? globaltimer_ns() : 0;

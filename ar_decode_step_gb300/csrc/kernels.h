@@ -195,6 +195,7 @@ struct StepParams {
     int rs[5];   // rows per ring stage: QKV, O, gate/up, down, head
     int wpr[5];  // column segments (warps) per row, same order
     int ns, slot_bytes, xs_bytes, part_bytes;
+    unsigned ns_magic;  // floor(2^32 / ns) + 1 (ring_magic)
     int xf_off;  // FP8: byte offset in the activation scratch of the fp32 copy of a plain input
     int pf_stages;  // how many stages the L2 prefetch runs ahead of the ring copies
     int pf_max;     // ... and how far it may run ahead while the ring is full

@@ -394,6 +394,7 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
 // them in registers across the step.
 struct CtaState {
     int pos, nsplit, chunk, nunits;
+    int unit_g, unit_split;        // this CTA's attention unit (kv head, split), if blockIdx.x < nunits
     int rows[5][2];                // this CTA's output rows per projection kind
     unsigned long long* cwait;     // traced runs: consumer wait per projection (thread 0), else null
     unsigned long long* cstr;      // traced runs: this CTA's per-stage trace, else null
@@ -415,7 +416,7 @@ __device__ __forceinline__ StepSmem step_smem(unsigned char* smem, const StepPar
     m.xs = smem + kBarrierBytes + tbl_bytes;
     m.part = reinterpret_cast<float*>(m.xs + p.xs_bytes);
     m.ring = Ring{reinterpret_cast<uint64_t*>(smem), reinterpret_cast<uint64_t*>(smem) + p.ns,
-                  m.xs + p.xs_bytes + p.part_bytes, (uint32_t)p.slot_bytes, p.ns};
+                  m.xs + p.xs_bytes + p.part_bytes, (uint32_t)p.slot_bytes, p.ns, p.ns_magic};
     return m;
 }
 
@@ -546,7 +547,7 @@ __device__ __noinline__ int attn_phase(const StepParams& p, const CtaState& cs, 
         const Poll w = step_poll(p, abort);
         if (!xch_wait(xch_counter(p, l, kXQkv), gridDim.x, w)) return -1;
         const StepSmem m = step_smem(smem, p);
-        if (!attention_unit<G, TRACE>(p, m.sl[l], l, cs.pos, blockIdx.x / cs.nsplit, blockIdx.x % cs.nsplit,
+        if (!attention_unit<G, TRACE>(p, m.sl[l], l, cs.pos, cs.unit_g, cs.unit_split,
                                       cs.nsplit, cs.chunk, m.xs, s_last, w))
             return -1;
     }
@@ -605,6 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         s_cs.chunk = chunk;
         s_cs.nsplit = (len + chunk - 1) / chunk;
         s_cs.nunits = p.n_kv * s_cs.nsplit;
+        s_cs.unit_g = blockIdx.x / s_cs.nsplit;
+        s_cs.unit_split = blockIdx.x % s_cs.nsplit;
         s_cs.cwait = TRACE ? p.trace + (size_t)blockIdx.x * p.trace_stride + 8 + 19 * p.n_layers : nullptr;
         s_cs.cstr = (TRACE && p.stage_trace && blockIdx.x == 0) ? p.stage_trace : nullptr;
         s_cs.cstr_n = p.stage_trace_stride / 4;

@@ -373,6 +373,7 @@ int setup_persistent(tts_ctx* c) {
     if (ns < 2) return TTS_ERR_ARG;
     c->step_smem = 128 + tbl + xs + part + ns * slot;
     p.ns = ns;
+    p.ns_magic = 0xffffffffu / (unsigned)ns + 1u;
     p.slot_bytes = slot;
     p.xs_bytes = xs;
     p.part_bytes = part;
