@@ -112,6 +112,27 @@ __device__ __forceinline__ float consumer_sum(float v, float* red) {
     consumer_sync();
     return s;
 }
+// The sum of s and the max of m over the consumer threads, with one barrier:
+// red[0..15] must not be read any more from an earlier call, which holds when
+// calls are separated by at least one consumer barrier (as the stagings of
+// successive phases are).
+__device__ __forceinline__ void consumer_sum_max(float& s, float& m, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    s = warp_sum(s);
+    m = warp_max(m);
+    if (lane == 0) {
+        red[warp] = s;
+        red[kConsumerWarps + warp] = m;
+    }
+    consumer_sync();
+    s = red[0];
+    m = red[kConsumerWarps];
+#pragma unroll
+    for (int i = 1; i < kConsumerWarps; ++i) {  // fixed order: deterministic
+        s += red[i];
+        m = fmaxf(m, red[kConsumerWarps + i]);
+    }
+}
 __device__ __forceinline__ float consumer_max(float v, float* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v = warp_max(v);
@@ -557,28 +578,31 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
                 g[k] = *reinterpret_cast<const uint2*>(gamma + 4 * i);
             }
         }
-        float ss = 0.f;
+        // sum of squares and (FP8) max |h * gamma| in one reduction: the
+        // normalised amax is r * max |h * gamma| (r > 0)
+        float ss = 0.f, am = 0.f;
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
             const int i = threadIdx.x + k * kConsumers;
             if (i < n4) {
                 if (unset4(v[k])) v[k] = poll4_wait(x4 + i, w);
                 ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+                if constexpr (FP8)
+                    am = fmaxf(fmaxf(am, fmaxf(fabsf(v[k].x * bf16lo(g[k].x)), fabsf(v[k].y * bf16hi(g[k].x)))),
+                               fmaxf(fabsf(v[k].z * bf16lo(g[k].y)), fabsf(v[k].w * bf16hi(g[k].y))));
             }
         }
-        const float r = 1.0f / sqrtf(consumer_sum(ss, red) / (float)K + eps);
-        float am = 0.f;
+        consumer_sum_max(ss, am, red);
+        const float r = rsqrtf(ss * __frcp_rn((float)K) + eps);
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
             v[k].x *= r * bf16lo(g[k].x);
             v[k].y *= r * bf16hi(g[k].x);
             v[k].z *= r * bf16lo(g[k].y);
             v[k].w *= r * bf16hi(g[k].y);
-            if (FP8 && threadIdx.x + k * kConsumers < n4)
-                am = fmaxf(am, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
         }
         if constexpr (FP8) {
-            am = consumer_max(am, red);
+            am *= r;
             sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
             // non-negative floats order like their bit patterns
             if (calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(calib), __float_as_int(am));
@@ -616,7 +640,8 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
             }
             am = fmaxf(am, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
         }
-        am = consumer_max(am, red);
+        float unused = 0.f;
+        consumer_sum_max(unused, am, red);
         sa = __fdiv_rn(fmaxf(am, 1e-12f), 448.0f);
         if (calib && threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(calib), __float_as_int(am));
         if (sa_static) {

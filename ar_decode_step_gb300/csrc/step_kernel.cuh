@@ -140,7 +140,7 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
         const float4 v = poll4(reinterpret_cast<const float4*>(src) + lane, w);
         const bool ok = !unset4(v);
         const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
-        const float r = 1.0f / sqrtf(ss / (float)kHeadDim + p.eps);
+        const float r = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
         const uint2 gb = *reinterpret_cast<const uint2*>(gamma + 4 * lane);
         const float a[4] = {v.x * r * bf16lo(gb.x), v.y * r * bf16hi(gb.x), v.z * r * bf16lo(gb.y),
                             v.w * r * bf16hi(gb.y)};
