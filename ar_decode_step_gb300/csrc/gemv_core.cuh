@@ -891,17 +891,21 @@ __device__ __forceinline__ bool consume(const Proj& j, const Ring& ring, int& it
     return true;
 }
 
-// load_xseg_smem + consume as a separate (not inlined) function: its
-// registers are allocated on their own, so the state the caller keeps across
-// phases cannot push the stage loop's activation registers into local memory.
+// load_xseg_smem + consume.  consume_call is the separate (not inlined)
+// function: its registers are allocated on their own, so the state the caller
+// keeps across phases cannot push the bf16 stage loop's activation registers
+// (up to 20 float4 per lane) into local memory.  The FP8 loop keeps only a
+// pointer to its activation bytes; there the call's register save and restore
+// cost more than they protect (FP8 1.65 -> 1.54 ms/frame inlined, while bf16
+// inlined spilled and lost), so proj_phase inlines consume_body for FP8.
 // Returns the advanced stage counter, or -1 if a wait ran out.
 // `xplain`: bf16 weights only, a plain activation vector read from global
 // memory directly (then xs is not used); else the shared planes in xs.
 template <bool FP8, int EPI>
-__device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, const unsigned char* xs, float sa,
-                                        float* part, volatile int* abort, int* err, unsigned long long* wait_ns,
-                                        const EpiOut* so, unsigned long long* stage_tr, int stage_tr_n,
-                                        const float* xplain = nullptr, const Poll* poll = nullptr) {
+__device__ __forceinline__ int consume_body(const Proj& j, const Ring& ring, int it, const unsigned char* xs, float sa,
+                                            float* part, volatile int* abort, int* err, unsigned long long* wait_ns,
+                                            const EpiOut* so, unsigned long long* stage_tr, int stage_tr_n,
+                                            const float* xplain, const Poll* poll) {
     int rslot, sg, c0, c1;
     proj_segment(j, threadIdx.x >> 5, rslot, sg, c0, c1);
     XSeg<FP8> xr;
@@ -913,6 +917,29 @@ __device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, 
         load_xseg_smem<true>(xs, proj_cpr(j), c0, c1, xr);
     }
     return consume<FP8, EPI>(j, ring, it, xr, sa, part, abort, err, wait_ns, so, stage_tr, stage_tr_n) ? it : -1;
+}
+template <bool FP8, int EPI>
+__device__ __noinline__ int consume_call(const Proj j, const Ring ring, int it, const unsigned char* xs, float sa,
+                                        float* part, volatile int* abort, int* err, unsigned long long* wait_ns,
+                                        const EpiOut* so, unsigned long long* stage_tr, int stage_tr_n,
+                                        const float* xplain = nullptr, const Poll* poll = nullptr) {
+    return consume_body<FP8, EPI>(j, ring, it, xs, sa, part, abort, err, wait_ns, so, stage_tr, stage_tr_n, xplain,
+                                  poll);
+}
+// The stage loop and epilogue as proj_phase runs them: inlined for FP8, a
+// call for bf16 (see above).
+template <bool FP8, int EPI>
+__device__ __forceinline__ int consume_phase(const Proj& j, const Ring& ring, int it, const unsigned char* xs,
+                                             float sa, float* part, volatile int* abort, int* err,
+                                             unsigned long long* wait_ns, const EpiOut* so,
+                                             unsigned long long* stage_tr, int stage_tr_n,
+                                             const float* xplain = nullptr, const Poll* poll = nullptr) {
+    if constexpr (FP8)
+        return consume_body<FP8, EPI>(j, ring, it, xs, sa, part, abort, err, wait_ns, so, stage_tr, stage_tr_n,
+                                      xplain, poll);
+    else
+        return consume_call<FP8, EPI>(j, ring, it, xs, sa, part, abort, err, wait_ns, so, stage_tr, stage_tr_n,
+                                      xplain, poll);
 }
 
 // Philox4x32-10 counter-based generator (Salmon, Moraes, Dror and Shaw,

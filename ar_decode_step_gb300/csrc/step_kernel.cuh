@@ -501,17 +501,18 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
     if constexpr (KIND == 4) trace_mark<TRACE>(p, 1 + 14 * p.n_layers);
     else trace_mark<TRACE>(p, ev);
 
-    // the stage loop and epilogue in a function of their own (consume_call):
-    // allocated apart from the staging code above, it keeps the activation
-    // segment and the loop state in registers.  Traced launches also record
-    // the consumers' data waits and CTA 0's per-stage times.
+    // the stage loop and epilogue (consume_phase: for bf16 a function of its
+    // own, allocated apart from the staging code above, so that it keeps the
+    // activation segment and the loop state in registers; inlined for FP8).
+    // Traced launches also record the consumers' data waits and CTA 0's
+    // per-stage times.
     unsigned long long* cw = TRACE && cs.cwait && KIND < 4 ? cs.cwait + 4 * l + KIND : nullptr;
     unsigned long long* str = TRACE ? cs.cstr : nullptr;
     const int str_n = TRACE ? cs.cstr_n : 0;
     if constexpr (KIND == 1 || KIND == 3) {
         // residual add on this CTA's rows of h (kept in shared memory)
         const EpiOut so{s_hrows, xch_vec(p, l, KIND == 1 ? kXHo : kXHd)};
-        it = consume_call<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n,
+        it = consume_phase<FP8, kEpiResid>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n,
                                           FP8 ? nullptr : x, &w);
         if constexpr (TRACE && KIND == 3) {
             // layer-level checks: this CTA's rows of the residual stream after the layer
@@ -521,12 +522,12 @@ __device__ __noinline__ int proj_phase(const StepParams& p, const CtaState& cs, 
         }
     } else if constexpr (KIND == 2) {
         const EpiOut so{nullptr, xch_vec(p, l, kXAct)};
-        it = consume_call<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n);
+        it = consume_phase<FP8, kEpiSwiglu>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n);
     } else if constexpr (KIND == 0) {
         const EpiOut so{nullptr, xch_vec(p, l, kXQkv)};
-        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n);
+        it = consume_phase<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, &so, str, str_n);
     } else {
-        it = consume_call<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, nullptr, str,
+        it = consume_phase<FP8, kEpiStore>(j, m.ring, it, m.xs, sa, m.part, abort, &p.st->err, cw, nullptr, str,
                                           str_n);
     }
     const bool ok = it >= 0;
