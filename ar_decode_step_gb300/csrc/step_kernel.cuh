@@ -556,11 +556,11 @@ __device__ __forceinline__ int proj_phase(const StepParams& p, const CtaState& c
 }
 
 // This CTA's attention unit of layer l (CTAs without one only announce that
-// they are done).  Not inlined.  Returns the advanced stage counter, or -1 if
-// a wait ran out or the launch is aborting (every consumer thread alike).
+// they are done).  Returns the advanced stage counter, or -1 if a wait ran
+// out or the launch is aborting (every consumer thread alike).
 template <int G, bool TRACE>
-__device__ __noinline__ int attn_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l, int it,
-                                       int* s_last, volatile int* abort) {
+__device__ __forceinline__ int attn_phase_body(const StepParams& p, const CtaState& cs, unsigned char* smem, int l,
+                                               int it, int* s_last, volatile int* abort) {
     if ((int)blockIdx.x < cs.nunits) {
         const Poll w = step_poll(p, abort);
         if (!xch_wait(xch_counter(p, l, kXQkv), gridDim.x, w)) return -1;
@@ -573,6 +573,23 @@ __device__ __noinline__ int attn_phase(const StepParams& p, const CtaState& cs, 
     // complete only once every kv head's output is stored
     xch_publish(xch_counter(p, l, kXAttn));
     return it;
+}
+
+template <int G, bool TRACE>
+__device__ __noinline__ int attn_phase_call(const StepParams& p, const CtaState& cs, unsigned char* smem, int l,
+                                            int it, int* s_last, volatile int* abort) {
+    return attn_phase_body<G, TRACE>(p, cs, smem, l, it, s_last, abort);
+}
+// The attention phase as the step kernel runs it: inlined in the FP8 kernel
+// (FP8 1.530 -> 1.503 ms/frame), a call of its own in the bf16 one (inlined,
+// the bf16 step measured no better at its headline workload).
+template <bool FP8, int G, bool TRACE>
+__device__ __forceinline__ int attn_phase(const StepParams& p, const CtaState& cs, unsigned char* smem, int l, int it,
+                                          int* s_last, volatile int* abort) {
+    if constexpr (FP8)
+        return attn_phase_body<G, TRACE>(p, cs, smem, l, it, s_last, abort);
+    else
+        return attn_phase_call<G, TRACE>(p, cs, smem, l, it, s_last, abort);
 }
 
 template <int PREC, int G, bool TRACE>
@@ -823,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         const int ev = 1 + 14 * l;
         if ((it = proj_phase<FP8, 0, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
         trace_mark<TRACE>(p, ev + 2);
-        if ((it = attn_phase<G, TRACE>(s_p, s_cs, smem, l, it, &s_last, &s_abort)) < 0) return;
+        if ((it = attn_phase<FP8, G, TRACE>(s_p, s_cs, smem, l, it, &s_last, &s_abort)) < 0) return;
         trace_mark<TRACE>(p, ev + 3);
         trace_mark<TRACE>(p, ev + 4);
         if ((it = proj_phase<FP8, 1, TRACE>(s_p, s_cs, smem, l, it, red, &s_abort, s_hrows)) < 0) return;
