@@ -550,8 +550,9 @@ __device__ __forceinline__ void load_xseg_plain(const float* x, int c0, int c1, 
 // projection with inner dimension K into the shared layout of stage_x,
 // waiting for its elements:
 //   RMS:   x = h * r * gamma, r = 1/sqrt(sum(h^2)/K + eps)   (K <= kMaxRmsK)
-//   FP8:   sa = max(amax, 1e-12)/448, amax over the (normalised) values, or
-//          the site's static scale when one is set; x8 = e4m3(x/sa) as bytes
+//   FP8:   sa = max(amax, 1e-12)/448, amax over the (normalised) values (for
+//          RMS inputs r * max |h * gamma|, reduced with the sum), or the
+//          site's static scale when one is set; x8 = e4m3(x/sa) as bytes
 // (plain bf16 inputs are not staged: the stage loop reads them itself).
 // Every thread waits for its own elements, then the CTA reduces the
 // statistics in a fixed order.  Plain FP8 inputs go through xf, an fp32

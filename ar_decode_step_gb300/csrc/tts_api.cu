@@ -503,8 +503,9 @@ int init_impl(tts_ctx* c, const tts_config* cfg, const tts_weights* w) {
     // persistent kernel; prompts position by position through the decode step
     c->persistent = (k.options & TTS_OPT_SEPARATE_KERNELS) == 0;
     c->batched_prefill = (k.options & TTS_OPT_PREFILL_STEPS) == 0;
-    // the persistent kernel keeps a normalised activation in registers while
-    // its statistics arrive: longer hidden sizes take the graph of kernels
+    // the persistent kernel stages a normalised activation from registers
+    // (hidden <= kMaxRmsK) and plain ones through shared memory (<= kMaxPlainK):
+    // larger models take the graph of kernels
     if (c->cfg.hidden > kMaxRmsK || c->attn_dim > kMaxPlainK || c->cfg.inter > kMaxPlainK) c->persistent = false;
     if (c->persistent) TTS_TRY(setup_persistent(c));
     TTS_TRY(push_state(c, bos_state(c, 0, 0, -1)));
