@@ -227,15 +227,16 @@ struct StepParams {
 // embedding; then per layer l, from hidden + l * step_xch_layer_words: qkv
 // [qkv_rows], attention output [attn_dim], h after the attention [hidden],
 // MLP activation [inter], h after the MLP [hidden]; then the counters
-// (unsigned): last-arriver tickets of the attention [n_layers][n_kv] and of
-// the head [1], then the arrival counters of the vectors: the embedding [1],
-// then per layer the five vectors in the order above [n_layers][5].
+// (unsigned): last-arriver tickets of the attention [n_layers][n_q] (one per
+// unit slot: kv head, or q head) and of the head [1], then the arrival
+// counters of the vectors: the embedding [1], then per layer the five vectors
+// in the order above [n_layers][5].
 __host__ __device__ inline size_t step_xch_layer_words(int hidden, int qkv_rows, int attn_dim, int inter) {
     return (size_t)qkv_rows + attn_dim + 2 * (size_t)hidden + inter;
 }
-inline size_t step_xch_words(int n_layers, int hidden, int qkv_rows, int attn_dim, int inter, int n_kv) {
+inline size_t step_xch_words(int n_layers, int hidden, int qkv_rows, int attn_dim, int inter) {
     return (size_t)hidden + (size_t)n_layers * step_xch_layer_words(hidden, qkv_rows, attn_dim, inter) +
-           (size_t)n_layers * n_kv + 1 + 1 + 5 * (size_t)n_layers;
+           (size_t)n_layers * (attn_dim / 128) + 1 + 1 + 5 * (size_t)n_layers;
 }
 
 // Phase-trace layout of the persistent kernel, per CTA (see step.cu):

@@ -59,14 +59,15 @@ __device__ __forceinline__ float* xch_vec(const StepParams& p, int l, int kind) 
         default: return b + QKVR + A + p.hidden + p.inter;
     }
 }
-// The last-arriver tickets: attention of (layer l, kv head g) at l * n_kv + g,
-// the head at n_layers * n_kv.  Each starts the launch at kUnset.
+// The last-arriver tickets: attention of (layer l, unit slot u) at
+// l * n_q + u (u: the kv head, or the q head when a unit serves one q head),
+// the head at n_layers * n_q.  Each starts the launch at kUnset.
 __device__ __forceinline__ unsigned* xch_tickets(const StepParams& p) {
     return reinterpret_cast<unsigned*>(xch_vec(p, p.n_layers, kXQkv));
 }
 // The arrival counter of vector `kind` of layer l (l = -1: the embedding).
 __device__ __forceinline__ unsigned* xch_counter(const StepParams& p, int l, int kind) {
-    return xch_tickets(p) + p.n_layers * p.n_kv + 1 + (l < 0 ? 0 : 1 + 5 * l + kind);
+    return xch_tickets(p) + p.n_layers * p.n_q + 1 + (l < 0 ? 0 : 1 + 5 * l + kind);
 }
 __device__ __forceinline__ Poll step_poll(const StepParams& p, volatile int* abort) {
     return Poll{&p.st->err, abort, p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs};
@@ -113,8 +114,8 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[kAttnStep]) {
 // consumer thread alike) if a wait ran out or the launch is aborting.
 template <int G, bool TRACE>
 __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLayer& L, int layer, int pos, int g,
-                                               int split, int nsplit, int chunk, unsigned char* scratch, int* s_last,
-                                               const Poll& w) {
+                                               int q0, bool write_kv, int split, int nsplit, int chunk,
+                                               unsigned char* scratch, int* s_last, const Poll& w) {
     auto mark = [&](int k) {  // traced launches: the unit's progress
         if constexpr (TRACE)
             if (threadIdx.x == 0)
@@ -180,12 +181,14 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
     };
     load_k(t0 + kAttnStep * warp);
     load_v(t0 + kAttnStep * warp);
-    if (warp < G) norm_rope(qkv + (size_t)(g * G + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
+    if (warp < G) norm_rope(qkv + (size_t)(q0 + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
     if (has_new && warp == G) {
         const bool okk = norm_rope(qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
         const float4 v4 = poll4(reinterpret_cast<const float4*>(qkv + (size_t)(p.n_q + p.n_kv + g) * kHeadDim) + lane, w);
         const bool okv = !unset4(v4);
-        const bool store = __all_sync(0xffffffffu, okk && okv);  // a row that never arrived is not cached
+        // a row that never arrived is not cached; of the units sharing a kv
+        // head, one writes it (the others use their own identical copy)
+        const bool store = __all_sync(0xffffffffu, okk && okv) && write_kv;
         __syncwarp();
         const float vf[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
@@ -283,8 +286,9 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
     if (consumer_sync_or(*w.abort)) return false;
 
     // merge the warps; a single split writes the output directly
-    float* po = p.part_o + (((size_t)g * p.S + split) * G) * kHeadDim;
-    float* pml = p.part_ml + (((size_t)g * p.S + split) * G) * 2;
+    const int u = q0 / G;  // the unit's slot: kv head g (G = the group), or q head q0 (G = 1)
+    float* po = p.part_o + (((size_t)u * p.S + split) * G) * kHeadDim;
+    float* pml = p.part_ml + (((size_t)u * p.S + split) * G) * 2;
     for (int idx = threadIdx.x; idx < G * kHeadDim; idx += kConsumers) {
         const int jj = idx / kHeadDim, d = idx % kHeadDim;
         float M = -INFINITY;
@@ -296,7 +300,7 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
             O += sm.wo[w2][jj][d] * c;
         }
         if (nsplit == 1) {
-            st_relaxed(out + (size_t)(g * G + jj) * kHeadDim + d, O / Ls);
+            st_relaxed(out + (size_t)(q0 + jj) * kHeadDim + d, O / Ls);
         } else {
             po[idx] = O;
             if (d == 0) { pml[2 * jj] = M; pml[2 * jj + 1] = Ls; }
@@ -320,7 +324,7 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
         unsigned old;
         asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                      : "=r"(old)
-                     : "l"(xch_tickets(p) + layer * p.n_kv + g)
+                     : "l"(xch_tickets(p) + layer * p.n_q + u)
                      : "memory");
         *s_last = old + 1u == (unsigned)(nsplit - 1);
     }
@@ -331,8 +335,8 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
         // (idx = threadIdx.x + 256 e) into registers, kMergeBatch splits at a time
         constexpr int kMergeBatch = 20;
         constexpr int kEntries = (G * kHeadDim + kConsumers - 1) / kConsumers;
-        const float* po0 = p.part_o + ((size_t)g * p.S * G) * kHeadDim;
-        const float* pml0 = p.part_ml + ((size_t)g * p.S * G) * 2;
+        const float* po0 = p.part_o + ((size_t)u * p.S * G) * kHeadDim;
+        const float* pml0 = p.part_ml + ((size_t)u * p.S * G) * 2;
         float* mlw = &sm.wo[0][0][0];  // reuse: [nsplit][G][2] pairs, then [nsplit][G] weights
         float pv[kEntries][kMergeBatch];
         auto load_po = [&](int s0) {
@@ -380,7 +384,7 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
             const int idx = threadIdx.x + kConsumers * e;
             if (idx < G * kHeadDim) {
                 const int jj = idx / kHeadDim, d = idx % kHeadDim;
-                st_relaxed(out + (size_t)(g * G + jj) * kHeadDim + d, acc[e] / lsum[jj]);
+                st_relaxed(out + (size_t)(q0 + jj) * kHeadDim + d, acc[e] / lsum[jj]);
             }
         }
     }
@@ -394,7 +398,8 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
 // them in registers across the step.
 struct CtaState {
     int pos, nsplit, chunk, nunits;
-    int unit_g, unit_split;        // this CTA's attention unit (kv head, split), if blockIdx.x < nunits
+    int qsub;                      // attention units per kv head and split: 1 (all G q heads) or G (one each)
+    int unit_g, unit_j, unit_split;  // this CTA's attention unit (kv head, q head within it, split), if any
     int rows[5][2];                // this CTA's output rows per projection kind
     unsigned long long* cwait;     // traced runs: consumer wait per projection (thread 0), else null
     unsigned long long* cstr;      // traced runs: this CTA's per-stage trace, else null
@@ -565,9 +570,14 @@ __device__ __forceinline__ int attn_phase_body(const StepParams& p, const CtaSta
         const Poll w = step_poll(p, abort);
         if (!xch_wait(xch_counter(p, l, kXQkv), gridDim.x, w)) return -1;
         const StepSmem m = step_smem(smem, p);
-        if (!attention_unit<G, TRACE>(p, m.sl[l], l, cs.pos, cs.unit_g, cs.unit_split,
-                                      cs.nsplit, cs.chunk, m.xs, s_last, w))
-            return -1;
+        bool ok;
+        if (G > 1 && cs.qsub > 1)
+            ok = attention_unit<1, TRACE>(p, m.sl[l], l, cs.pos, cs.unit_g, cs.unit_g * G + cs.unit_j,
+                                          cs.unit_j == 0, cs.unit_split, cs.nsplit, cs.chunk, m.xs, s_last, w);
+        else
+            ok = attention_unit<G, TRACE>(p, m.sl[l], l, cs.pos, cs.unit_g, cs.unit_g * G, true, cs.unit_split,
+                                          cs.nsplit, cs.chunk, m.xs, s_last, w);
+        if (!ok) return -1;
     }
     // after its merge, if this unit merged: every CTA counts, so the count is
     // complete only once every kv head's output is stored
@@ -640,9 +650,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         if (chunk < kAttnMinChunk) chunk = kAttnMinChunk;
         s_cs.chunk = chunk;
         s_cs.nsplit = (len + chunk - 1) / chunk;
-        s_cs.nunits = p.n_kv * s_cs.nsplit;
-        s_cs.unit_g = blockIdx.x / s_cs.nsplit;
+        // short contexts leave most CTAs without a unit: then each q head of
+        // a kv head gets a unit of its own (the units of one kv head read the
+        // same cached rows; one of them writes the new row)
+        s_cs.qsub = (G > 1 && p.n_kv * G * s_cs.nsplit <= (int)gridDim.x) ? G : 1;
+        s_cs.nunits = p.n_kv * s_cs.qsub * s_cs.nsplit;
+        const int uq = blockIdx.x / s_cs.nsplit;  // (kv head, q head within it)
         s_cs.unit_split = blockIdx.x % s_cs.nsplit;
+        s_cs.unit_g = uq / s_cs.qsub;
+        s_cs.unit_j = uq % s_cs.qsub;
         s_cs.cwait = TRACE ? p.trace + (size_t)blockIdx.x * p.trace_stride + 8 + 19 * p.n_layers : nullptr;
         s_cs.cstr = (TRACE && p.stage_trace && blockIdx.x == 0) ? p.stage_trace : nullptr;
         s_cs.cstr_n = p.stage_trace_stride / 4;
@@ -852,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     }
     if (p.decode) {
         if ((it = proj_phase<FP8, 4, TRACE>(s_p, s_cs, smem, 0, it, red, &s_abort, s_hrows)) < 0) return;
-        head_tail(p.logits, p.n_cb, p.cb_vocab, p.st, xch_tickets(p) + p.n_layers * p.n_kv, kUnset, p.hist,
+        head_tail(p.logits, p.n_cb, p.cb_vocab, p.st, xch_tickets(p) + p.n_layers * p.n_q, kUnset, p.hist,
                   p.hist_cap, &s_last, s_codes);
         trace_mark<TRACE>(p, 1 + 14 * p.n_layers + 2);
     }

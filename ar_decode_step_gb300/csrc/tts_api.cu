@@ -386,7 +386,7 @@ int setup_persistent(tts_ctx* c) {
     }
     TTS_TRY(dalloc(c, &c->d_layers, (size_t)k.n_layers));
     TTS_CK(cudaMemcpy(c->d_layers, layers.data(), layers.size() * sizeof(StepLayer), cudaMemcpyHostToDevice));
-    c->xch_bytes = 4 * step_xch_words(k.n_layers, H, c->qkv_rows, A, I, k.n_kv_heads);
+    c->xch_bytes = 4 * step_xch_words(k.n_layers, H, c->qkv_rows, A, I);
     TTS_TRY(dalloc(c, &c->xch, c->xch_bytes / 4));
     p.fp8_sa = nullptr;
     p.fp8_calib = nullptr;
