@@ -138,18 +138,22 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
     // 4l..4l+3; its rotation partner dims (+-64) sit in lane l^16.  Returns
     // whether the lane's row elements arrived.
     auto norm_rope = [&](const float* src, const __nv_bfloat16* gamma, float* dst, float post) {
+        // the gains and this position's (cos, sin) pairs do not depend on the
+        // exchanged row: their loads go out before the wait for it
+        const uint2 gb = *reinterpret_cast<const uint2*>(gamma + 4 * lane);
+        const float4 cs01 = *reinterpret_cast<const float4*>(rope + ((4 * lane) & 63));
+        const float4 cs23 = *reinterpret_cast<const float4*>(rope + ((4 * lane) & 63) + 2);
         const float4 v = poll4(reinterpret_cast<const float4*>(src) + lane, w);
         const bool ok = !unset4(v);
         const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
         const float r = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-        const uint2 gb = *reinterpret_cast<const uint2*>(gamma + 4 * lane);
         const float a[4] = {v.x * r * bf16lo(gb.x), v.y * r * bf16hi(gb.x), v.z * r * bf16lo(gb.y),
                             v.w * r * bf16hi(gb.y)};
+        const float c[4] = {cs01.x, cs01.z, cs23.x, cs23.z}, sn[4] = {cs01.y, cs01.w, cs23.y, cs23.w};
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const float partner = __shfl_xor_sync(0xffffffffu, a[jj], 16);
-            const float2 cs = rope[(4 * lane + jj) & 63];
-            dst[4 * lane + jj] = (lane < 16 ? a[jj] * cs.x - partner * cs.y : a[jj] * cs.x + partner * cs.y) * post;
+            dst[4 * lane + jj] = (lane < 16 ? a[jj] * c[jj] - partner * sn[jj] : a[jj] * c[jj] + partner * sn[jj]) * post;
         }
         return ok;
     };
