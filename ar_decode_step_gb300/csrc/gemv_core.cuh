@@ -80,6 +80,15 @@ __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t e4m3_byte(float x) {
     return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
+// x / sa for the four elements of v as E4M3 bytes, v.x in the lowest byte
+// (pairs converted by one instruction each, same rounding as e4m3_byte).
+__device__ __forceinline__ uint32_t e4m3x4_div(const float4 v, float sa, float rsa) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(div_rn_by(v.x, sa, rsa), div_rn_by(v.y, sa, rsa)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(div_rn_by(v.z, sa, rsa), div_rn_by(v.w, sa, rsa)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
@@ -469,8 +478,7 @@ __device__ __forceinline__ float stage_x(const float* x, const __nv_bfloat16* ga
         uint32_t* xs4 = reinterpret_cast<uint32_t*>(xs);  // E4M3 bytes, in order
         for (int i = threadIdx.x; i < K / 4; i += kConsumers) {
             const float4 v = load(i);
-            xs4[i] = e4m3_byte(div_rn_by(v.x, sa, rsa)) | (e4m3_byte(div_rn_by(v.y, sa, rsa)) << 8) |
-                     (e4m3_byte(div_rn_by(v.z, sa, rsa)) << 16) | (e4m3_byte(div_rn_by(v.w, sa, rsa)) << 24);
+            xs4[i] = e4m3x4_div(v, sa, rsa);
         }
     }
     consumer_sync();
@@ -623,8 +631,7 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
                     reinterpret_cast<float4*>(xs)[((e & 7) >> 2) * cpr + (e >> 3)] = v[k];
                 } else {
                     reinterpret_cast<uint32_t*>(xs)[i] =
-                        e4m3_byte(div_rn_by(v[k].x, sa, rsa)) | (e4m3_byte(div_rn_by(v[k].y, sa, rsa)) << 8) |
-                        (e4m3_byte(div_rn_by(v[k].z, sa, rsa)) << 16) | (e4m3_byte(div_rn_by(v[k].w, sa, rsa)) << 24);
+                        e4m3x4_div(v[k], sa, rsa);
                 }
             }
         }
@@ -654,8 +661,7 @@ __device__ float stage_x_xch(const float* x, const __nv_bfloat16* gamma, int K, 
         for (int i = threadIdx.x; i < n4; i += kConsumers) {
             const float4 v = reinterpret_cast<const float4*>(xf)[i];
             reinterpret_cast<uint32_t*>(xs)[i] =
-                e4m3_byte(div_rn_by(v.x, sa, rsa)) | (e4m3_byte(div_rn_by(v.y, sa, rsa)) << 8) |
-                (e4m3_byte(div_rn_by(v.z, sa, rsa)) << 16) | (e4m3_byte(div_rn_by(v.w, sa, rsa)) << 24);
+                e4m3x4_div(v, sa, rsa);
         }
     }
     return consumer_sync_or(*w.abort) ? -1.0f : sa;
