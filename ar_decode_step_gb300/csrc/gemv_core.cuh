@@ -327,8 +327,10 @@ struct Ring {
 
 // floor(2^32 / ns) + 1 for a ring of ns >= 2 slots (every ring here has at
 // least two): it / ns = __umulhi(it, ring_magic(ns)) exactly for every
-// it < 2^32 / ns (the error term stays below 1 / ns), which saves the
-// consumers a run-time division at every phase start.
+// it < 2^32 / ns (the error term stays below 1 / ns; division by an
+// invariant integer through a multiply-high, as in Granlund and Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994), which
+// saves the consumers a run-time division at every phase start.
 __host__ __device__ inline uint32_t ring_magic(int ns) { return 0xffffffffu / (uint32_t)ns + 1u; }
 // Slot and phase parity of ring stage `it`.
 __device__ __forceinline__ void ring_pos(const Ring& r, int it, int& slot, uint32_t& phase) {
