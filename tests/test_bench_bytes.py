@@ -27,3 +27,19 @@ def test_step_bytes_counts_every_array_once():
         for precision in (0, 1):
             assert bench.step_bytes(d, precision, ctx) == _arrays_bytes(w, precision) + embed_rows + kv
 
+
+
+def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    """bench.read_traffic scales a capture to n layers (fixed + n x per layer)
+    and refuses a record whose source digest is not the kernel's."""
+    import json
+    (tmp_path / "profiles").mkdir()
+    rec = {"source_digest": "abc", "method": "m",
+           "workloads": {"w": {"fixed": 1000.0, "per_layer": 10.0}}}
+    (tmp_path / "profiles" / "step_kernel_traffic.txt").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_digest", lambda: "abc")
+    assert bench.read_traffic("w", 36)[0] == 1000.0 + 36 * 10.0
+    assert bench.read_traffic("other", 36)[0] is None
+    monkeypatch.setattr(bench, "source_digest", lambda: "changed")
+    assert bench.read_traffic("w", 36)[0] is None
