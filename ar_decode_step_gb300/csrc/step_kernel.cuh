@@ -185,8 +185,13 @@ __device__ __forceinline__ bool attention_unit(const StepParams& p, const StepLa
     };
     load_k(t0 + kAttnStep * warp);
     load_v(t0 + kAttnStep * warp);
+    // warp w < G takes query head q0 + w; the new key/value row goes to the
+    // first warp without a query head, or to the last warp (after its query
+    // head) when the group fills every consumer warp
+    static_assert(G <= kConsumerWarps, "one consumer warp per query head of the group");
+    constexpr int kNewRowWarp = G < kConsumerWarps ? G : kConsumerWarps - 1;
     if (warp < G) norm_rope(qkv + (size_t)(q0 + warp) * kHeadDim, L.qn, sm.qs[warp], scale);
-    if (has_new && warp == G) {
+    if (has_new && warp == kNewRowWarp) {
         const bool okk = norm_rope(qkv + (size_t)(p.n_q + g) * kHeadDim, L.kn, sm.knew, 1.0f);
         const float4 v4 = poll4(reinterpret_cast<const float4*>(qkv + (size_t)(p.n_q + p.n_kv + g) * kHeadDim) + lane, w);
         const bool okv = !unset4(v4);

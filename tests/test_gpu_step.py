@@ -146,6 +146,42 @@ def test_one_layer_full_width(ads, t0):
     dec.close()
 
 
+@pytest.mark.parametrize("precision", [0, 1], ids=["bf16", "fp8"])
+def test_one_layer_full_width_attention_schedule_edges(ads, precision):
+    """One full-width layer decoding across the edges of the step kernel's
+    attention schedule (152 CTAs, 8 kv heads, splits of at least 64
+    positions over at most 19 splits per kv head), teacher-forced against the
+    oracle frame by frame, with the new K/V rows compared as well:
+    - 255 to 258 attended positions: at 256 the four q heads of a kv head
+      still get a unit each (4 splits of 64); at 257 a fifth split appears,
+      holding one position, and the units become one per (kv head, split);
+    - 1215 to 1220: the split length goes from 64 to 65 positions (19
+      splits, the last one ragged and not a multiple of the 8 positions a
+      warp scores at a time), and the last frame runs at the last cache
+      position, after which the cache is full."""
+    d = synth.Dims(n_layers=1)
+    max_pos = 1220
+    fp8 = precision == 1
+    w, dec, orc = make_pair(ads, d, max_pos, precision)
+    k, v = synth.make_kv_prefix(d, max_pos - 6, max_pos)
+    for prefix, frames, stream in ((254, 4, 31), (max_pos - 6, 6, 32)):
+        kd, vd = upload_kv(k, v, prefix)
+        dec.set_kv(kd, vd, prefix)
+        orc.set_kv(k, v, prefix)
+        codes = synth.random_codes(frames, seed=2, stream=stream)
+        stats = run_teacher_forced(dec, orc, codes, 8, fp8, f"context {prefix + 1}")
+        print(f"contexts {prefix + 1}..{prefix + frames}:", stats)
+        gk, gv = dec.get_kv(prefix, prefix + frames)
+        check_kv_rows(gk, orc.k[:, :, prefix:prefix + frames], f"K rows from {prefix}")
+        check_kv_rows(gv, orc.v[:, :, prefix:prefix + frames], f"V rows from {prefix}")
+    assert dec.state()[0] == max_pos
+    with pytest.raises(ads.TtsError) as e:
+        dec.decode_step(codes[-1])
+    assert e.value.status == -3
+    assert dec.state()[0] == max_pos
+    dec.close()
+
+
 def test_errors_leave_state_unchanged(ads):
     d = reduced_dims(1)
     w = synth.make_weights(d)
