@@ -79,7 +79,7 @@ def lib():
                 "or_attention": (None, [vp, vp, vp, i32, i32, i32, i32, i32, vp]),
                 "or_embed": (None, [vp, i32, i32, i32, vp, vp]),
                 "or_argmax": (i32, [vp, i32]),
-                "or_delay_code": (i32, [i32, i32, i32, i32]),
+                "or_delay_code": (i32, [i32, i32, i32, i32, i32]),
                 "or_philox4x32_10": (None, [vp, vp, vp]),
                 "or_sample_code": (i32, [vp, i32, dbl, ctypes.c_uint64, i32, i32, vp]),
                 "or_decode_step": (i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights),
@@ -209,8 +209,8 @@ def argmax(v: np.ndarray) -> int:
     return lib().or_argmax(_p(v), v.size)
 
 
-def delay_code(k: int, t: int, eoc: int, am: int) -> int:
-    return lib().or_delay_code(k, t, eoc, am)
+def delay_code(k: int, t: int, eoc: int, am: int, V: int = 1026) -> int:
+    return lib().or_delay_code(k, t, eoc, am, V)
 
 
 def philox4x32_10(ctr, key):

@@ -326,12 +326,14 @@ int or_sample_code(const double* logits, int V, double T, uint64_t seed, int t, 
 
 /* Delay pattern [FlashRT header "delay pattern"; FlashRT s5 "BOC/EOC";
  * SGLang arch]: codebook k runs k frames behind codebook 0.  At frame t,
- * codebook k has not started while t < k and emits BOS-pad (1024); once
- * codebook 0 has emitted EOC (1025) at frame eoc, codebook k emits EOC from
- * frame eoc + k on; otherwise it emits its argmax. */
-int or_delay_code(int k, int t, int eoc, int argmax_code) {
-    if (t < k) return 1024;
-    if (eoc >= 0 && t >= eoc + k) return 1025;
+ * codebook k has not started while t < k and emits BOS-pad; once codebook 0
+ * has emitted EOC at frame eoc, codebook k emits EOC from frame eoc + k on;
+ * otherwise it emits its argmax.  The pages' codebooks have 1026 entries:
+ * 1024 acoustic codes, then BOS-pad (1024) and EOC (1025).  For another
+ * vocabulary size V the last two entries take those roles (V - 2, V - 1). */
+int or_delay_code(int k, int t, int eoc, int argmax_code, int V) {
+    if (t < k) return V - 2;
+    if (eoc >= 0 && t >= eoc + k) return V - 1;
     return argmax_code;
 }
 
@@ -470,7 +472,7 @@ static void head_codes(const or_dims* d, const or_weights* w, const or_state* st
                 if (v != am && row[v] > second) second = row[v];
             gaps[k] = row[am] - second;
         }
-        codes_out[k] = or_delay_code(k, t, eoc, am);
+        codes_out[k] = or_delay_code(k, t, eoc, am, V);
     }
     if (logits) memcpy(logits, lg, sizeof(double) * (size_t)C * V);
     free(f);
@@ -503,7 +505,7 @@ int or_decode_step(const or_dims* d, const or_weights* w, or_state* st,
     or_embed(w->embed, C, V, H, codes_in, h);
     layer_stack(d, w, st, st->pos, h, 0);
     head_codes(d, w, st, h, codes_out, logits, gaps);
-    if (st->eoc < 0 && codes_out[0] == 1025) st->eoc = st->t;
+    if (st->eoc < 0 && codes_out[0] == V - 1) st->eoc = st->t;
     st->pos += 1;
     st->t += 1;
     free(h);

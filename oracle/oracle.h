@@ -101,7 +101,7 @@ void   or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t o
  * distance of u * total from the nearest running sum, relative to the total
  * (how far the draw is from flipping to a neighbouring code). */
 int    or_sample_code(const double* logits, int V, double T, uint64_t seed, int t, int k, double* margin);
-int    or_delay_code(int k, int t, int eoc, int argmax_code);
+int    or_delay_code(int k, int t, int eoc, int argmax_code, int V);
 
 /* ---- the step ---- */
 /* One decode step at st->pos, frame st->t.  Writes K/V at st->pos, fills

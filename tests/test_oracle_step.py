@@ -5,6 +5,8 @@ written here with torch library routines (F.rms_norm, matmul,
 scaled_dot_product_attention, F.silu, torch's own bf16/e4m3 casts).  The two
 share no code; a mis-wired residual, a norm gain on the wrong vector, a
 transposed head or a wrong KV write position fails these tests.  No GPU."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -119,16 +121,17 @@ class TorchRestatement:
         f = F.rms_norm(h, (d.hidden,), self.fn, d.rms_eps)
         logits = (self.head @ f).view(d.n_cb, d.cb_vocab)
         out = []
+        bos, eoc_code = d.cb_vocab - 2, d.cb_vocab - 1  # 1024 and 1025 for the 1026-entry codebooks
         for k in range(d.n_cb):
             am = int(torch.argmax(logits[k]))
             if self.t < k:
-                c = 1024
+                c = bos
             elif self.eoc >= 0 and self.t >= self.eoc + k:
-                c = 1025
+                c = eoc_code
             else:
                 c = am
             out.append(c)
-        if self.eoc < 0 and out[0] == 1025:
+        if self.eoc < 0 and out[0] == eoc_code:
             self.eoc = self.t
         self.pos += 1
         self.t += 1
@@ -157,6 +160,38 @@ def test_tiny_step_matches_torch_restatement(fp8):
         assert np.array_equal(out[live], rout[live]), f
         cin = out
     assert orc.pos == 12
+
+
+def test_other_vocabulary_bos_eoc_and_forced_eoc():
+    """4 codebooks of 40 entries: BOS-pad and EOC are the last two entries
+    (38, 39), as 1024 and 1025 are of the pages' 1026.  Codebook 0's head rows
+    are zero except its EOC row, set to the sign pattern of frame 0's
+    normalised final stream, so codebook 0 emits EOC at frame 0; the delay
+    mask then fixes every code of frames 0..4, which both the oracle and the
+    torch restatement must produce."""
+    d = synth.Dims(n_layers=2, hidden=64, n_q=4, n_kv=2, head_dim=16, inter=96, n_cb=4, cb_vocab=40)
+    w = synth.make_weights(d, std=0.1, gamma_variant=True)
+    V = d.cb_vocab
+    codes = np.random.default_rng(4).integers(0, V - 2, (5, d.n_cb)).astype(np.int32)
+    probe = TorchRestatement(w, MAXPOS)
+    h0 = probe.layers(codes[0])[-1]
+    f0 = F.rms_norm(h0, (d.hidden,), probe.fn, d.rms_eps)
+    head = w.head.copy()
+    head[:V] = 0
+    head[V - 1] = np.where(f0.numpy() >= 0, 0x3F80, 0xBF80).astype(np.uint16)  # bf16 +1 / -1
+    w = dataclasses.replace(w, head=head)
+    orc = oracle.Oracle(w, MAXPOS)
+    ref = TorchRestatement(w, MAXPOS)
+    want = [[V - 1] + [V - 1 if t >= k else V - 2 for k in range(1, d.n_cb)] for t in range(5)]
+    for t in range(5):
+        out, logits, _ = orc.decode_step(codes[t])
+        rout, rlogits = ref.step(codes[t])
+        assert np.allclose(logits, rlogits, rtol=1e-9, atol=1e-9), t
+        assert out.tolist() == want[t] == rout.tolist(), (t, out, rout)
+    assert orc.st.eoc == ref.eoc == 0
+    # the un-forced path: without the EOC row, codes are the argmax, in [0, V)
+    assert all(oracle.delay_code(k, 9, -1, 7, V) == 7 for k in range(d.n_cb))
+    assert oracle.delay_code(3, 2, -1, 7, V) == V - 2 and oracle.delay_code(3, 5, 2, 7, V) == V - 1
 
 
 def test_tiny_step_with_kv_prefix_and_kv_contents():
