@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import adopt_gpu_cache, check_frame, check_kv_rows, reduced_dims, to_binding_dims, upload_kv
+from helpers import (BF16_COS, FP8_COS, adopt_gpu_cache, check_frame, check_kv_rows, cosine, reduced_dims,
+                     to_binding_dims, upload_kv)
 
 pytestmark = pytest.mark.gpu
 
@@ -179,6 +180,57 @@ def test_one_layer_full_width_attention_schedule_edges(ads, precision):
         dec.decode_step(codes[-1])
     assert e.value.status == -3
     assert dec.state()[0] == max_pos
+    dec.close()
+
+
+@pytest.mark.parametrize("precision", [0, 1], ids=["bf16", "fp8"])
+def test_device_loop_input_hidden_trace_and_gemv_timing(ads, precision):
+    """The calls around the device loop, each checked against the oracle:
+    - tts_set_input then one device-loop frame (tts_decode_steps) is the
+      teacher-forced frame for those codes;
+    - tts_get_hidden returns that frame's residual stream after the last
+      layer (the oracle's embedding and layers composed at the same position);
+    - a traced frame (tts_trace_step: the phase-stamping variant of the step
+      kernel) computes the same frame: its logits meet the frame bar and
+      every CTA stamped its start;
+    - timing each projection as separate launches (tts_time_gemv) leaves the
+      decode state usable: the next frame still meets the bar."""
+    fp8 = precision == 1
+    d = reduced_dims(2)
+    max_pos = 64
+    w, dec, orc = make_pair(ads, d, max_pos, precision, gamma_variant=True)
+    k, v = synth.make_kv_prefix(d, 30, max_pos)
+    kd, vd = upload_kv(k, v, 30)
+    dec.set_kv(kd, vd, 30)
+    orc.set_kv(k, v, 30)
+    dec.set_frame(8)
+    orc.set_frame(8)
+    codes = synth.random_codes(4, seed=2, stream=61)
+    # set_input + one device-loop frame; the oracle's final residual stream
+    pos = orc.pos
+    h = orc.embed(codes[0])
+    for l in range(d.n_layers):
+        h = orc.layer(l, pos, h)
+    dec.set_input(codes[0])
+    g = dec.decode_steps(1)[0]
+    o, ol, og = orc.decode_step(codes[0])
+    check_frame(g, dec.get_logits(), o, ol, og, fp8, 8, -1, "set_input + decode_steps")
+    hc = cosine(dec.get_hidden(), h)
+    assert hc >= (FP8_COS if fp8 else BF16_COS), f"hidden cos {hc}"
+    # a traced frame
+    dec.set_input(codes[1])
+    tr = dec.trace_step()
+    o, ol, og = orc.decode_step(codes[1])
+    lc = cosine(dec.get_logits(), ol)
+    assert lc >= (FP8_COS if fp8 else BF16_COS), f"traced frame cos {lc}"
+    assert tr.shape[1] == 8 + 31 * d.n_layers and (tr[:, 0] > 0).all()
+    assert dec.state() == (orc.pos, orc.st.t, orc.st.eoc)
+    # projection timings, then a frame
+    for kind in range(5):
+        assert dec.time_gemv(kind, 2) > 0.0
+    g = dec.decode_step(codes[2])
+    o, ol, og = orc.decode_step(codes[2])
+    check_frame(g, dec.get_logits(), o, ol, og, fp8, 10, -1, "after the projection timings")
     dec.close()
 
 

@@ -50,14 +50,14 @@ def check_kv(gpu_bits, oracle_bits, fp8: bool, where: str):
         assert c >= FP8_COS, f"{where}: layer {l}: cos {c}"
 
 
-def decode_segments(dec, orc, k, v, fp8: bool, where: str):
+def decode_segments(dec, orc, k, v, fp8: bool, where: str, n_cb: int = 8):
     """Teacher-forced frames from each SEGMENTS prefix; the new K/V rows are
     checked after each segment."""
     for prefix, stream in SEGMENTS:
         kd, vd = upload_kv(k, v, prefix)
         dec.set_kv(kd, vd, prefix)
         orc.set_kv(k, v, prefix)
-        codes = synth.random_codes(FRAMES, seed=2, stream=stream)
+        codes = synth.random_codes(FRAMES, n_cb=n_cb, seed=2, stream=stream)
         dec.set_frame(8)
         orc.set_frame(8)
         stats = []
@@ -94,6 +94,66 @@ def test_query_group_sizes(ads, n_q, n_kv, precision):
     check_kv(gv, orc.v[:, :, :24], fp8, f"{where}: prefill V")
     k, v = synth.make_kv_prefix(d, SEGMENTS[-1][0], MAX_POS)
     decode_segments(dec, orc, k, v, fp8, where)
+    dec.close()
+
+
+@pytest.mark.parametrize("precision", [0, 1], ids=["bf16", "fp8"])
+def test_codebook_count_and_vocabulary(ads, precision):
+    """4 codebooks of 2050 entries (BOS-pad 2048, EOC 2049) instead of 8 of
+    1026: the embedding gather, the head's rows, the per-codebook argmax and
+    the delay mask follow the configuration."""
+    fp8 = precision == 1
+    d = synth.Dims(n_layers=2, hidden=512, n_q=8, n_kv=2, head_dim=128, inter=1024, n_cb=4, cb_vocab=2050)
+    w = synth.make_weights(d, gamma_variant=True)
+    dw = ads.DeviceWeights(w, precision=precision)
+    dec = ads.Decoder(to_binding_dims(d), dw, MAX_POS)
+    orc = oracle.Oracle(w, MAX_POS, precision=precision)
+    k, v = synth.make_kv_prefix(d, SEGMENTS[-1][0], MAX_POS)
+    decode_segments(dec, orc, k, v, fp8, f"4 x 2050 codebooks, {'fp8' if fp8 else 'bf16'}", n_cb=4)
+    # frame 0 from the all-BOS input: codebooks 1..3 are forced to BOS-pad
+    dec.set_kv(*upload_kv(k, v, 40), 40)
+    orc.set_kv(k, v, 40)
+    dec.set_frame(0)
+    orc.set_frame(0)
+    bos = np.full(4, 2048, np.int32)
+    g = dec.decode_step(bos)
+    o, ol, og = orc.decode_step(bos)
+    check_frame(g, dec.get_logits(), o, ol, og, fp8, 0, -1, "4 x 2050, frame 0")
+    assert (g[1:] == 2048).all()
+    dec.close()
+
+
+@pytest.mark.parametrize("precision", [0, 1], ids=["bf16", "fp8"])
+def test_longest_context(ads, precision):
+    """The largest cache the library accepts (65536 positions): the last
+    three positions decoded against the oracle (64 splits of 1024 positions
+    per kv head), then the cache is full."""
+    fp8 = precision == 1
+    d = reduced_dims(2)
+    max_pos = 65536
+    w = synth.make_weights(d, gamma_variant=True)
+    dw = ads.DeviceWeights(w, precision=precision)
+    dec = ads.Decoder(to_binding_dims(d), dw, max_pos)
+    orc = oracle.Oracle(w, max_pos, precision=precision)
+    prefix = max_pos - FRAMES
+    k, v = synth.make_kv_prefix(d, prefix, max_pos)
+    kd, vd = upload_kv(k, v, prefix)
+    dec.set_kv(kd, vd, prefix)
+    orc.set_kv(k, v, prefix)
+    codes = synth.random_codes(FRAMES, seed=2, stream=53)
+    dec.set_frame(8)
+    orc.set_frame(8)
+    for f, cin in enumerate(codes):
+        g = dec.decode_step(cin)
+        o, ol, og = orc.decode_step(cin)
+        check_frame(g, dec.get_logits(), o, ol, og, fp8, 8 + f, -1, f"context {prefix + 1 + f}")
+    gk, gv = dec.get_kv(prefix, max_pos)
+    check_kv(gk, orc.k[:, :, prefix:], fp8, "K rows at the end of the cache")
+    check_kv(gv, orc.v[:, :, prefix:], fp8, "V rows at the end of the cache")
+    assert dec.state()[0] == max_pos
+    with pytest.raises(ads.TtsError) as e:
+        dec.decode_step(codes[-1])
+    assert e.value.status == -3
     dec.close()
 
 
