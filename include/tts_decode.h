@@ -191,8 +191,10 @@ int tts_set_input(tts_ctx* ctx, const int32_t* codes);
  * down projections of each layer; a site set to 0 keeps the per-token
  * (dynamic) scale; NULL makes every site dynamic again.  With a static scale
  * s, x quantises to e4m3(x / s), values beyond 448 s saturating.  Applies to
- * every later step.  TTS_ERR_UNSUPPORTED for BF16 contexts or without the
- * persistent step kernel; TTS_ERR_ARG for a negative or non-finite scale. */
+ * every later decode step (and to prompts prefilled position by position,
+ * TTS_OPT_PREFILL_STEPS); the batched prefill keeps per-token scales.
+ * TTS_ERR_UNSUPPORTED for BF16 contexts or without the persistent step
+ * kernel; TTS_ERR_ARG for a negative or non-finite scale. */
 int tts_set_fp8_scales(tts_ctx* ctx, const float* scales);
 
 /* FP8 calibration run: n_frames free-running decode frames from the current
