@@ -232,8 +232,10 @@ int tts_get_kv(tts_ctx* ctx, void* k_host, void* v_host, int p0, int p1);
 /* HOST fp32 [n_codebooks*cb_vocab]: the logits of the last decode step. */
 int tts_get_logits(tts_ctx* ctx, float* logits_host);
 
-/* HOST fp32 [hidden]: the residual stream after the last step or prefill
- * position (the input of the final RMSNorm). */
+/* HOST fp32 [hidden]: the residual stream after the last layer of the last
+ * decode step (the input of the final RMSNorm), or of the last prompt row
+ * of a position-by-position prefill; the batched prefill leaves it as it
+ * was. */
 int tts_get_hidden(tts_ctx* ctx, float* hidden_host);
 
 /* Set the frame index and the EOC frame (-1 = none) used by the delay mask. */
